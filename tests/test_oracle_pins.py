@@ -1,0 +1,550 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Witnesses used: PyTorch CPU eager bfloat16/float32 ops (a library), mpmath at
+50 digits, binary64 brute force, closed forms and invariants.  Nothing here
+touches a GPU or the CUDA library.  Each pin is chosen so that a plausible
+mistake in the oracle (a dropped term, a wrong sign or index, a missed or
+extra rounding point) fails it.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def bf(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+
+
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of bfloat16 numbers at |v| (2^(e-7)), floored at the subnormal step."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.maximum(np.exp2(e - 7), 2.0 ** -133)
+
+
+# ---------------------------------------------------------------- rounding
+
+
+def _torch_bf16_bits(f32_bits: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(f32_bits.view(np.float32).copy())
+    return u16(t.to(torch.bfloat16))
+
+
+def _check_rounding(orc, bits):
+    bits = np.ascontiguousarray(bits, dtype=np.uint32)
+    got = orc.f32_to_bf16(bits.view(np.float32))
+    ref = _torch_bf16_bits(bits)
+    nan = (bits & 0x7FFFFFFF) > 0x7F800000
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.all(got[nan] == 0x7FFF)
+    assert np.all((ref[nan] & 0x7FFF) > 0x7F80)  # torch also gives a NaN
+
+
+def test_bf16_rounding_every_high_half(orc):
+    """All 65536 kept halves x the discarded halves that decide nearest-even."""
+    lows = np.array([0x0000, 0x0001, 0x3FFF, 0x7FFF, 0x8000, 0x8001, 0xBFFF, 0xFFFF], np.uint32)
+    hi = np.arange(65536, dtype=np.uint32)
+    _check_rounding(orc, ((hi[:, None] << 16) | lows[None, :]).reshape(-1))
+
+
+def test_bf16_rounding_every_low_half(orc):
+    """All 65536 discarded halves under kept halves of both parities, both signs,
+    the subnormal range, the largest finite value and infinity."""
+    his = np.array([0x0000, 0x0001, 0x007F, 0x0080, 0x3F80, 0x3F81, 0x4049, 0x7F7E, 0x7F7F,
+                    0x7F80, 0x8000, 0x8001, 0xBF80, 0xBF81, 0xFF7F, 0xFF80], np.uint32)
+    lo = np.arange(65536, dtype=np.uint32)
+    _check_rounding(orc, ((his[:, None] << 16) | lo[None, :]).reshape(-1))
+
+
+def test_bf16_rounding_random(orc):
+    rng = np.random.default_rng(1)
+    _check_rounding(orc, rng.integers(0, 2**32, size=1 << 22, dtype=np.uint64).astype(np.uint32))
+
+
+def test_no_fused_multiply_add(orc):
+    """(1+2^-12)^2 - (1+2^-11) is 2^-24 exactly; two roundings give 0."""
+    a = 1.0 + 2.0 ** -12
+    assert orc.probe_mul_add(a, a, -(1.0 + 2.0 ** -11)) == 0.0
+
+
+# ---------------------------------------------------------------- tanh
+
+
+def _nearest_bf16_mp(x_bits: int, mp) -> int:
+    """The bfloat16 nearest to tanh(x) for a finite bfloat16 x, ties to even,
+    searched among the neighbours of a binary64 estimate, compared at 50 digits."""
+    x = float(np.array([x_bits << 16], np.uint32).view(np.float32)[0])
+    t = mp.tanh(mp.mpf(x))
+    est = np.array([float(t)], np.float32).view(np.uint32)[0] >> 16
+    cands = set()
+    for d in (-2, -1, 0, 1, 2):
+        c = (int(est) + d) & 0xFFFF
+        if (c & 0x7FFF) <= 0x7F80:
+            cands.add(c)
+    # also try the sign-flipped encodings near zero
+    if abs(x) < 1e-30:
+        cands.update({0x0000, 0x8000})
+    best = None
+    for c in sorted(cands):
+        v = float(np.array([c << 16], np.uint32).view(np.float32)[0])
+        err = abs(mp.mpf(v) - t)
+        key = (err, c & 1)  # on a tie, the even encoding wins
+        if best is None or key < best[0]:
+            best = (key, c)
+    return best[1]
+
+
+def test_tanh_table_exhaustive_against_mpmath(orc):
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 50
+    table = orc.tanh_table()
+    bad = []
+    for g in range(65536):
+        a = g & 0x7FFF
+        if a > 0x7F80:
+            if table[g] != 0x7FFF:
+                bad.append(g)
+            continue
+        if a == 0x7F80:
+            want = (g & 0x8000) | 0x3F80
+        elif a == 0:
+            want = g  # tanh(+-0) = +-0
+        else:
+            want = _nearest_bf16_mp(g, mp)
+        if table[g] != want:
+            bad.append(g)
+    assert not bad, [hex(b) for b in bad[:10]]
+
+
+def test_tanh_table_odd_and_saturating(orc):
+    t = orc.tanh_table()
+    g = np.arange(0x7F80)
+    assert np.array_equal(t[g | 0x8000], t[g] | 0x8000)
+    assert t[0x4080] == 0x3F80  # tanh(4) rounds to 1
+    assert t[0x0000] == 0x0000 and t[0x8000] == 0x8000
+
+
+# ---------------------------------------------------------------- Welford-128
+
+
+def _welford_textbook(xs: np.ndarray):
+    """Welford (1962) running mean and M2 in binary32, one element at a time
+    (Knuth, TAOCP vol. 2, 4.2.2) -- the special case of a single active lane."""
+    f = np.float32
+    n = f(0); mean = f(0); m2 = f(0)
+    for v in xs.astype(np.float32):
+        n = f(n + f(1))
+        d = f(v - mean)
+        mean = f(mean + f(d / n))
+        m2 = f(m2 + f(d * f(v - mean)))
+    return mean, m2, n
+
+
+def _chan(a, b):
+    """Chan, Golub & LeVeque pairwise update, with r = nB/n (binary32)."""
+    f = np.float32
+    (ma, qa, na), (mb, qb, nb) = a, b
+    n = f(na + nb)
+    d = f(mb - ma)
+    r = f(nb / n)
+    return f(ma + f(d * r)), f(f(qa + qb) + f(f(d * d) * f(na * r))), n
+
+
+@pytest.mark.parametrize("D", [1, 2, 3, 5, 7, 8])
+def test_welford_single_lane_is_textbook(orc, D):
+    rng = np.random.default_rng(D)
+    for _ in range(50):
+        x = orc.f32_to_bf16(rng.standard_normal(D).astype(np.float32) * 3 + 1)
+        got = orc.welford128(x)
+        want = _welford_textbook(orc.bf16_to_f32(x))
+        assert got == tuple(float(v) for v in want)
+
+
+def test_welford_two_lanes_is_one_chan_combine(orc):
+    rng = np.random.default_rng(7)
+    for D in (9, 12, 16):
+        for _ in range(50):
+            x = orc.f32_to_bf16(rng.standard_normal(D).astype(np.float32))
+            xf = orc.bf16_to_f32(x)
+            want = _chan(_welford_textbook(xf[:8]), _welford_textbook(xf[8:]))
+            assert orc.welford128(x) == tuple(float(v) for v in want)
+
+
+@pytest.mark.parametrize("D", [1, 7, 8, 100, 512, 1000, 1024, 3072, 5120, 8192])
+def test_welford_against_float64(orc, D):
+    rng = np.random.default_rng(D)
+    for scale_, offset in ((1.0, 0.0), (20.0, 3.0), (1e-3, 100.0)):
+        x = orc.f32_to_bf16((rng.standard_normal(D) * scale_ + offset).astype(np.float32))
+        xf = orc.bf16_to_f32(x).astype(np.float64)
+        mean, m2, n = orc.welford128(x)
+        assert n == D
+        amax = np.abs(xf).max()
+        assert abs(mean - xf.mean()) <= D * 2.0 ** -23 * amax
+        var64 = ((xf - xf.mean()) ** 2).sum()
+        assert abs(m2 - var64) <= 2.0 ** -12 * var64 + D * 2.0 ** -40 * amax * amax
+
+
+def test_welford_constant_row_is_exact(orc):
+    for D in (1, 9, 512, 3072, 8192):
+        for c in (0x3F80, 0xC2C8, 0x0001, 0x7F00):
+            mean, m2, n = orc.welford128(np.full(D, c, np.uint16))
+            assert np.float32(mean).view(np.uint32) == np.uint32(c << 16)
+            assert m2 == 0.0 and n == D
+
+
+# ---------------------------------------------------------------- Sum-128
+
+
+def test_sum128_integer_rows_are_exact(orc):
+    """Small integers: every square and partial sum is exact, so S = sum x^2."""
+    rng = np.random.default_rng(3)
+    for D in (1, 8, 129, 1000, 8192):
+        xi = rng.integers(-16, 17, size=D)
+        x = orc.f32_to_bf16(xi.astype(np.float32))
+        assert orc.sum128_sq(x) == float((xi * xi).sum())
+
+
+def test_sum128_against_float64(orc):
+    rng = np.random.default_rng(4)
+    for D in (100, 3072, 8192):
+        x = orc.f32_to_bf16(rng.standard_normal(D).astype(np.float32))
+        xf = orc.bf16_to_f32(x).astype(np.float64)
+        sq = orc.bf16_to_f32(orc.f32_to_bf16((xf * xf).astype(np.float32))).astype(np.float64)
+        S = orc.sum128_sq(x)
+        # binary32 summation error bound over at most 64 + 7 additions per path
+        assert abs(S - sq.sum()) <= 80 * 2.0 ** -24 * sq.sum()
+        # and the rounding of the squares is really there (relative 2^-9 scale)
+        assert abs(S - (xf * xf).sum()) <= 2.0 ** -8 * (xf * xf).sum()
+
+
+# ---------------------------------------------------------------- LN + modulate
+
+
+def _ln_case(D, rows=4, seed=0, mrows=2):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(rows, D, generator=g).to(torch.bfloat16)
+    sc = (torch.randn(mrows, D, generator=g) * 0.1).to(torch.bfloat16)
+    sh = (torch.randn(mrows, D, generator=g) * 0.1).to(torch.bfloat16)
+    return x, sc, sh
+
+
+@pytest.mark.parametrize("D", [2, 3, 8, 16, 64, 512, 3072])
+def test_ln_output_within_one_ulp_of_float64_layer_norm(orc, D):
+    """scale = shift = 0 leaves n = bf16(LN(x)); compare with torch.layer_norm
+    in binary64 (biased variance, eps inside the root)."""
+    x, _, _ = _ln_case(D, rows=64, seed=D)
+    zeros = np.zeros((1, D), np.uint16)
+    n = orc.bf16_to_f32(orc.ln_modulate(u16(x), zeros, zeros, 1e-6)).astype(np.float64)
+    ref = torch.nn.functional.layer_norm(x.double(), (D,), eps=float(np.float32(1e-6))).numpy()
+    assert np.all(np.abs(n - ref) <= bf16_ulp(ref))
+
+
+def test_modulate_step_equals_torch_eager_bf16(orc):
+    """Given n, out must equal PyTorch CPU eager (n * (1 + scale)) + shift."""
+    D, rows = 3072, 32
+    x, sc, sh = _ln_case(D, rows=rows, seed=11, mrows=2)
+    zeros = np.zeros((1, D), np.uint16)
+    n = bf(orc.ln_modulate(u16(x), zeros, zeros, 1e-6)).reshape(rows, D)
+    got = orc.ln_modulate(u16(x), u16(sc), u16(sh), 1e-6)
+    per = rows // 2
+    sc_r = sc.repeat_interleave(per, dim=0)
+    sh_r = sh.repeat_interleave(per, dim=0)
+    want = u16((n * (1 + sc_r)) + sh_r)
+    assert np.array_equal(got.reshape(-1), want.reshape(-1))
+
+
+def test_constant_row_gives_shift(orc):
+    D = 512
+    _, sc, sh = _ln_case(D, rows=2, seed=5, mrows=1)
+    for c in (0.0, 1.0, -3.5, 1e-20):
+        x = torch.full((3, D), c).to(torch.bfloat16)
+        got = orc.ln_modulate(u16(x), u16(sc), u16(sh), 1e-6)
+        assert np.array_equal(got, np.broadcast_to(u16(sh), got.shape))
+
+
+def test_modulation_row_mapping(orc):
+    """Row r uses modulation row r // (rows // mod_rows)."""
+    D, rows = 64, 12
+    x, sc, sh = _ln_case(D, rows=rows, seed=9, mrows=3)
+    got = orc.ln_modulate(u16(x), u16(sc), u16(sh), 1e-6)
+    for r in range(rows):
+        one = orc.ln_modulate(u16(x[r:r + 1]), u16(sc[r // 4:r // 4 + 1]), u16(sh[r // 4:r // 4 + 1]))
+        assert np.array_equal(got[r], one[0])
+
+
+def test_ln_f64_reference_matches_torch(orc):
+    D = 300
+    x, sc, sh = _ln_case(D, rows=8, seed=13, mrows=2)
+    out, mag = orc.ln_modulate_f64(u16(x), u16(sc), u16(sh), 1e-6)
+    ln = torch.nn.functional.layer_norm(x.double(), (D,), eps=float(np.float32(1e-6)))
+    want = ln * (1 + sc.double().repeat_interleave(4, 0)) + sh.double().repeat_interleave(4, 0)
+    assert np.allclose(out, want.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.all(mag >= np.abs(out))
+
+
+def test_lossless_ln_modulate_near_exact(orc):
+    """First-order error budget of the bit-exact chain, with u = 2^-8 the unit
+    roundoff of bfloat16 and an error of k*u relative to a term T being at most
+    k ulps of T: n = bf16(LN) (u), t = bf16(1+scale) (u), bf16(n*t) (u): 3u on
+    the product, plus half an ulp for the final sum.  So <= 3.5 bf16 ulps of the
+    largest term of the exact result."""
+    for d, D in ((synth.tiny_ln_modulate(), 512), (synth.image_dit_block(seq=64), 3072)):
+        x, sc, sh = u16(d["x"]).reshape(-1, D), u16(d["scale"]), u16(d["shift"])
+        got = orc.bf16_to_f32(orc.ln_modulate(x, sc, sh, 1e-6)).astype(np.float64)
+        ex, mag = orc.ln_modulate_f64(x, sc, sh, 1e-6)
+        assert np.all(np.abs(got - ex) <= 3.5 * 1.01 * bf16_ulp(mag))
+
+
+# ---------------------------------------------------------------- RMSNorm
+
+
+def _rms_chain_torch(x: torch.Tensor, S: np.ndarray, w: torch.Tensor, sc: torch.Tensor, eps=1e-6):
+    """Everything after the row sum, in PyTorch CPU eager ops, following the
+    rounding points of the BF16-native rmsnorm_scale excerpt (PR #34085 digest,
+    关键源码片段)."""
+    D = x.shape[-1]
+    Sf = torch.from_numpy(np.asarray(S, np.float32)).reshape(-1, 1)
+    ms = (Sf / D).to(torch.bfloat16)
+    inner = (ms.float() + np.float32(eps)).to(torch.bfloat16)
+    rstd = (1.0 / torch.sqrt(inner.float())).to(torch.bfloat16)
+    return ((x * rstd) * w) * sc
+
+
+def test_rmsnorm_scale_chain_equals_torch_eager(orc):
+    d = synth.tiny_ln_modulate()
+    x = d["x"].reshape(-1, 512)
+    S = np.array([orc.sum128_sq(u16(x[r])) for r in range(x.shape[0])])
+    got = orc.rmsnorm_scale(u16(x), u16(d["weight"]), u16(d["scale"]), 1e-6)
+    want = _rms_chain_torch(x, S, d["weight"], d["scale"].repeat_interleave(256, 0))
+    assert np.array_equal(got, u16(want))
+
+
+def test_rmsnorm_constant_row_closed_form(orc):
+    """Constant row c: S = D*bf16(c^2) exactly, so ms = bf16(c^2)."""
+    D = 4096
+    ones = np.full((1, D), 0x3F80, np.uint16)
+    for c in (0.5, 1.25, -3.0, 7.0):
+        x = np.full((2, D), int(orc.f32_to_bf16(np.array([c], np.float32))[0]), np.uint16)
+        cb = float(orc.bf16_to_f32(x[:1, :1])[0, 0])
+        sq = float(orc.bf16_to_f32(orc.f32_to_bf16(np.array([cb * cb], np.float32)))[0])
+        assert orc.sum128_sq(x[0]) == D * sq
+        inner = np.float32(orc.bf16_to_f32(orc.f32_to_bf16(np.array([np.float32(sq) + np.float32(1e-6)], np.float32)))[0])
+        rstd = orc.bf16_to_f32(orc.f32_to_bf16(np.array([np.float32(1) / np.sqrt(inner)], np.float32)))[0]
+        want = orc.f32_to_bf16(np.array([np.float32(cb) * rstd], np.float32))[0]
+        got = orc.rmsnorm_scale(x, ones[0], ones, 1e-6)
+        assert np.all(got == want)
+
+
+def test_rmsnorm_zero_row_and_unit_rms(orc):
+    D = 3072
+    rng = np.random.default_rng(2)
+    x = orc.f32_to_bf16(rng.standard_normal((16, D)).astype(np.float32) * 5)
+    x[3] = 0
+    ones = np.full((1, D), 0x3F80, np.uint16)
+    y = orc.bf16_to_f32(orc.rmsnorm_scale(x, ones[0], ones, 1e-6)).astype(np.float64)
+    assert np.all(y[3] == 0)
+    rms = np.sqrt((np.delete(y, 3, 0) ** 2).mean(axis=1))
+    assert np.all(np.abs(rms - 1.0) < 2.0 ** -6)
+
+
+def test_rmsnorm_f64_reference_matches_torch(orc):
+    d = synth.tiny_ln_modulate()
+    x = d["x"].reshape(-1, 512)
+    out, _ = orc.rmsnorm_scale_f64(u16(x), u16(d["weight"]), u16(d["scale"]), 1e-6)
+    xd = x.double()
+    want = xd * torch.rsqrt((xd * xd).mean(-1, keepdim=True) + float(np.float32(1e-6)))
+    want = want * d["weight"].double() * d["scale"].double().repeat_interleave(256, 0)
+    assert np.allclose(out, want.numpy(), rtol=1e-12, atol=1e-15)
+
+
+# ---------------------------------------------------------------- tanh residual
+
+
+def test_rmsnorm_tanh_residual_composition(orc):
+    """out = bf16(r + bf16(tanh_bf16(g) * n)) with n the rmsnorm chain without
+    scale (rmsnorm_scale with scale 1 gives n, since bf16(n*1) = n); the last two
+    steps are checked against PyTorch CPU eager bf16 ops."""
+    D, rows = 1000, 24
+    g = torch.Generator().manual_seed(21)
+    x = torch.randn(rows, D, generator=g).to(torch.bfloat16)
+    gate = torch.randn(rows, D, generator=g).to(torch.bfloat16)
+    res = torch.randn(rows, D, generator=g).to(torch.bfloat16)
+    w = (1 + 0.05 * torch.randn(D, generator=g)).to(torch.bfloat16)
+    ones = np.full((1, D), 0x3F80, np.uint16)
+    n = bf(orc.rmsnorm_scale(u16(x), u16(w), ones, 1e-6))
+    tg = bf(orc.tanh_table()[u16(gate)])
+    want = u16(res + tg * n)
+    got = orc.rmsnorm_tanh_residual(u16(x), u16(gate), u16(res), u16(w), 1e-6)
+    assert np.array_equal(got, want)
+
+
+def test_rmsnorm_chains_near_exact(orc):
+    """First-order budget (u = 2^-8, k*u relative = at most k ulps): the rounded
+    squares, bf16(S/D) and bf16(ms+eps) give 3u under the root, halved by it,
+    plus u for bf16(rstd): 2.5u; bf16(x*rstd) and bf16(.*w): 4.5u on n.
+    rmsnorm_scale adds bf16(n*scale): <= 5.5 ulps.  The tanh residual adds the
+    rounded tanh and bf16(tg*n): 6.5u on p, plus half an ulp for the sum: <= 7."""
+    for D, T in ((1024, 77), (3072, 300), (8192, 40)):
+        d = synth.sweep_case(D, T)
+        x, g, r, w, sc = (u16(d[k].contiguous())
+                          for k in ("x", "gate_tok", "residual", "weight", "scale"))
+        got = orc.bf16_to_f32(orc.rmsnorm_tanh_residual(x, g, r, w, 1e-6)).astype(np.float64)
+        ex, mag = orc.rmsnorm_tanh_residual_f64(x, g, r, w, 1e-6)
+        assert np.all(np.abs(got - ex) <= 7 * 1.01 * bf16_ulp(mag))
+        got = orc.bf16_to_f32(orc.rmsnorm_scale(x, w, sc, 1e-6)).astype(np.float64)
+        ex, mag = orc.rmsnorm_scale_f64(x, w, sc, 1e-6)
+        assert np.all(np.abs(got - ex) <= 5.5 * 1.01 * bf16_ulp(mag))
+
+
+# ---------------------------------------------------------------- gated residual
+
+
+def test_residual_gate_add_equals_torch_eager(orc):
+    g = torch.Generator().manual_seed(31)
+    rows, D = 64, 777
+    x = torch.randn(rows, D, generator=g).to(torch.bfloat16)
+    y = torch.randn(rows, D, generator=g).to(torch.bfloat16)
+    gate = (torch.randn(4, D, generator=g)).to(torch.bfloat16)
+    # extremes: overflow to inf, subnormal products, exact cancellation
+    x[0, :4] = torch.tensor([3e38, -3e38, 1e-38, 0.0]).to(torch.bfloat16)
+    y[0, :4] = torch.tensor([3e38, 3e38, 1e-38, 0.0]).to(torch.bfloat16)
+    got = orc.residual_gate_add(u16(x), u16(gate), u16(y))
+    want = x + gate.repeat_interleave(16, 0) * y
+    assert np.array_equal(got, u16(want))
+
+
+def test_residual_gate_add_zero_gate_is_identity(orc):
+    g = torch.Generator().manual_seed(32)
+    x = torch.randn(8, 96, generator=g).to(torch.bfloat16)
+    y = torch.randn(8, 96, generator=g).to(torch.bfloat16)
+    z = np.zeros((1, 96), np.uint16)
+    assert np.array_equal(orc.residual_gate_add(u16(x), z, u16(y)), u16(x))
+
+
+# ---------------------------------------------------------------- QKV epilogue
+
+
+def _small_qkv(**kw):
+    return synth.qkv_epilogue_case(batch=2, s_txt=5, grid_h=3, grid_w=4, heads=3, **kw)
+
+
+def _run_qkv(orc, d, cos_txt=None, sin_txt=None, cos_img=None, sin_img=None):
+    return orc.qkv_epilogue(u16(d["txt"].contiguous()), u16(d["img"].contiguous()), d["batch"],
+                            d["heads"], d["head_dim"], u16(d["wq_txt"]), u16(d["wk_txt"]),
+                            u16(d["wq_img"]), u16(d["wk_img"]),
+                            (d["cos_txt"] if cos_txt is None else cos_txt).numpy(),
+                            (d["sin_txt"] if sin_txt is None else sin_txt).numpy(),
+                            (d["cos_img"] if cos_img is None else cos_img).numpy(),
+                            (d["sin_img"] if sin_img is None else sin_img).numpy(), d["eps"])
+
+
+def test_qkv_v_is_bit_copy_and_layout(orc):
+    d = _small_qkv()
+    B, H, hd = d["batch"], d["heads"], d["head_dim"]
+    joint = _run_qkv(orc, d)
+    txt = u16(d["txt"].contiguous()).reshape(B, 5, 3, H, hd)
+    img = u16(d["img"].contiguous()).reshape(B, 12, 3, H, hd)
+    assert joint.shape == (B, 3, H, 17, hd)
+    # V: text first, then image
+    assert np.array_equal(joint[:, 2, :, :5], txt[:, :, 2].transpose(0, 2, 1, 3))
+    assert np.array_equal(joint[:, 2, :, 5:], img[:, :, 2].transpose(0, 2, 1, 3))
+
+
+def test_qkv_identity_rotation_is_head_rmsnorm(orc):
+    """cos = 1, sin = 0: each Q/K head equals the rmsnorm chain at D = hd with
+    scale 1, using the branch's own weight."""
+    d = _small_qkv()
+    B, H, hd = d["batch"], d["heads"], d["head_dim"]
+    one = lambda S: torch.ones(S, hd // 2)
+    zero = lambda S: torch.zeros(S, hd // 2)
+    joint = _run_qkv(orc, d, one(5), zero(5), one(12), zero(12))
+    ones = np.full((1, hd), 0x3F80, np.uint16)
+    for name, S, off, wq, wk in (("txt", 5, 0, "wq_txt", "wk_txt"), ("img", 12, 5, "wq_img", "wk_img")):
+        src = u16(d[name].contiguous()).reshape(B, S, 3, H, hd)
+        for part, w in ((0, wq), (1, wk)):
+            heads = src[:, :, part].reshape(-1, hd)
+            want = orc.rmsnorm_scale(heads, u16(d[w]), ones, 1e-6).reshape(B, S, H, hd)
+            assert np.array_equal(joint[:, part, :, off:off + S], want.transpose(0, 2, 1, 3))
+
+
+def test_qkv_rotation_equals_torch_eager_and_position_zero(orc):
+    """o0 = bf16(n0*c - n1*s), o1 = bf16(n0*s + n1*c) in binary32 eager ops,
+    applied to the identity-rotation output n; token 0 (c=1, s=0) is n."""
+    d = _small_qkv()
+    B, H, hd = d["batch"], d["heads"], d["head_dim"]
+    one = lambda S: torch.ones(S, hd // 2)
+    zero = lambda S: torch.zeros(S, hd // 2)
+    n = _run_qkv(orc, d, one(5), zero(5), one(12), zero(12))
+    joint = _run_qkv(orc, d)
+    cos = torch.cat([d["cos_txt"], d["cos_img"]])  # [17, hd/2]
+    sin = torch.cat([d["sin_txt"], d["sin_img"]])
+    nt = bf(n[:, :2]).float().reshape(B, 2, H, 17, hd // 2, 2)
+    n0, n1 = nt[..., 0], nt[..., 1]
+    o0 = (n0 * cos - n1 * sin).to(torch.bfloat16)
+    o1 = (n0 * sin + n1 * cos).to(torch.bfloat16)
+    want = torch.stack([o0, o1], -1).reshape(B, 2, H, 17, hd)
+    assert np.array_equal(joint[:, :2], u16(want))
+    assert np.array_equal(joint[:, :2, :, 0], n[:, :2, :, 0])  # text position 0
+    assert np.array_equal(joint[:, :2, :, 5], n[:, :2, :, 5])  # image cell (0, 0)
+
+
+def test_qkv_rotation_preserves_pair_norm(orc):
+    d = _small_qkv()
+    B, H, hd = d["batch"], d["heads"], d["head_dim"]
+    one = lambda S: torch.ones(S, hd // 2)
+    zero = lambda S: torch.zeros(S, hd // 2)
+    n = orc.bf16_to_f32(_run_qkv(orc, d, one(5), zero(5), one(12), zero(12))[:, :2]).astype(np.float64)
+    o = orc.bf16_to_f32(_run_qkv(orc, d)[:, :2]).astype(np.float64)
+    n2 = (n.reshape(-1, 2) ** 2).sum(1)
+    o2 = (o.reshape(-1, 2) ** 2).sum(1)
+    amax = np.abs(n.reshape(-1, 2)).max(1)
+    assert np.all(np.abs(np.sqrt(o2) - np.sqrt(n2)) <= 2 * bf16_ulp(amax))
+
+
+def test_qkv_rotation_composes(orc):
+    """Rotating by p1 and then by p2 matches rotating by p1 + p2 (binary64 check
+    on the oracle's rotation with the synthetic text tables)."""
+    d = synth.qkv_epilogue_case(batch=1, s_txt=40, grid_h=1, grid_w=1, heads=1)
+    hd = d["head_dim"]
+    cos, sin = d["cos_txt"].double().numpy(), d["sin_txt"].double().numpy()
+    p1, p2 = 7, 30
+    c = cos[p1] * cos[p2] - sin[p1] * sin[p2]
+    s = sin[p1] * cos[p2] + cos[p1] * sin[p2]
+    assert np.allclose(c, cos[p1 + p2], atol=1e-6) and np.allclose(s, sin[p1 + p2], atol=1e-6)
+    # the oracle applies exactly these tables: the rotation of token p1+p2 is
+    # within rounding of rotating token p1's normalised pair by table p2
+    one = torch.ones(40, hd // 2); zero = torch.zeros(40, hd // 2)
+    dd = dict(d)
+    row = d["txt"][p1].clone()
+    dd["txt"] = torch.stack([row] * 40)
+    n = orc.bf16_to_f32(_run_qkv(orc, dd, one, zero, d["cos_img"], d["sin_img"])[0, 0, 0, 0]).astype(np.float64)
+    o = orc.bf16_to_f32(_run_qkv(orc, dd)[0, 0, 0]).astype(np.float64)  # [40, hd]
+    n0, n1 = n[0::2], n[1::2]
+    a0 = n0 * cos[p1] - n1 * sin[p1]
+    a1 = n0 * sin[p1] + n1 * cos[p1]
+    b0 = a0 * cos[p2] - a1 * sin[p2]
+    b1 = a0 * sin[p2] + a1 * cos[p2]
+    assert np.allclose(o[p1 + p2, 0::2], b0, atol=2 * 2.0 ** -7 * np.abs(n).max())
+    assert np.allclose(o[p1 + p2, 1::2], b1, atol=2 * 2.0 ** -7 * np.abs(n).max())
+
+
+def test_qk_head_f64_reference(orc):
+    d = _small_qkv()
+    hd = d["head_dim"]
+    src = u16(d["txt"][3, :hd].contiguous())
+    out, _ = orc.qk_head_f64(src, u16(d["wq_txt"]), d["cos_txt"][3].numpy(), d["sin_txt"][3].numpy())
+    x = d["txt"][3, :hd].double()
+    n = x * torch.rsqrt((x * x).mean() + float(np.float32(1e-6))) * d["wq_txt"].double()
+    c, s = d["cos_txt"][3].double(), d["sin_txt"][3].double()
+    want = torch.stack([n[0::2] * c - n[1::2] * s, n[0::2] * s + n[1::2] * c], -1).reshape(-1)
+    assert np.allclose(out, want.numpy(), rtol=1e-12, atol=1e-14)
