@@ -1,0 +1,406 @@
+"""Benchmark of the DiT norm/modulation hot path (one JSON line on rank 0).
+
+Workload (one step): the image-DiT block norm path at Qwen-Image scale,
+  ln_modulate:       out1 = LN(x) * (1 + scale) + shift   x [2, 4352, 3072]
+  residual_gate_add: out2 = x' + gate * y                  x', y [2, 4352, 3072]
+with per-sample scale/shift/gate [2, 3072], bfloat16, lossless variant, every
+call through the C ABI of libmbx.so.  Inputs are synthetic (seeded, N(0,1)
+activations with 1 % outliers x20, N(0,0.1) modulation).
+
+L2 policy: three buffer sets of 267 MB each (x, out1, x', y, out2) are used
+in turn, so a step never reads a tensor the previous ~530 MB of traffic
+touched (L2 is 129 MB); the per-sample modulation vectors (36 KB) stay in L2,
+as they would in a model.
+
+Metric: achieved HBM GB/s = algorithmic bytes (every input read once, every
+output written once) / device time, from CUDA events on the launching stream.
+Multi-GPU (torchrun): each rank runs its own copy of the workload (rows are
+independent: no collective on the data path); the barrier and the max over
+ranks of the timed region are the only communication.
+
+--impl reference times the CPU oracle (oracle/, plain C) on a bounded sample
+of the same workload, on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (% of GB300 peak) and µs/call for LN+AdaLN modulate"
+B, S, D = 2, 4352, 3072
+ELEMS = B * S * D
+T_BYTES = ELEMS * 2                                  # one [2,4352,3072] bf16 tensor
+LN_BYTES = 2 * T_BYTES + 2 * B * D * 2               # read x, write out, scale + shift
+RGA_BYTES = 3 * T_BYTES + B * D * 2                  # read x', y, write out, gate
+STEP_BYTES = LN_BYTES + RGA_BYTES
+WORKLOAD = ("image-DiT block norm path: ln_modulate x[2,4352,3072] (per-sample scale/shift "
+            "[2,3072], eps 1e-6) then residual_gate_add x'[2,4352,3072] + gate[2,3072]*y, "
+            "bf16, lossless")
+L2_NOTE = "3 rotating buffer sets of 267 MB (inputs larger than L2 per step, no re-read)"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_sha(op: str) -> str:
+    k = os.path.join(ROOT, "modulation_bit_exact_gb300", "csrc", "kernels")
+    files = ["numerics.cuh", "rowops.cuh", {"ln_modulate": "ln_modulate.cu",
+                                             "residual_gate_add": "residual.cu"}[op]]
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(k, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(op: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = kernel_sha(op)
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == op and parts[2] == sha:
+                return int(parts[1])
+    return None
+
+
+class Clocks:
+    """nvidia-smi sampling (every 100 ms) around the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", self.gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------- CPU oracle
+
+
+def oracle_rate(budget_s: float, rows_per_call: int = 64):
+    """GB/s of the CPU oracle on row samples of the workload (both operations),
+    over about budget_s seconds; returns (GB/s, rows done, seconds)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import synth
+    d = synth.image_dit_block(seq=256)  # the same recipe, 512 rows
+    u = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1, D)
+    X, Y = u(d["x"]), u(d["y"])
+    SC, SH, G = u(d["scale"]), u(d["shift"]), u(d["gate"])
+    oracle.lib()
+    done, t0 = 0, time.perf_counter()
+    while True:
+        r0 = (done % (X.shape[0] // rows_per_call)) * rows_per_call
+        xs, ys = X[r0:r0 + rows_per_call], Y[r0:r0 + rows_per_call]
+        m = (r0 // 256)
+        oracle.ln_modulate(xs, SC[m:m + 1], SH[m:m + 1], 1e-6)
+        oracle.residual_gate_add(xs, G[m:m + 1], ys)
+        done += rows_per_call
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    per_row = (2 * 2 * D) + (3 * 2 * D)  # ln: read + write; rga: 2 reads + write
+    return done * per_row / el / 1e9, done, el
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, on this host's cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+
+    import oracle
+    import synth
+    d = synth.image_dit_block(seq=256)
+    u = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1, D)
+    X, Y = u(d["x"]), u(d["y"])
+    SC, SH, G = u(d["scale"]), u(d["shift"]), u(d["gate"])
+    oracle.lib()
+    # size a step so that warmup + steps take about 60 s in all
+    t0 = time.perf_counter()
+    oracle.ln_modulate(X[:8], SC[:1], SH[:1], 1e-6)
+    oracle.residual_gate_add(X[:8], G[:1], Y[:8])
+    per_row = (time.perf_counter() - t0) / 8
+    rows = int(max(1, min(512, 60.0 / max(1, args.steps + args.warmup) / max(per_row, 1e-9))))
+
+    def step(i):
+        r0 = (i * rows) % (X.shape[0] - rows + 1)
+        m = r0 // 256
+        oracle.ln_modulate(X[r0:r0 + rows], SC[m:m + 1], SH[m:m + 1], 1e-6)
+        oracle.residual_gate_add(X[r0:r0 + rows], G[m:m + 1], Y[r0:r0 + rows])
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    el = time.perf_counter() - t0
+    bytes_per_step = rows * ((2 * 2 * D) + (3 * 2 * D))
+    gbs = bytes_per_step * args.steps / el / 1e9
+    sample = (f"{rows} rows of x[2,4352,3072] per step (both operations; the full step is "
+              f"8704 rows), 1 thread of {os.cpu_count()} host cores")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------- GPU arm
+
+
+def run_gpu(args):
+    import ctypes
+
+    import torch
+
+    import modulation_bit_exact_gb300 as mbx
+    import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    L = mbx.lib()
+    stream = torch.cuda.current_stream(dev)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+
+    # three buffer sets
+    sets = []
+    for i in range(3):
+        d = synth.image_dit_block(seed=2 + 100 * i + 1000 * rank, device=dev)
+        d2 = synth.image_dit_block(seed=3 + 100 * i + 1000 * rank, device=dev)
+        s = dict(x=d["x"], scale=d["scale"], shift=d["shift"], out1=torch.empty_like(d["x"]),
+                 xb=d2["x"], gate=d["gate"], y=d["y"], out2=torch.empty_like(d["x"]))
+        v = {k: mbx._view(t) for k, t in s.items()}
+        sets.append((s, v))
+    del d, d2
+    torch.cuda.synchronize(dev)
+    eps = ctypes.c_float(1e-6)
+    ref = ctypes.byref
+
+    def launch(i, ev=None):
+        _, v = sets[i % 3]
+        st = L.mbx_ln_modulate(ref(v["out1"]), ref(v["x"]), ref(v["scale"]), ref(v["shift"]), eps, 0, sptr)
+        if ev is not None:
+            ev.record(stream)
+        st |= L.mbx_residual_gate_add(ref(v["out2"]), ref(v["xb"]), ref(v["gate"]), ref(v["y"]), 0, sptr)
+        return st
+
+    for i in range(args.warmup):
+        if launch(i) != 0:
+            raise RuntimeError("launch failed")
+    torch.cuda.synchronize(dev)
+
+    # timed region: per-kernel events at the boundaries (E_i0, ln, E_i1, rga, E_(i+1)0)
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K + 1)]
+    gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    if not gpu_uuid.startswith("GPU-"):
+        gpu_uuid = "GPU-" + gpu_uuid
+    clocks = Clocks(gpu_uuid)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with clocks:
+        ev[0].record(stream)
+        for i in range(K):
+            launch(i, ev[2 * i + 1])
+            ev[2 * i + 2].record(stream)
+        torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    total_ms = ev[0].elapsed_time(ev[2 * K])
+    ln_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(K))
+    rga_ms = sum(ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(K))
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end: pinned host inputs -> device, both calls, outputs -> host
+    e2e = None
+    if rank == 0 or True:
+        host = {k: torch.empty(sets[0][0][k].shape, dtype=torch.bfloat16, pin_memory=True)
+                for k in ("x", "xb", "y", "scale", "shift", "gate", "out1", "out2")}
+        for k in ("x", "xb", "y", "scale", "shift", "gate"):
+            host[k].copy_(sets[0][0][k])
+        dsets = sets[0]
+        n_e2e = max(3, min(50, K // 100))
+
+        def e2e_step():
+            s, v = dsets
+            for k in ("x", "xb", "y", "scale", "shift", "gate"):
+                s[k].copy_(host[k], non_blocking=True)
+            L.mbx_ln_modulate(ref(v["out1"]), ref(v["x"]), ref(v["scale"]), ref(v["shift"]), eps, 0, sptr)
+            L.mbx_residual_gate_add(ref(v["out2"]), ref(v["xb"]), ref(v["gate"]), ref(v["y"]), 0, sptr)
+            host["out1"].copy_(s["out1"], non_blocking=True)
+            host["out2"].copy_(s["out2"], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        h2d = sum(host[k].numel() * 2 for k in ("x", "xb", "y", "scale", "shift", "gate"))
+        d2h = sum(host[k].numel() * 2 for k in ("out1", "out2"))
+        e2e = {"value": round(STEP_BYTES * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms, 4), "steps": n_e2e}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = peaks()
+    ln_us = ln_ms / K * 1e3
+    rga_us = rga_ms / K * 1e3
+    kern = {
+        "ln_modulate": {"us_per_call": round(ln_us, 3), "bytes": LN_BYTES,
+                        "gbs": round(LN_BYTES / (ln_us * 1e-6) / 1e9, 1)},
+        "residual_gate_add": {"us_per_call": round(rga_us, 3), "bytes": RGA_BYTES,
+                              "gbs": round(RGA_BYTES / (rga_us * 1e-6) / 1e9, 1)},
+    }
+    for k in kern.values():
+        k["frac"] = round(k["gbs"] / peak, 4)
+    dom = max(kern, key=lambda k: kern[k]["us_per_call"])
+    roof = {"bound": "hbm", "achieved": kern[dom]["gbs"], "peak": peak, "unit": "GB/s",
+            "frac": kern[dom]["frac"], "traffic": dram_traffic(dom), "kernel": dom,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s"}
+    cpu_gbs, cpu_rows, cpu_s = oracle_rate(args.cpu_seconds)
+    value = STEP_BYTES * K * world / (total_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": L2_NOTE, "variant": "lossless",
+                   "parallelism": f"replicas x{world} (row-independent, no data-path collective)"},
+        "ln_modulate_us_per_call": kern["ln_modulate"]["us_per_call"],
+        "frac_of_hbm_peak": round(value / world / peak, 4),
+        "frac_of_8tbs_spec": round(value / world / 8000.0, 4),
+        "kernels": kern,
+        "roofline": roof,
+        "cpu_baseline": {"value": round(cpu_gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{cpu_rows} rows of the workload (both operations) in "
+                                   f"{cpu_s:.1f} s, 1 thread of {os.cpu_count()} host cores"},
+        "e2e": e2e,
+        "gpu_launches": 2 * K * world,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="mbx", choices=["mbx", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,232 @@
+/*
+ * mbx.h -- C ABI of libmbx.so, bit-exact DiT norm/modulation kernels for GB300
+ * (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Tensors are described by views: a 2-D [rows, cols] array of bfloat16 whose
+ * last dimension is contiguous and whose rows start `row_stride` elements
+ * apart (row_stride >= cols; padding between rows is never read or written).
+ * `data` is a device pointer on the CUDA device that is current on the calling
+ * thread.  The caller owns every buffer: the library allocates nothing, frees
+ * nothing and never synchronises; work is enqueued on `stream` (a
+ * cudaStream_t; NULL is the legacy default stream) and the call returns once
+ * it is enqueued.
+ *
+ * Every argument is validated on the host before anything is launched; on
+ * any error the call returns a negative MBX_E_* status and launches nothing
+ * (mbx_status_string() names it).  The checks are the guard set of the
+ * BF16-native RMSNorm wrapper in "#34085 [diffusion] Clean up kernels and
+ * shared fast paths" (prhub.com.cn), sections 实现拆解 item 2 and 关键源码片段:
+ * one device, all bfloat16, hidden size <= 8192, non-empty, weight of shape
+ * [D] and contiguous, flat row stride, rows of x a multiple of the modulation
+ * rows.  In addition every view must lie inside one device allocation
+ * (MBX_E_BOUNDS), and an output may not overlap an input except where an
+ * entry point allows in-place use (MBX_E_ALIAS).
+ *
+ * Modulation broadcast: a modulation view (scale, shift, gate) has `mod_rows`
+ * rows with rows(x) % mod_rows == 0, and row r of x uses modulation row
+ * r / (rows(x) / mod_rows): per-sample modulation is mod_rows = batch,
+ * per-token modulation is mod_rows = rows(x) (same digest, 关键源码片段:
+ * batch = row // seq_len).
+ *
+ * Variants: MBX_LOSSLESS reproduces, bit for bit, the rounding order of the
+ * eager BF16 chain ("Agent-assisted SGLang diffusion kernel optimisation:
+ * Qwen-Image, FLUX.2 and video models", tahou.com, section
+ * 扩散Kernel对数值精度的敏感性); MBX_HIGH evaluates the same formula in one
+ * binary32 pass with a single rounding to bfloat16 at the output (same
+ * section: the "plain fusion" the lossless path replaces; same article,
+ * section 质量分级机制: the non-lossless quality tiers).
+ *
+ * Aligned fast path: rows whose start addresses are 16-byte aligned, with
+ * cols a multiple of 8, use 128-bit accesses; any other view takes a scalar
+ * path with the same arithmetic and order, so results are identical.
+ */
+#ifndef MBX_H
+#define MBX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MBX_API __attribute__((visibility("default")))
+#else
+#define MBX_API
+#endif
+
+#define MBX_ABI_VERSION 1
+
+/* dtype codes: bfloat16 is the only accepted element type. */
+enum { MBX_BF16 = 1 };
+
+/* variant codes */
+enum { MBX_LOSSLESS = 0, MBX_HIGH = 1 };
+
+/* status codes */
+enum {
+    MBX_OK = 0,
+    MBX_E_NULL = -1,          /* a required pointer is NULL                       */
+    MBX_E_DTYPE = -2,         /* an operand is not bfloat16                       */
+    MBX_E_EMPTY = -3,         /* rows or cols is zero (or negative)               */
+    MBX_E_DIM_TOO_LARGE = -4, /* cols (hidden size) above 8192                    */
+    MBX_E_SHAPE = -5,         /* shapes disagree, or rows % mod_rows != 0         */
+    MBX_E_STRIDE = -6,        /* row_stride < cols                                */
+    MBX_E_ALIGN = -7,         /* a pointer is not aligned to its element type     */
+    MBX_E_ALIAS = -8,         /* an output overlaps an input                      */
+    MBX_E_DEVICE = -9,        /* a pointer is not device memory of this device    */
+    MBX_E_BOUNDS = -10,       /* a view runs past the end of its allocation       */
+    MBX_E_VARIANT = -11,      /* variant is not MBX_LOSSLESS or MBX_HIGH          */
+    MBX_E_ARG = -12,          /* another argument is out of range (eps, heads...) */
+    MBX_E_CUDA = -13          /* the CUDA runtime reported an error               */
+};
+
+/* Read-only view of a [rows, cols] bfloat16 array (row_stride in elements). */
+typedef struct {
+    const void* data;
+    int64_t rows;
+    int64_t cols;
+    int64_t row_stride;
+    int32_t dtype;
+} mbx_cview;
+
+/* Writable view, same layout rules. */
+typedef struct {
+    void* data;
+    int64_t rows;
+    int64_t cols;
+    int64_t row_stride;
+    int32_t dtype;
+} mbx_view;
+
+/*
+ * LayerNorm (no affine) fused with AdaLN modulate.
+ * Defined in: tahou.com SGLang diffusion article, section
+ * 扩散Kernel对数值精度的敏感性 -- y = LN(x); y = y*(1+scale)+shift.
+ *   lossless: mean and M2 by Welford over 128 lanes (8-element chunks, chunk c
+ *     on lane c mod 128) combined by a fixed halving tree; var = M2/D;
+ *     rstd = 1/sqrt(var+eps) (correctly rounded); n = bf16((x-mean)*rstd);
+ *     out = bf16(bf16(n * bf16(1+scale)) + shift).
+ *   high: the same formula in one binary32 pass, rounded once.
+ * out [rows, D]; x [rows, D]; scale, shift [mod_rows, D].  eps >= 0, finite.
+ * out must not overlap x, scale or shift.
+ */
+MBX_API int mbx_ln_modulate(const mbx_view* out, const mbx_cview* x, const mbx_cview* scale,
+                            const mbx_cview* shift, float eps, int variant, void* stream);
+
+/*
+ * BF16-native RMSNorm times weight times scale.
+ * Defined in: prhub.com.cn digest of SGLang PR #34085, section 关键源码片段
+ * (rmsnorm_scale): squares rounded to bf16, row sum in binary32 (here over the
+ * same 128 lanes and tree as LayerNorm), ms = bf16(sum/D),
+ * rstd = bf16(1/sqrt(bf16(ms+eps))), out = bf16(bf16(bf16(x*rstd)*w)*scale).
+ * out [rows, D]; x [rows, D]; weight [1, D] contiguous; scale [mod_rows, D].
+ */
+MBX_API int mbx_rmsnorm_scale(const mbx_view* out, const mbx_cview* x, const mbx_cview* weight,
+                              const mbx_cview* scale, float eps, int variant, void* stream);
+
+/*
+ * out = residual + tanh(gate) * RMSNorm(x) * weight, BF16-native.
+ * Defined in: PR #34085 digest, 实现拆解 item 2 (rmsnorm_tanh_residual);
+ * "AI Agent 驱动的 SGLang Kernel 一等公民" (163.com), 3.2 (rmsnorm +
+ * tanh(gate)·x + residual).  n = bf16(bf16(x*rstd)*w) with rstd as in
+ * mbx_rmsnorm_scale; tg = the bfloat16 nearest to tanh(gate);
+ * out = bf16(residual + bf16(tg*n)).
+ * out, x, residual [rows, D]; gate [mod_rows, D]; weight [1, D].
+ * out may be exactly residual (same pointer and stride) for an in-place
+ * residual update; any other overlap is MBX_E_ALIAS.
+ */
+MBX_API int mbx_rmsnorm_tanh_residual(const mbx_view* out, const mbx_cview* x,
+                                      const mbx_cview* gate, const mbx_cview* residual,
+                                      const mbx_cview* weight, float eps, int variant,
+                                      void* stream);
+
+/*
+ * Gated residual add: out = bf16(x + bf16(gate * y)).
+ * Defined in: PR #34085 digest, 实现拆解 item 3 (residual_gate_add); 163.com
+ * article, 3.2 (residual + gate·update).
+ * out, x, y [rows, D]; gate [mod_rows, D].  out may be exactly x (in-place
+ * residual update); any other overlap is MBX_E_ALIAS.
+ */
+MBX_API int mbx_residual_gate_add(const mbx_view* out, const mbx_cview* x, const mbx_cview* gate,
+                                  const mbx_cview* y, int variant, void* stream);
+
+/*
+ * Fused post-GEMM QKV epilogue.
+ * Defined in: tahou.com SGLang diffusion article, section 合并QKV投影时的数值问题:
+ * after the merged QKV GEMM one kernel does Q/K RMSNorm, interleaved RoPE,
+ * the V copy, and writes text and image tokens into one joint QKV buffer,
+ * reading the GEMM output through strided views.
+ *   txt_qkv [batch*S_txt, 3*H*hd], img_qkv [batch*S_img, 3*H*hd]: columns
+ *     [0,H*hd) are Q, [H*hd,2H*hd) K, [2H*hd,3H*hd) V; head h of a part is
+ *     its columns [h*hd, (h+1)*hd).  Either branch may have 0 rows (NULL data).
+ *   joint [batch*3*H*(S_txt+S_img), hd], contiguous: element
+ *     (b, part, h, s, e) at row ((b*3+part)*H+h)*(S_txt+S_img)+s; text tokens
+ *     occupy s in [0,S_txt), image tokens [S_txt, S_txt+S_img).
+ *   wq_*, wk_* [1, hd]: per-branch Q and K RMSNorm weights.
+ *   cos_*, sin_* : binary32 [S, hd/2] per-token tables (device pointers,
+ *     16-byte aligned); pair i = (2i, 2i+1) of a head of token s rotates by
+ *     (cos[s][i], sin[s][i]): o0 = n0*c - n1*s, o1 = n0*s + n1*c.
+ *   lossless: Q/K heads use the mbx_rmsnorm_scale chain without the scale
+ *     (n = bf16(bf16(x*rstd)*w)), then o = bf16 of the binary32 rotation.
+ *   hd must be 64, 128 or 256; branch rows must be 16-byte aligned.
+ */
+MBX_API int mbx_qk_norm_rope_qkv_epilogue(const mbx_view* joint, const mbx_cview* txt_qkv,
+                                          const mbx_cview* img_qkv, int64_t batch, int64_t heads,
+                                          const mbx_cview* wq_txt, const mbx_cview* wk_txt,
+                                          const mbx_cview* wq_img, const mbx_cview* wk_img,
+                                          const float* cos_txt, const float* sin_txt,
+                                          const float* cos_img, const float* sin_img, float eps,
+                                          int variant, void* stream);
+
+/*
+ * Validation only: the same checks as the matching entry point, nothing is
+ * launched and no stream is touched.  Returns MBX_OK or the status the entry
+ * point would return (the "can_use" query of the tahou.com article, section
+ * SGLang扩散Kernel的验证流程).
+ */
+MBX_API int mbx_check_ln_modulate(const mbx_view* out, const mbx_cview* x, const mbx_cview* scale,
+                                  const mbx_cview* shift, float eps, int variant);
+MBX_API int mbx_check_rmsnorm_scale(const mbx_view* out, const mbx_cview* x,
+                                    const mbx_cview* weight, const mbx_cview* scale, float eps,
+                                    int variant);
+MBX_API int mbx_check_rmsnorm_tanh_residual(const mbx_view* out, const mbx_cview* x,
+                                            const mbx_cview* gate, const mbx_cview* residual,
+                                            const mbx_cview* weight, float eps, int variant);
+MBX_API int mbx_check_residual_gate_add(const mbx_view* out, const mbx_cview* x,
+                                        const mbx_cview* gate, const mbx_cview* y, int variant);
+MBX_API int mbx_check_qk_norm_rope_qkv_epilogue(
+    const mbx_view* joint, const mbx_cview* txt_qkv, const mbx_cview* img_qkv, int64_t batch,
+    int64_t heads, const mbx_cview* wq_txt, const mbx_cview* wk_txt, const mbx_cview* wq_img,
+    const mbx_cview* wk_img, const float* cos_txt, const float* sin_txt, const float* cos_img,
+    const float* sin_img, float eps, int variant);
+
+/*
+ * Exhaustive self-test of the kernels' arithmetic building blocks against the
+ * GPU's own correctly rounded binary32 operations (no counterpart on the
+ * pages; it backs the bit-exactness of the lossless paths):
+ *   which = 0: division by each Welford count k = 1..64 (the kernels'
+ *              double-word reciprocal with Markstein's correction) vs
+ *              div.rn, for every finite binary32 numerator;
+ *   which = 1: the bfloat16-pair multiply vs binary32 multiply + round, for
+ *              every pair of bfloat16 operands;
+ *   which = 2: the bfloat16-pair add vs binary32 add + round, every pair.
+ * counts: device pointer to 2 uint64 counters (caller-owned), overwritten
+ * with {mismatches between non-NaN results, mismatches where either is NaN}.
+ * Enqueued on `stream`; the caller synchronises before reading counts.
+ */
+MBX_API int mbx_selftest(int which, unsigned long long* counts, void* stream);
+
+/* Static name of a status code ("MBX_OK", "MBX_E_SHAPE: ..."). */
+MBX_API const char* mbx_status_string(int status);
+
+/* MBX_ABI_VERSION of the loaded library. */
+MBX_API int mbx_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MBX_H */

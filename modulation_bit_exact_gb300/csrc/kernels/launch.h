@@ -1,0 +1,96 @@
+// launch.h -- internal interface between the C ABI (mbx_api.cu) and the
+// kernel translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mbx {
+
+struct LnModParams {
+    uint16_t* out;
+    int64_t out_stride;
+    const uint16_t* x;
+    int64_t x_stride;
+    const uint16_t* scale;
+    int64_t scale_stride;
+    const uint16_t* shift;
+    int64_t shift_stride;
+    int64_t rows;
+    int D;
+    int64_t seq;  // rows / mod_rows: row r uses modulation row r / seq
+    float eps;
+};
+
+struct RmsScaleParams {
+    uint16_t* out;
+    int64_t out_stride;
+    const uint16_t* x;
+    int64_t x_stride;
+    const uint16_t* weight;
+    const uint16_t* scale;
+    int64_t scale_stride;
+    int64_t rows;
+    int D;
+    int64_t seq;
+    float eps;
+};
+
+struct RmsTanhParams {
+    uint16_t* out;
+    int64_t out_stride;
+    const uint16_t* x;
+    int64_t x_stride;
+    const uint16_t* gate;
+    int64_t gate_stride;
+    const uint16_t* residual;
+    int64_t res_stride;
+    const uint16_t* weight;
+    int64_t rows;
+    int D;
+    int64_t seq;
+    float eps;
+};
+
+struct GateAddParams {
+    uint16_t* out;
+    int64_t out_stride;
+    const uint16_t* x;
+    int64_t x_stride;
+    const uint16_t* gate;
+    int64_t gate_stride;
+    const uint16_t* y;
+    int64_t y_stride;
+    int64_t rows;
+    int D;
+    int64_t seq;
+};
+
+struct QkvParams {
+    uint16_t* joint;
+    const uint16_t* txt;
+    int64_t txt_stride;
+    const uint16_t* img;
+    int64_t img_stride;
+    int64_t s_txt, s_img, batch;
+    int heads, head_dim;
+    const uint16_t *wq_txt, *wk_txt, *wq_img, *wk_img;
+    const float *cos_txt, *sin_txt, *cos_img, *sin_img;
+    float eps;
+};
+
+// ceil(ceil(D / 8) / 128): chunks per lane of a row of D elements.
+inline int chunks_per_lane(int D) { return ((D + 7) / 8 + 127) / 128; }
+
+// Persistent grid size: min(ceil(units / units_per_block), SMs x resident
+// blocks of `kernel` at `block` threads); -1 if the runtime cannot tell.
+int grid_for_rows(const void* kernel, int64_t units, int units_per_block, int block);
+
+cudaError_t launch_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s);
+cudaError_t launch_rmsnorm_scale(const RmsScaleParams& p, bool vec, bool high, cudaStream_t s);
+cudaError_t launch_rmsnorm_tanh_residual(const RmsTanhParams& p, bool vec, bool high, cudaStream_t s);
+cudaError_t launch_residual_gate_add(const GateAddParams& p, bool vec, bool high, cudaStream_t s);
+cudaError_t launch_qkv_epilogue(const QkvParams& p, bool high, cudaStream_t s);
+cudaError_t launch_selftest(int which, unsigned long long* counts, cudaStream_t s);
+
+}  // namespace mbx

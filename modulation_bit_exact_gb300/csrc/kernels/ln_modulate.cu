@@ -1,0 +1,226 @@
+// ln_modulate.cu -- LayerNorm (no affine) fused with AdaLN modulate.
+//
+// "Agent-assisted SGLang diffusion kernel optimisation: Qwen-Image, FLUX.2 and
+// video models" (tahou.com), section 扩散Kernel对数值精度的敏感性:
+//   y = LN(x); y = y * (1 + scale) + shift
+// Lossless path (bit-exact to the eager BF16 chain, in the fixed order of
+// rowops.cuh):
+//   per lane, Welford over its elements: n += 1; d = x - mean;
+//     mean += d / n (correctly rounded, Markstein-corrected for the
+//     compile-time count); m2 += d * (x - mean)
+//   fixed tree of Chan combines; var = m2 / D; rstd = 1 / sqrt(var + eps)
+//   nrm = bf16((x - mean) * rstd)          (the BF16 store between LN and modulate)
+//   out = bf16(bf16(nrm * bf16(1 + scale)) + shift)
+// High path: the same formula in one binary32 pass (two-pass mean/variance
+// over registers, fused multiply-add allowed) with one rounding at the output.
+#include "launch.h"
+#include "rowops.cuh"
+
+namespace mbx {
+
+__device__ __forceinline__ u64 sel2(bool a, bool b, u64 n, u64 o) {
+    return f2(a ? f2lo(n) : f2lo(o), b ? f2hi(n) : f2hi(o));
+}
+
+// Welford statistics of every lane this thread owns.
+template <class C>
+__device__ __forceinline__ void welford_lanes(const uint4 (&v)[C::M][C::J], int t, int D,
+                                              Wf (&L)[C::M]) {
+    // elements left in the last chunk of each lane (<= 0: no last chunk)
+    int lim[C::M];
+#pragma unroll
+    for (int m = 0; m < C::M; ++m) lim[m] = D - kChunk * (t + C::TPR * m + kLanes * (C::J - 1));
+
+    if constexpr (C::M >= 2) {
+        constexpr int P = C::M / 2;  // lane pairs (m, m + P) share an f32x2
+        u64 mean[P], m2[P];
+#pragma unroll
+        for (int p = 0; p < P; ++p) mean[p] = m2[p] = f2(0.0f, 0.0f);
+        static_for<0, C::J>([&](auto jc) {
+            constexpr int j = decltype(jc)::value;
+            static_for<0, kChunk>([&](auto ec) {
+                constexpr int e = decltype(ec)::value;
+                constexpr int K = kChunk * j + e + 1;
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    u64 x = pair_elem(w_of(v[p][j], e / 2), w_of(v[p + P][j], e / 2), e & 1);
+                    if constexpr (j < C::J - 1) {
+                        welford_step2<K>(x, mean[p], m2[p]);
+                    } else {
+                        u64 mn = mean[p], q = m2[p];
+                        welford_step2<K>(x, mn, q);
+                        bool va = e < lim[p], vb = e < lim[p + P];
+                        mean[p] = sel2(va, vb, mn, mean[p]);
+                        m2[p] = sel2(va, vb, q, m2[p]);
+                    }
+                }
+            });
+        });
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            L[p].mean = f2lo(mean[p]);
+            L[p].m2 = f2lo(m2[p]);
+            L[p + P].mean = f2hi(mean[p]);
+            L[p + P].m2 = f2hi(m2[p]);
+        }
+    } else {
+        float mean = 0.0f, m2 = 0.0f;
+        static_for<0, C::J>([&](auto jc) {
+            constexpr int j = decltype(jc)::value;
+            static_for<0, kChunk>([&](auto ec) {
+                constexpr int e = decltype(ec)::value;
+                constexpr int K = kChunk * j + e + 1;
+                uint32_t w = w_of(v[0][j], e / 2);
+                float x = (e & 1) ? hi_f(w) : lo_f(w);
+                if constexpr (j < C::J - 1) {
+                    welford_step<K>(x, mean, m2);
+                } else {
+                    float mn = mean, q = m2;
+                    welford_step<K>(x, mn, q);
+                    if (e < lim[0]) {
+                        mean = mn;
+                        m2 = q;
+                    }
+                }
+            });
+        });
+        L[0].mean = mean;
+        L[0].m2 = m2;
+    }
+#pragma unroll
+    for (int m = 0; m < C::M; ++m) {
+        int last = lim[m] <= 0 ? 0 : (lim[m] >= kChunk ? kChunk : lim[m]);
+        L[m].n = (float)(kChunk * (C::J - 1) + last);
+    }
+}
+
+template <int TPR, int J, bool VEC, bool HIGH>
+__global__ void __launch_bounds__(kBlock) ln_modulate_kernel(LnModParams p) {
+    using C = RowCfg<TPR, J, VEC>;
+    __shared__ TreeSmem smem[C::RPC];
+    const RowLoop rl = row_loop<C>();
+    TreeSmem& sm = smem[rl.group];
+    const int D = p.D;
+    const int nch = (D + kChunk - 1) / kChunk;
+    const bool per_token = p.seq == 1;
+
+    for (int64_t row = rl.first; row < p.rows; row += rl.step) {
+        uint4 v[C::M][C::J];
+        load_row<C>(v, p.x + row * p.x_stride, rl.t, D, true);
+
+        float mean, rstd;
+        if constexpr (!HIGH) {
+            Wf L[C::M];
+            welford_lanes<C>(v, rl.t, D, L);
+            Wf s = tree_reduce<C>(L, rl.t, sm, rl.bar_id, wf_combine);
+            mean = s.mean;
+            if (rl.t == 0) {
+                float var = __fdiv_rn(s.m2, (float)D);
+                rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, p.eps)));
+            }
+        } else {
+            float acc[C::M];
+#pragma unroll
+            for (int m = 0; m < C::M; ++m) {
+                acc[m] = 0.0f;
+#pragma unroll
+                for (int j = 0; j < C::J; ++j)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t w = w_of(v[m][j], i);
+                        acc[m] += lo_f(w) + hi_f(w);
+                    }
+            }
+            float s = tree_reduce<C>(acc, rl.t, sm, rl.bar_id, sum_combine);
+            float dummy = 0.0f;
+            mean = s / (float)D;
+            group_bcast<C>(mean, dummy, rl.t, sm, rl.bar_id);
+#pragma unroll
+            for (int m = 0; m < C::M; ++m) {
+                acc[m] = 0.0f;
+                int lim = D - kChunk * (rl.t + C::TPR * m + kLanes * (C::J - 1));
+#pragma unroll
+                for (int j = 0; j < C::J; ++j)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t w = w_of(v[m][j], i);
+                        float d0 = lo_f(w) - mean, d1 = hi_f(w) - mean;
+                        if (j == C::J - 1) {
+                            d0 = 2 * i < lim ? d0 : 0.0f;
+                            d1 = 2 * i + 1 < lim ? d1 : 0.0f;
+                        }
+                        acc[m] += d0 * d0 + d1 * d1;
+                    }
+            }
+            float q = tree_reduce<C>(acc, rl.t, sm, rl.bar_id, sum_combine);
+            if (rl.t == 0) rstd = rsqrtf(q / (float)D + p.eps);
+        }
+        group_bcast<C>(mean, rstd, rl.t, sm, rl.bar_id);
+
+        const int64_t mrow = per_token ? row : row / p.seq;
+        const uint16_t* sc_row = p.scale + mrow * p.scale_stride;
+        const uint16_t* sh_row = p.shift + mrow * p.shift_stride;
+        uint16_t* out_row = p.out + row * p.out_stride;
+        const u64 mean2 = f2(mean, mean), rstd2 = f2(rstd, rstd);
+        const uint32_t one2 = 0x3f803f80u;
+#pragma unroll
+        for (int j = 0; j < C::J; ++j)
+#pragma unroll
+            for (int m = 0; m < C::M; ++m) {
+                int c = rl.t + C::TPR * m + kLanes * j;
+                if (c >= nch) continue;
+                uint4 sc = load_chunk<VEC>(sc_row, c, D, per_token);
+                uint4 sh = load_chunk<VEC>(sh_row, c, D, per_token);
+                uint4 o;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t xw = w_of(v[m][j], i), sw = w_of(sc, i), hw = w_of(sh, i);
+                    uint32_t ow;
+                    if constexpr (!HIGH) {
+                        uint32_t nrm = pack2_rn(mul2(sub2(widen2(xw), mean2), rstd2));
+                        ow = badd(bmul(nrm, badd(one2, sw)), hw);
+                    } else {
+                        float y0 = fmaf((lo_f(xw) - mean) * rstd, 1.0f + lo_f(sw), lo_f(hw));
+                        float y1 = fmaf((hi_f(xw) - mean) * rstd, 1.0f + hi_f(sw), hi_f(hw));
+                        ow = pack_rn(y0, y1);
+                    }
+                    w_set(o, i, ow);
+                }
+                store_chunk<VEC>(out_row, c, D, o);
+            }
+    }
+}
+
+// ------------------------------------------------------------------ host
+
+template <int TPR, int J, bool VEC, bool HIGH>
+static cudaError_t launch_one(const LnModParams& p, cudaStream_t s) {
+    auto k = ln_modulate_kernel<TPR, J, VEC, HIGH>;
+    int grid = grid_for_rows(reinterpret_cast<const void*>(k), p.rows, kBlock / TPR, kBlock);
+    if (grid < 0) return cudaErrorUnknown;
+    k<<<grid, kBlock, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int TPR, int J>
+static cudaError_t launch_j(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
+    if (vec) return high ? launch_one<TPR, J, true, true>(p, s) : launch_one<TPR, J, true, false>(p, s);
+    return high ? launch_one<TPR, J, false, true>(p, s) : launch_one<TPR, J, false, false>(p, s);
+}
+
+cudaError_t launch_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
+    const int J = chunks_per_lane(p.D);
+    switch (J) {
+        case 1: return launch_j<32, 1>(p, vec, high, s);
+        case 2: return launch_j<32, 2>(p, vec, high, s);
+        case 3: return launch_j<32, 3>(p, vec, high, s);
+        case 4: return launch_j<32, 4>(p, vec, high, s);
+        case 5: return launch_j<64, 5>(p, vec, high, s);
+        case 6: return launch_j<64, 6>(p, vec, high, s);
+        case 7: return launch_j<64, 7>(p, vec, high, s);
+        case 8: return launch_j<64, 8>(p, vec, high, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace mbx

@@ -1,0 +1,257 @@
+// numerics.cuh -- arithmetic building blocks of the sm_103a kernels.
+//
+// Every binary32 operation of a lossless path is an explicitly rounded PTX
+// instruction (add/sub/mul/fma/div/sqrt .rn), so no multiply-add is ever
+// contracted and no approximate instruction is used.  Two packed forms carry
+// most of the work:
+//   * f32x2 -- add/sub/mul/fma.rn.f32x2 operate on two independent binary32
+//     values in a 64-bit register pair (two Welford lanes, or two adjacent
+//     elements), each half rounded exactly like the scalar instruction.  A
+//     packed product is never fed to a packed sum: ptxas fuses that pair into
+//     one multiply-add even with explicit .rn and -fmad=false, so wherever a
+//     rounded product feeds a sum the scalar __fmul_rn / __fadd_rn intrinsics
+//     (documented never to be merged) are used instead;
+//   * bf16x2 -- mul/add.rn.bf16x2 compute bf16(a*b) and bf16(a+b) from the
+//     exact result.  For bfloat16 operands these equal rounding the binary32
+//     result to bfloat16 (the product of two 8-bit significands and the sum of
+//     two bfloat16 values are exact in binary32 except far below the smallest
+//     normal, where the intermediate grid is 2^16 times finer than bfloat16's
+//     and cannot create a new halfway case); mbx_selftest(1|2) checks this on
+//     every pair of operands.
+#pragma once
+
+#include <cstdint>
+#include <type_traits>
+
+namespace mbx {
+
+typedef unsigned long long u64;
+
+// ---------------------------------------------------------------- bfloat16
+
+// A 32-bit word holds two bfloat16 values: element 2i in the low half and
+// element 2i+1 in the high half (little-endian memory order).
+__device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// bf16 of two binary32 values, nearest-even; `lo` goes to the low half.
+__device__ __forceinline__ uint32_t pack_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t bmul(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t badd(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// The same two operations written as binary32 arithmetic plus one rounding:
+// the definition the packed instructions are checked against.
+__device__ __forceinline__ uint32_t bmul_ref(uint32_t a, uint32_t b) {
+    return pack_rn(__fmul_rn(lo_f(a), lo_f(b)), __fmul_rn(hi_f(a), hi_f(b)));
+}
+__device__ __forceinline__ uint32_t badd_ref(uint32_t a, uint32_t b) {
+    return pack_rn(__fadd_rn(lo_f(a), lo_f(b)), __fadd_rn(hi_f(a), hi_f(b)));
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(float v) {  // a bfloat16 splat (v exact in bf16)
+    uint32_t h = __float_as_uint(v) >> 16;
+    return h | (h << 16);
+}
+
+// ---------------------------------------------------------------- f32x2
+
+__device__ __forceinline__ u64 f2(float lo, float hi) {
+    u64 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float f2lo(u64 v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2hi(u64 v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ u64 add2(u64 a, u64 b) {
+    u64 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ u64 sub2(u64 a, u64 b) {
+    u64 r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
+    u64 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
+    u64 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// Two adjacent bfloat16 elements of a word, widened to an f32x2.
+__device__ __forceinline__ u64 widen2(uint32_t w) { return f2(lo_f(w), hi_f(w)); }
+// Element e (0/1) of word a and the same element of word b as an f32x2.
+__device__ __forceinline__ u64 pair_elem(uint32_t a, uint32_t b, int e) {
+    return e ? f2(hi_f(a), hi_f(b)) : f2(lo_f(a), lo_f(b));
+}
+__device__ __forceinline__ uint32_t pack2_rn(u64 v) { return pack_rn(f2lo(v), f2hi(v)); }
+
+// ---------------------------------------------------------------- division by k
+
+// Correctly rounded d / K for a compile-time count K (1 <= K <= 64).
+//   1. q0 = RN(d*yh + RN(d*yl)) with (yh, yl) a double-word reciprocal of K,
+//      yh = RN(1/K), yl ~ 1/K - yh: d*(yh + yl) is within about 2^-47 of d/K
+//      relative, so q0 is within an ulp of d/K (Brisebarre, Muller & Raina,
+//      "Accelerating correctly rounded floating-point division when the
+//      divisor is known in advance", IEEE Trans. Computers 53(8), 2004).
+//   2. Markstein's correction (P. Markstein, IBM J. Res. Dev. 34(1), 1990):
+//      with q0 within an ulp, r = d - q0*K is exact in one fused multiply-add
+//      and q = RN(q0 + r*yh) is RN(d/K).
+// The remainder of step 2 is exact only while d/K stays clear of the
+// subnormal range, so |d| < 2^-90 (zeros included) takes div.rn directly;
+// that branch is rare for real rows.  mbx_selftest(0) compares the result
+// with div.rn.f32 for every finite binary32 d and every K.  (A non-finite d
+// only occurs in a row whose mean and M2 are already inf/NaN, and every
+// output of such a row is the canonical NaN whatever the quotient's NaN/inf
+// value.)
+template <int K>
+struct Recip {
+    static_assert(K >= 1 && K <= 64, "Welford counts are 1..64");
+    static constexpr float yh = 1.0f / (float)K;
+    static constexpr float yl = (float)(1.0 / (double)K - (double)yh);
+    static constexpr float negk = -(float)K;
+};
+
+constexpr float kDivTiny = 0x1p-90f;
+
+template <int K>
+__device__ __forceinline__ float div_k(float d) {
+    if (fabsf(d) < kDivTiny) return __fdiv_rn(d, (float)K);
+    float q0 = __fmaf_rn(d, Recip<K>::yh, __fmul_rn(d, Recip<K>::yl));
+    float r = __fmaf_rn(q0, Recip<K>::negk, d);
+    return __fmaf_rn(r, Recip<K>::yh, q0);
+}
+
+template <int K>
+__device__ __forceinline__ u64 div_k2(u64 d) {
+    const float dl = f2lo(d), dh = f2hi(d);
+    if (fminf(fabsf(dl), fabsf(dh)) < kDivTiny) return f2(__fdiv_rn(dl, (float)K), __fdiv_rn(dh, (float)K));
+    const u64 yh = f2(Recip<K>::yh, Recip<K>::yh);
+    const u64 yl = f2(Recip<K>::yl, Recip<K>::yl);
+    const u64 nk = f2(Recip<K>::negk, Recip<K>::negk);
+    u64 q0 = fma2(d, yh, mul2(d, yl));
+    u64 r = fma2(q0, nk, d);
+    return fma2(r, yh, q0);
+}
+
+// ---------------------------------------------------------------- compile-time loops
+
+template <int I, int N, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+    if constexpr (I < N) {
+        f(std::integral_constant<int, I>{});
+        static_for<I + 1, N>(f);
+    }
+}
+
+// ---------------------------------------------------------------- Welford
+
+// One Welford step of count K on two lanes at once (x, mean, m2 as f32x2):
+//   d = x - mean; mean += d / K; m2 += d * (x - mean)
+template <int K>
+__device__ __forceinline__ void welford_step2(u64 x, u64& mean, u64& m2) {
+    u64 d = sub2(x, mean);
+    mean = add2(mean, div_k2<K>(d));
+    // The product feeding the sum uses the scalar __fmul_rn/__fadd_rn, which
+    // are never merged into a fused multiply-add; ptxas does fuse a packed
+    // mul.rn.f32x2 into a following add.rn.f32x2.
+    const u64 t = sub2(x, mean);
+    m2 = f2(__fadd_rn(f2lo(m2), __fmul_rn(f2lo(d), f2lo(t))),
+            __fadd_rn(f2hi(m2), __fmul_rn(f2hi(d), f2hi(t))));
+}
+
+template <int K>
+__device__ __forceinline__ void welford_step(float x, float& mean, float& m2) {
+    float d = __fsub_rn(x, mean);
+    mean = __fadd_rn(mean, div_k<K>(d));
+    m2 = __fadd_rn(m2, __fmul_rn(d, __fsub_rn(x, mean)));
+}
+
+struct Wf {
+    float mean, m2, n;
+};
+
+// Chan pairwise combine, a = lower lane:  n = na+nb; d = mb-ma; r = nb/n;
+// mean = ma + d*r; m2 = (qa+qb) + (d*d)*(na*r).  An empty side is an identity.
+__device__ __forceinline__ Wf wf_combine(Wf a, Wf b) {
+    if (b.n == 0.0f) return a;
+    if (a.n == 0.0f) return b;
+    Wf c;
+    c.n = __fadd_rn(a.n, b.n);
+    float d = __fsub_rn(b.mean, a.mean);
+    float r = __fdiv_rn(b.n, c.n);
+    c.mean = __fadd_rn(a.mean, __fmul_rn(d, r));
+    c.m2 = __fadd_rn(__fadd_rn(a.m2, b.m2), __fmul_rn(__fmul_rn(d, d), __fmul_rn(a.n, r)));
+    return c;
+}
+
+__device__ __forceinline__ Wf wf_shfl_down(Wf v, int s, unsigned mask = 0xffffffffu) {
+    Wf o;
+    o.mean = __shfl_down_sync(mask, v.mean, s);
+    o.m2 = __shfl_down_sync(mask, v.m2, s);
+    o.n = __shfl_down_sync(mask, v.n, s);
+    return o;
+}
+
+// ---------------------------------------------------------------- memory
+
+// 16-byte streaming load (read once: not kept in L1).
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+// 16-byte load of data shared by many rows (kept in L1).
+__device__ __forceinline__ uint4 ld_shared_row(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ uint16_t ld_u16(const void* p) {
+    uint16_t v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_u16(void* p, uint16_t v) {
+    asm volatile("st.global.u16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t w_of(const uint4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ void w_set(uint4& v, int i, uint32_t w) {
+    if (i == 0) v.x = w;
+    else if (i == 1) v.y = w;
+    else if (i == 2) v.z = w;
+    else v.w = w;
+}
+
+}  // namespace mbx

@@ -1,0 +1,87 @@
+// residual.cu -- gated residual add, out = bf16(x + bf16(gate * y)).
+//
+// "#34085 [diffusion] Clean up kernels and shared fast paths" (prhub.com.cn),
+// section 实现拆解 item 3 (the unified residual_gate_add entry); "AI Agent
+// 驱动的 SGLang Kernel 一等公民" (163.com), 3.2 (residual + gate·update).
+// Lossless: the product and the sum are each rounded to bfloat16, as the
+// eager chain x + gate * y does.  High: one fused multiply-add in binary32,
+// rounded once.
+#include "launch.h"
+#include "rowops.cuh"
+
+namespace mbx {
+
+template <int J, bool VEC, bool HIGH>
+__global__ void __launch_bounds__(kBlock) residual_gate_add_kernel(GateAddParams p) {
+    using C = RowCfg<128, J, VEC>;  // one 128-thread group per row, no reduction
+    const RowLoop rl = row_loop<C>();
+    const int D = p.D;
+    const int nch = (D + kChunk - 1) / kChunk;
+    const bool per_token = p.seq == 1;
+
+    for (int64_t row = rl.first; row < p.rows; row += rl.step) {
+        const uint16_t* x_row = p.x + row * p.x_stride;
+        const uint16_t* y_row = p.y + row * p.y_stride;
+        const uint16_t* g_row = p.gate + (per_token ? row : row / p.seq) * p.gate_stride;
+        uint16_t* out_row = p.out + row * p.out_stride;
+        uint4 xv[J], yv[J], gv[J];
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            int c = rl.t + kLanes * j;
+            if (c < nch) {
+                xv[j] = load_chunk<VEC>(x_row, c, D, true);
+                yv[j] = load_chunk<VEC>(y_row, c, D, true);
+                gv[j] = load_chunk<VEC>(g_row, c, D, per_token);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            int c = rl.t + kLanes * j;
+            if (c >= nch) continue;
+            uint4 o;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t xw = w_of(xv[j], i), yw = w_of(yv[j], i), gw = w_of(gv[j], i);
+                uint32_t ow;
+                if constexpr (!HIGH) {
+                    ow = badd(xw, bmul(gw, yw));
+                } else {
+                    ow = pack_rn(fmaf(lo_f(gw), lo_f(yw), lo_f(xw)), fmaf(hi_f(gw), hi_f(yw), hi_f(xw)));
+                }
+                w_set(o, i, ow);
+            }
+            store_chunk<VEC>(out_row, c, D, o);
+        }
+    }
+}
+
+template <int J, bool VEC, bool HIGH>
+static cudaError_t launch_one(const GateAddParams& p, cudaStream_t s) {
+    auto k = residual_gate_add_kernel<J, VEC, HIGH>;
+    int grid = grid_for_rows(reinterpret_cast<const void*>(k), p.rows, kBlock / 128, kBlock);
+    if (grid < 0) return cudaErrorUnknown;
+    k<<<grid, kBlock, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int J>
+static cudaError_t launch_j(const GateAddParams& p, bool vec, bool high, cudaStream_t s) {
+    if (vec) return high ? launch_one<J, true, true>(p, s) : launch_one<J, true, false>(p, s);
+    return high ? launch_one<J, false, true>(p, s) : launch_one<J, false, false>(p, s);
+}
+
+cudaError_t launch_residual_gate_add(const GateAddParams& p, bool vec, bool high, cudaStream_t s) {
+    switch (chunks_per_lane(p.D)) {
+        case 1: return launch_j<1>(p, vec, high, s);
+        case 2: return launch_j<2>(p, vec, high, s);
+        case 3: return launch_j<3>(p, vec, high, s);
+        case 4: return launch_j<4>(p, vec, high, s);
+        case 5: return launch_j<5>(p, vec, high, s);
+        case 6: return launch_j<6>(p, vec, high, s);
+        case 7: return launch_j<7>(p, vec, high, s);
+        case 8: return launch_j<8>(p, vec, high, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace mbx

@@ -1,0 +1,219 @@
+// rowops.cuh -- the row machinery shared by the norm kernels.
+//
+// A row of D bfloat16 values is cut into 8-element chunks (16 bytes); chunk c
+// belongs to logical lane c mod 128, and a lane visits its chunks in
+// ascending order.  A group of TPR threads (32, 64 or 128) owns one row at a
+// time: thread t holds the M = 128/TPR lanes t, t+TPR, ..., so for every
+// chunk index j the group's loads cover TPR consecutive chunks (coalesced
+// 128-bit accesses).  Per-lane results are combined by the fixed halving tree
+//   for s = 64, 32, ..., 1:  L[l] = combine(L[l], L[l+s])   (l < s)
+// realised as: levels s >= TPR inside a thread, 32 <= s < TPR through shared
+// memory between the group's warps, s < 32 by warp shuffles.  Every
+// realisation performs the same operations on the same operands, so the
+// result does not depend on TPR.
+//
+// The lane/chunk order and the tree follow the bit-exact LayerNorm
+// description of "Agent-assisted SGLang diffusion kernel optimisation:
+// Qwen-Image, FLUX.2 and video models" (tahou.com), section
+// 扩散Kernel对数值精度的敏感性 (a 128-thread Welford and a fixed shuffle tree).
+#pragma once
+
+#include "numerics.cuh"
+
+namespace mbx {
+
+constexpr int kLanes = 128;
+constexpr int kChunk = 8;
+constexpr int kBlock = 256;  // threads per CTA of the row kernels
+
+template <int TPR_, int J_, bool VEC_>
+struct RowCfg {
+    static constexpr int TPR = TPR_;          // threads per row group
+    static constexpr int J = J_;              // chunks per lane (max)
+    static constexpr int M = kLanes / TPR_;   // lanes per thread
+    static constexpr bool VEC = VEC_;         // 128-bit accesses allowed
+    static constexpr int RPC = kBlock / TPR_; // row groups per CTA
+    static_assert(TPR_ == 32 || TPR_ == 64 || TPR_ == 128, "TPR");
+};
+
+// Shared memory of one row group for the cross-warp tree levels.
+struct TreeSmem {
+    float a64[3][64];
+    float a32[3][32];
+    float bcast[4];
+};
+
+__device__ __forceinline__ void group_bar(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Chunk c of a row: 8 elements, zero-filled past D.
+template <bool VEC>
+__device__ __forceinline__ uint4 load_chunk(const uint16_t* row, int c, int D, bool stream) {
+    if constexpr (VEC) {
+        const uint16_t* p = row + (int64_t)c * kChunk;
+        return stream ? ld_stream(p) : ld_shared_row(p);
+    } else {
+        uint4 v = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            int e0 = c * kChunk + 2 * i;
+            uint32_t lo = e0 < D ? ld_u16(row + e0) : 0u;
+            uint32_t hi = e0 + 1 < D ? ld_u16(row + e0 + 1) : 0u;
+            w_set(v, i, lo | (hi << 16));
+        }
+        return v;
+    }
+}
+
+template <bool VEC>
+__device__ __forceinline__ void store_chunk(uint16_t* row, int c, int D, uint4 v) {
+    if constexpr (VEC) {
+        st_v4(row + (int64_t)c * kChunk, v);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            int e0 = c * kChunk + 2 * i;
+            uint32_t w = w_of(v, i);
+            if (e0 < D) st_u16(row + e0, (uint16_t)(w & 0xffffu));
+            if (e0 + 1 < D) st_u16(row + e0 + 1, (uint16_t)(w >> 16));
+        }
+    }
+}
+
+// Elements of chunk c that exist (0..8).
+__device__ __forceinline__ int chunk_len(int c, int D) {
+    int n = D - c * kChunk;
+    return n <= 0 ? 0 : (n >= kChunk ? kChunk : n);
+}
+
+// Number of elements of lane l (its count in the Welford / sum).
+__device__ __forceinline__ int lane_count(int l, int D) {
+    int nch = (D + kChunk - 1) / kChunk;
+    if (l >= nch) return 0;
+    int full = (nch - 1 - l) / kLanes;  // chunks of lane l before its last one
+    return full * kChunk + chunk_len(l + full * kLanes, D);
+}
+
+// Load every chunk of the row owned by this thread: v[m][j] is chunk
+// t + TPR*m + 128*j.
+template <class C>
+__device__ __forceinline__ void load_row(uint4 (&v)[C::M][C::J], const uint16_t* row, int t, int D,
+                                         bool stream) {
+    const int nch = (D + kChunk - 1) / kChunk;
+#pragma unroll
+    for (int j = 0; j < C::J; ++j)
+#pragma unroll
+        for (int m = 0; m < C::M; ++m) {
+            int c = t + C::TPR * m + kLanes * j;
+            v[m][j] = c < nch ? load_chunk<C::VEC>(row, c, D, stream) : make_uint4(0, 0, 0, 0);
+        }
+}
+
+// ------------------------------------------------------------------ tree
+
+__device__ __forceinline__ float sum_combine(float a, float b) { return __fadd_rn(a, b); }
+
+__device__ __forceinline__ float shfl_down_t(float v, int s) { return __shfl_down_sync(0xffffffffu, v, s); }
+__device__ __forceinline__ Wf shfl_down_t(Wf v, int s) { return wf_shfl_down(v, s); }
+
+__device__ __forceinline__ void smem_put(float (&a)[3][64], int i, float v) { a[0][i] = v; }
+__device__ __forceinline__ void smem_put(float (&a)[3][64], int i, Wf v) {
+    a[0][i] = v.mean; a[1][i] = v.m2; a[2][i] = v.n;
+}
+__device__ __forceinline__ void smem_get(const float (&a)[3][64], int i, float& v) { v = a[0][i]; }
+__device__ __forceinline__ void smem_get(const float (&a)[3][64], int i, Wf& v) {
+    v.mean = a[0][i]; v.m2 = a[1][i]; v.n = a[2][i];
+}
+__device__ __forceinline__ void smem_put32(float (&a)[3][32], int i, float v) { a[0][i] = v; }
+__device__ __forceinline__ void smem_put32(float (&a)[3][32], int i, Wf v) {
+    a[0][i] = v.mean; a[1][i] = v.m2; a[2][i] = v.n;
+}
+__device__ __forceinline__ void smem_get32(const float (&a)[3][32], int i, float& v) { v = a[0][i]; }
+__device__ __forceinline__ void smem_get32(const float (&a)[3][32], int i, Wf& v) {
+    v.mean = a[0][i]; v.m2 = a[1][i]; v.n = a[2][i];
+}
+
+// Reduce the M per-lane values of every thread of the group along the fixed
+// tree.  The returned value is meaningful in group thread 0 only.
+template <class C, class T, class Comb>
+__device__ __forceinline__ T tree_reduce(T (&L)[C::M], int t, TreeSmem& sm, int bar_id, Comb comb) {
+    // levels inside the thread: lane t+TPR*m with lane t+TPR*(m + s/TPR)
+#pragma unroll
+    for (int s = 64; s >= C::TPR; s /= 2) {
+        constexpr int dummy = 0;
+        (void)dummy;
+#pragma unroll
+        for (int m = 0; m < s / C::TPR; ++m) L[m] = comb(L[m], L[m + s / C::TPR]);
+    }
+    T v = L[0];
+    // levels between warps of the group
+    if constexpr (C::TPR == 128) {
+        if (t >= 64) smem_put(sm.a64, t - 64, v);
+        group_bar(bar_id, C::TPR);
+        if (t < 64) {
+            T o;
+            smem_get(sm.a64, t, o);
+            v = comb(v, o);
+        }
+        if (t >= 32 && t < 64) smem_put32(sm.a32, t - 32, v);
+        group_bar(bar_id, C::TPR);
+        if (t < 32) {
+            T o;
+            smem_get32(sm.a32, t, o);
+            v = comb(v, o);
+        }
+    } else if constexpr (C::TPR == 64) {
+        if (t >= 32) smem_put32(sm.a32, t - 32, v);
+        group_bar(bar_id, C::TPR);
+        if (t < 32) {
+            T o;
+            smem_get32(sm.a32, t, o);
+            v = comb(v, o);
+        }
+    }
+    // levels inside the first warp
+    if (t < 32) {
+#pragma unroll
+        for (int s = 16; s >= 1; s /= 2) v = comb(v, shfl_down_t(v, s));
+    }
+    return v;
+}
+
+// Make two floats computed by group thread 0 visible to the whole group.
+template <class C>
+__device__ __forceinline__ void group_bcast(float& a, float& b, int t, TreeSmem& sm, int bar_id) {
+    if constexpr (C::TPR == 32) {
+        a = __shfl_sync(0xffffffffu, a, 0);
+        b = __shfl_sync(0xffffffffu, b, 0);
+    } else {
+        if (t == 0) {
+            sm.bcast[0] = a;
+            sm.bcast[1] = b;
+        }
+        group_bar(bar_id, C::TPR);
+        a = sm.bcast[0];
+        b = sm.bcast[1];
+    }
+}
+
+// Grid-wide row-group loop parameters.
+struct RowLoop {
+    int t;       // thread index within the row group
+    int group;   // row group within the CTA
+    int bar_id;  // named barrier of the group (1..RPC)
+    int64_t first, step;
+};
+
+template <class C>
+__device__ __forceinline__ RowLoop row_loop() {
+    RowLoop r;
+    r.t = threadIdx.x % C::TPR;
+    r.group = threadIdx.x / C::TPR;
+    r.bar_id = 1 + r.group;
+    r.first = (int64_t)blockIdx.x * C::RPC + r.group;
+    r.step = (int64_t)gridDim.x * C::RPC;
+    return r;
+}
+
+}  // namespace mbx

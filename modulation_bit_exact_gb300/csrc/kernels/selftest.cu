@@ -1,0 +1,83 @@
+// selftest.cu -- exhaustive checks of the arithmetic building blocks that the
+// lossless kernels rely on, against the GPU's own correctly rounded binary32
+// operations:
+//   0: div_k<K>(d) (double-word reciprocal + Markstein correction) ==
+//      div.rn(d, K) for K = 1..64 and every finite binary32 d;
+//   1: mul.rn.bf16x2 == binary32 multiply then round, every operand pair;
+//   2: add.rn.bf16x2 == binary32 add then round, every operand pair.
+// A mismatch where either result is a NaN is counted apart from the others:
+// NaN payloads never reach a bfloat16 output except as the canonical NaN.
+#include "launch.h"
+#include "numerics.cuh"
+
+namespace mbx {
+
+__device__ __forceinline__ bool is_nan32(uint32_t u) { return (u & 0x7fffffffu) > 0x7f800000u; }
+__device__ __forceinline__ bool is_nan16(uint32_t h) { return (h & 0x7fffu) > 0x7f80u; }
+
+__global__ void selftest_div_kernel(unsigned long long* counts) {
+    unsigned long long bad = 0, bad_nan = 0;
+    const uint64_t total = 1ull << 32;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (uint64_t)gridDim.x * blockDim.x) {
+        const float d = __uint_as_float((uint32_t)i);
+        if (!isfinite(d)) continue;  // finite numerators only (see numerics.cuh)
+        static_for<1, 65>([&](auto kc) {
+            constexpr int K = decltype(kc)::value;
+            uint32_t got = __float_as_uint(div_k<K>(d));
+            uint32_t want = __float_as_uint(__fdiv_rn(d, (float)K));
+            if (got != want) {
+                if (is_nan32(got) || is_nan32(want)) ++bad_nan;
+                else ++bad;
+            }
+        });
+    }
+    if (bad) atomicAdd(&counts[0], bad);
+    if (bad_nan) atomicAdd(&counts[1], bad_nan);
+}
+
+// Every (a, b) pair of bfloat16 operands: a = i >> 16, b = i & 0xffff packed
+// as (a,b) and (b,a) in the two halves, so both halves see every pair.
+template <bool MUL>
+__global__ void selftest_bf16x2_kernel(unsigned long long* counts) {
+    unsigned long long bad = 0, bad_nan = 0;
+    const uint64_t total = 1ull << 32;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (uint64_t)gridDim.x * blockDim.x) {
+        const uint32_t a = (uint32_t)(i >> 16), b = (uint32_t)(i & 0xffffu);
+        const uint32_t A = a | (b << 16), B = b | (a << 16);
+        const uint32_t got = MUL ? bmul(A, B) : badd(A, B);
+        const uint32_t want = MUL ? bmul_ref(A, B) : badd_ref(A, B);
+        if (got != want) {
+            uint32_t x = got ^ want;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t sh = 16 * h;
+                if ((x >> sh) & 0xffffu) {
+                    if (is_nan16((got >> sh) & 0xffffu) || is_nan16((want >> sh) & 0xffffu)) ++bad_nan;
+                    else ++bad;
+                }
+            }
+        }
+    }
+    if (bad) atomicAdd(&counts[0], bad);
+    if (bad_nan) atomicAdd(&counts[1], bad_nan);
+}
+
+cudaError_t launch_selftest(int which, unsigned long long* counts, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(counts, 0, 2 * sizeof(unsigned long long), s);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int grid = sms * 8, block = 256;
+    switch (which) {
+        case 0: selftest_div_kernel<<<grid, block, 0, s>>>(counts); break;
+        case 1: selftest_bf16x2_kernel<true><<<grid, block, 0, s>>>(counts); break;
+        case 2: selftest_bf16x2_kernel<false><<<grid, block, 0, s>>>(counts); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace mbx

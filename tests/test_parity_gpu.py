@@ -1,0 +1,205 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Lossless variants: every element equal bit for bit.  High variants: within 2
+bfloat16 ulps of the largest term of the exact binary64 result (the single-pass
+error budget stated for them), see gpu_util.assert_high_close.
+Inputs come from the seeded generators in synth/, outputs of the oracle from
+oracle/; nothing the CUDA path computes feeds the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.gpu_util import assert_bits_equal, assert_high_close, guarded, u16
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def mbx():
+    import modulation_bit_exact_gb300 as m
+    m.lib()
+    return m
+
+
+def _rows2(t):
+    return u16(t).reshape(-1, t.shape[-1])
+
+
+# ------------------------------------------------------------------ configs 1, 2
+
+
+def test_tiny_ln_modulate_and_rmsnorm_scale(mbx):
+    d = synth.tiny_ln_modulate()
+    x, sc, sh, w = (d[k].to(DEV) for k in ("x", "scale", "shift", "weight"))
+    X, SC, SH, W = _rows2(d["x"]), u16(d["scale"]), u16(d["shift"]), u16(d["weight"])
+    assert_bits_equal(u16(mbx.ln_modulate(x, sc, sh)), oracle.ln_modulate(X, SC, SH, 1e-6).reshape(2, 256, 512), "ln")
+    assert_bits_equal(u16(mbx.rmsnorm_scale(x, w, sc)), oracle.rmsnorm_scale(X, W, SC, 1e-6).reshape(2, 256, 512), "rms")
+    ex, mag = oracle.ln_modulate_f64(X, SC, SH, 1e-6)
+    assert_high_close(_rows2(mbx.ln_modulate(x, sc, sh, variant="high")), ex, mag, what="ln high")
+    ex, mag = oracle.rmsnorm_scale_f64(X, W, SC, 1e-6)
+    assert_high_close(_rows2(mbx.rmsnorm_scale(x, w, sc, variant="high")), ex, mag, what="rms high")
+
+
+def test_image_dit_block_full_size(mbx):
+    """Image-DiT norm path at its full size, as the benchmark runs it."""
+    d = synth.image_dit_block()
+    x, sc, sh, g, y = (d[k].to(DEV) for k in ("x", "scale", "shift", "gate", "y"))
+    X, SC, SH, G, Y = _rows2(d["x"]), u16(d["scale"]), u16(d["shift"]), u16(d["gate"]), _rows2(d["y"])
+    assert_bits_equal(_rows2(mbx.ln_modulate(x, sc, sh)), oracle.ln_modulate(X, SC, SH, 1e-6), "ln")
+    assert_bits_equal(_rows2(mbx.residual_gate_add(x, g, y)), oracle.residual_gate_add(X, G, Y), "rga")
+    rows = np.r_[0:64, 4352 - 32:4352 + 32, 8704 - 64:8704]
+    ex, mag = oracle.ln_modulate_f64(X[rows], SC[rows // 4352], SH[rows // 4352], 1e-6)
+    assert_high_close(_rows2(mbx.ln_modulate(x, sc, sh, variant="high"))[rows], ex, mag, what="ln high")
+    ex, mag = oracle.residual_gate_add_f64(X, G, Y)
+    assert_high_close(_rows2(mbx.residual_gate_add(x, g, y, variant="high")), ex, mag, what="rga high")
+
+
+# ------------------------------------------------------------------ config 3
+
+
+def _qkv_gpu(mbx, q, variant="lossless", out=None):
+    qd = {k: (v.to(DEV) if torch.is_tensor(v) else v) for k, v in q.items()}
+    return mbx.qk_norm_rope_qkv_epilogue(
+        qd["txt"], qd["img"], q["batch"], q["heads"], q["head_dim"], qd["wq_txt"], qd["wk_txt"],
+        qd["wq_img"], qd["wk_img"], qd["cos_txt"], qd["sin_txt"], qd["cos_img"], qd["sin_img"],
+        q["eps"], variant=variant, out=out)
+
+
+def _qkv_oracle(q):
+    return oracle.qkv_epilogue(
+        None if q["txt"] is None else u16(q["txt"]), u16(q["img"]), q["batch"], q["heads"],
+        q["head_dim"], u16(q["wq_txt"]), u16(q["wk_txt"]), u16(q["wq_img"]), u16(q["wk_img"]),
+        q["cos_txt"].numpy(), q["sin_txt"].numpy(), q["cos_img"].numpy(), q["sin_img"].numpy(),
+        q["eps"])
+
+
+def test_qkv_epilogue_full_size(mbx):
+    q = synth.qkv_epilogue_case()
+    assert_bits_equal(u16(_qkv_gpu(mbx, q)), _qkv_oracle(q), "joint")
+
+
+def _qkv_high_check(mbx, q):
+    got = u16(_qkv_gpu(mbx, q, variant="high"))
+    want = _qkv_oracle(q)
+    B, H, hd = q["batch"], q["heads"], q["head_dim"]
+    assert np.array_equal(got[:, 2], want[:, 2])  # V is a copy in both variants
+    s_txt = q["txt"].shape[0] // B
+    for b in range(B):
+        for part in (0, 1):
+            for h in range(H):
+                for name, S, off, w in (("txt", s_txt, 0, "wq_txt" if part == 0 else "wk_txt"),
+                                        ("img", q["img"].shape[0] // B, s_txt, "wq_img" if part == 0 else "wk_img")):
+                    src = u16(q[name]).reshape(B, S, 3, H, hd)
+                    tab = "txt" if name == "txt" else "img"
+                    for s in range(0, S, max(1, S // 7)):
+                        ex, mag = oracle.qk_head_f64(src[b, s, part, h], u16(q[w]),
+                                                     q["cos_" + tab][s].numpy(), q["sin_" + tab][s].numpy())
+                        assert_high_close(got[b, part, h, off + s], ex, mag, what="qkv high")
+
+
+def test_qkv_epilogue_high(mbx):
+    _qkv_high_check(mbx, synth.qkv_epilogue_case(batch=2, s_txt=16, grid_h=8, grid_w=8, heads=6))
+
+
+@pytest.mark.parametrize("hd,heads,pad", [(64, 3, 0), (64, 8, 64), (128, 5, 8), (256, 2, 0), (256, 7, 24)])
+def test_qkv_epilogue_shapes(mbx, hd, heads, pad):
+    q = synth.qkv_epilogue_case(batch=3, s_txt=9, grid_h=5, grid_w=7, heads=heads, head_dim=hd, row_pad=pad)
+    assert_bits_equal(u16(_qkv_gpu(mbx, q)), _qkv_oracle(q), f"hd={hd} H={heads}")
+
+
+def test_qkv_epilogue_image_only_and_guard_zone(mbx):
+    q = synth.qkv_epilogue_case(batch=2, s_txt=3, grid_h=4, grid_w=4, heads=4)
+    q["txt"] = None
+    q["cos_txt"] = q["sin_txt"] = torch.zeros(0, 64)
+    out, check = guarded((2, 3, 4, 16, 128), DEV)
+    _qkv_gpu(mbx, q, out=out)
+    torch.cuda.synchronize()
+    check()
+    assert_bits_equal(u16(out), _qkv_oracle(q), "image only")
+
+
+# ------------------------------------------------------------------ config 4
+
+
+def _sample_rows(T, n=384, seed=0):
+    rng = np.random.default_rng(seed)
+    r = np.unique(np.r_[0, 1, T // 2, T - 2, T - 1, rng.integers(0, T, size=n)])
+    return r[(r >= 0) & (r < T)]
+
+
+def test_video_dit_per_token_full_size(mbx):
+    d = synth.video_dit_block(device=DEV)
+    x, sc, sh, g, r, w = (d[k] for k in ("x", "scale", "shift", "gate", "residual", "weight"))
+    rows = _sample_rows(32760)
+    idx = torch.from_numpy(rows).to(DEV)
+
+    def pick(t):
+        return u16(t.reshape(-1, 5120).index_select(0, idx))
+
+    X, SC, SH, G, R, W = pick(x), pick(sc), pick(sh), pick(g), pick(r), u16(w)
+    out = mbx.ln_modulate(x, sc, sh)
+    assert_bits_equal(pick(out), oracle.ln_modulate(X, SC, SH, 1e-6), "ln per-token")
+    out = mbx.rmsnorm_tanh_residual(x, g, r, w)
+    assert_bits_equal(pick(out), oracle.rmsnorm_tanh_residual(X, G, R, W, 1e-6), "tanh residual")
+    ex, mag = oracle.ln_modulate_f64(X, SC, SH, 1e-6)
+    assert_high_close(pick(mbx.ln_modulate(x, sc, sh, variant="high")), ex, mag, what="ln high")
+    ex, mag = oracle.rmsnorm_tanh_residual_f64(X, G, R, W, 1e-6)
+    assert_high_close(pick(mbx.rmsnorm_tanh_residual(x, g, r, w, variant="high")), ex, mag,
+                      what="tanh residual high")
+
+
+# ------------------------------------------------------------------ config 5 (sweep)
+
+
+def _sweep_ops(mbx, d, rows=None, variant="lossless"):
+    """Run all four row operations on a sweep cell; returns {op: (gpu bits, oracle thunk)}."""
+    x, y, gt, r, sc, sh, g, w = (d[k] for k in ("x", "y", "gate_tok", "residual", "scale", "shift", "gate", "weight"))
+    T, D = x.shape
+    sel = slice(None) if rows is None else rows
+    pick = (lambda t: u16(t)[sel]) if rows is None else (lambda t: u16(t.index_select(0, torch.from_numpy(rows).to(t.device))))
+    xs, ys, gts, rs = pick(x), pick(y), pick(gt), pick(r)
+    SC, SH, G, W = u16(sc), u16(sh), u16(g), u16(w)
+    res = {}
+    res["ln_modulate"] = (pick(mbx.ln_modulate(x, sc, sh, variant=variant)),
+                          lambda: oracle.ln_modulate(xs, SC, SH, 1e-6),
+                          lambda: oracle.ln_modulate_f64(xs, SC, SH, 1e-6))
+    res["rmsnorm_scale"] = (pick(mbx.rmsnorm_scale(x, w, sc, variant=variant)),
+                            lambda: oracle.rmsnorm_scale(xs, W, SC, 1e-6),
+                            lambda: oracle.rmsnorm_scale_f64(xs, W, SC, 1e-6))
+    res["rmsnorm_tanh_residual"] = (pick(mbx.rmsnorm_tanh_residual(x, gt, r, w, variant=variant)),
+                                    lambda: oracle.rmsnorm_tanh_residual(xs, gts, rs, W, 1e-6),
+                                    lambda: oracle.rmsnorm_tanh_residual_f64(xs, gts, rs, W, 1e-6))
+    res["residual_gate_add"] = (pick(mbx.residual_gate_add(x, g, y, variant=variant)),
+                                lambda: oracle.residual_gate_add(xs, G, ys),
+                                lambda: oracle.residual_gate_add_f64(xs, G, ys))
+    return res
+
+
+@pytest.mark.parametrize("D", synth.SWEEP_D)
+@pytest.mark.parametrize("T", synth.SWEEP_T)
+def test_sweep(mbx, D, T):
+    big = T * D > 64 * 1024 * 1024
+    d = synth.sweep_case(D, T, device=DEV if big else "cpu")
+    if not big:
+        d = {k: (v.to(DEV) if torch.is_tensor(v) else v) for k, v in d.items()}
+    rows = _sample_rows(T, n=96, seed=D) if big else None
+    for name, (got, want, _) in _sweep_ops(mbx, d, rows).items():
+        assert_bits_equal(got, want(), f"{name} D={D} T={T}")
+    rows_h = rows if big else _sample_rows(T, n=48, seed=D)
+    for name, (got, _, exact) in _sweep_ops(mbx, d, rows_h, variant="high").items():
+        ex, mag = exact()
+        assert_high_close(got, ex, mag, what=f"{name} high D={D} T={T}")
+
+
+@pytest.mark.parametrize("D", [1024, 4096, 8192])
+def test_sweep_qkv(mbx, D):
+    """The epilogue on sweep hidden sizes: H = D/128 heads of 128, a square-ish
+    image grid, 77 text tokens, padded rows."""
+    h, w = synth.grid_for(256)
+    q = synth.qkv_epilogue_case(batch=1, s_txt=77, grid_h=h, grid_w=w, heads=D // 128, row_pad=64)
+    assert_bits_equal(u16(_qkv_gpu(mbx, q)), _qkv_oracle(q), f"qkv D={D}")
