@@ -212,7 +212,11 @@ MBX_API int mbx_check_qk_norm_rope_qkv_epilogue(
  *              div.rn, for every finite binary32 numerator;
  *   which = 1: the bfloat16-pair multiply vs binary32 multiply + round, for
  *              every pair of bfloat16 operands;
- *   which = 2: the bfloat16-pair add vs binary32 add + round, every pair.
+ *   which = 2: the bfloat16-pair add vs binary32 add + round, every pair;
+ *   which = 3: the unguarded division the kernels use for lanes whose
+ *              elements all have |x| >= 2^-60, vs div.rn, for every count
+ *              k = 1..64 and every binary32 numerator with |d| >= 2^-100,
+ *              and +0.
  * counts: device pointer to 2 uint64 counters (caller-owned), overwritten
  * with {mismatches between non-NaN results, mismatches where either is NaN}.
  * Enqueued on `stream`; the caller synchronises before reading counts.

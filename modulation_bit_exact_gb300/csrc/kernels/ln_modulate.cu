@@ -22,8 +22,9 @@ __device__ __forceinline__ u64 sel2(bool a, bool b, u64 n, u64 o) {
     return f2(a ? f2lo(n) : f2lo(o), b ? f2hi(n) : f2hi(o));
 }
 
-// Welford statistics of every lane this thread owns.
-template <class C>
+// Welford statistics of every lane this thread owns (GUARD: division safe for
+// any d; otherwise the fast division, for lanes that pass lanes_plain).
+template <class C, bool GUARD>
 __device__ __forceinline__ void welford_lanes(const uint4 (&v)[C::M][C::J], int t, int D,
                                               Wf (&L)[C::M]) {
     // elements left in the last chunk of each lane (<= 0: no last chunk)
@@ -45,10 +46,10 @@ __device__ __forceinline__ void welford_lanes(const uint4 (&v)[C::M][C::J], int 
                 for (int p = 0; p < P; ++p) {
                     u64 x = pair_elem(w_of(v[p][j], e / 2), w_of(v[p + P][j], e / 2), e & 1);
                     if constexpr (j < C::J - 1) {
-                        welford_step2<K>(x, mean[p], m2[p]);
+                        welford_step2<K, GUARD>(x, mean[p], m2[p]);
                     } else {
                         u64 mn = mean[p], q = m2[p];
-                        welford_step2<K>(x, mn, q);
+                        welford_step2<K, GUARD>(x, mn, q);
                         bool va = e < lim[p], vb = e < lim[p + P];
                         mean[p] = sel2(va, vb, mn, mean[p]);
                         m2[p] = sel2(va, vb, q, m2[p]);
@@ -73,10 +74,10 @@ __device__ __forceinline__ void welford_lanes(const uint4 (&v)[C::M][C::J], int 
                 uint32_t w = w_of(v[0][j], e / 2);
                 float x = (e & 1) ? hi_f(w) : lo_f(w);
                 if constexpr (j < C::J - 1) {
-                    welford_step<K>(x, mean, m2);
+                    welford_step<K, GUARD>(x, mean, m2);
                 } else {
                     float mn = mean, q = m2;
-                    welford_step<K>(x, mn, q);
+                    welford_step<K, GUARD>(x, mn, q);
                     if (e < lim[0]) {
                         mean = mn;
                         m2 = q;
@@ -111,7 +112,8 @@ __global__ void __launch_bounds__(kBlock) ln_modulate_kernel(LnModParams p) {
         float mean, rstd;
         if constexpr (!HIGH) {
             Wf L[C::M];
-            welford_lanes<C>(v, rl.t, D, L);
+            if (lanes_plain<C>(v, rl.t, nch)) welford_lanes<C, false>(v, rl.t, D, L);
+            else welford_lanes<C, true>(v, rl.t, D, L);
             Wf s = tree_reduce<C>(L, rl.t, sm, rl.bar_id, wf_combine);
             mean = s.mean;
             if (rl.t == 0) {
@@ -211,14 +213,15 @@ static cudaError_t launch_j(const LnModParams& p, bool vec, bool high, cudaStrea
 cudaError_t launch_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
     const int J = chunks_per_lane(p.D);
     switch (J) {
+        // threads per row: enough that a thread holds at most ~5 chunks of x
         case 1: return launch_j<32, 1>(p, vec, high, s);
         case 2: return launch_j<32, 2>(p, vec, high, s);
-        case 3: return launch_j<32, 3>(p, vec, high, s);
-        case 4: return launch_j<32, 4>(p, vec, high, s);
+        case 3: return launch_j<64, 3>(p, vec, high, s);
+        case 4: return launch_j<64, 4>(p, vec, high, s);
         case 5: return launch_j<64, 5>(p, vec, high, s);
-        case 6: return launch_j<64, 6>(p, vec, high, s);
-        case 7: return launch_j<64, 7>(p, vec, high, s);
-        case 8: return launch_j<64, 8>(p, vec, high, s);
+        case 6: return launch_j<128, 6>(p, vec, high, s);
+        case 7: return launch_j<128, 7>(p, vec, high, s);
+        case 8: return launch_j<128, 8>(p, vec, high, s);
         default: return cudaErrorInvalidValue;
     }
 }

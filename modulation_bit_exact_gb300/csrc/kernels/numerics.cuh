@@ -97,6 +97,12 @@ __device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
     return r;
 }
 
+__device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // Two adjacent bfloat16 elements of a word, widened to an f32x2.
 __device__ __forceinline__ u64 widen2(uint32_t w) { return f2(lo_f(w), hi_f(w)); }
 // Element e (0/1) of word a and the same element of word b as an f32x2.
@@ -107,50 +113,54 @@ __device__ __forceinline__ uint32_t pack2_rn(u64 v) { return pack_rn(f2lo(v), f2
 
 // ---------------------------------------------------------------- division by k
 
-// Correctly rounded d / K for a compile-time count K (1 <= K <= 64).
-//   1. q0 = RN(d*yh + RN(d*yl)) with (yh, yl) a double-word reciprocal of K,
-//      yh = RN(1/K), yl ~ 1/K - yh: d*(yh + yl) is within about 2^-47 of d/K
-//      relative, so q0 is within an ulp of d/K (Brisebarre, Muller & Raina,
-//      "Accelerating correctly rounded floating-point division when the
-//      divisor is known in advance", IEEE Trans. Computers 53(8), 2004).
-//   2. Markstein's correction (P. Markstein, IBM J. Res. Dev. 34(1), 1990):
-//      with q0 within an ulp, r = d - q0*K is exact in one fused multiply-add
-//      and q = RN(q0 + r*yh) is RN(d/K).
-// The remainder of step 2 is exact only while d/K stays clear of the
-// subnormal range, so |d| < 2^-90 (zeros included) takes div.rn directly;
-// that branch is rare for real rows.  mbx_selftest(0) compares the result
-// with div.rn.f32 for every finite binary32 d and every K.  (A non-finite d
-// only occurs in a row whose mean and M2 are already inf/NaN, and every
-// output of such a row is the canonical NaN whatever the quotient's NaN/inf
-// value.)
+// Correctly rounded d / K for a compile-time count K (1 <= K <= 64), by
+// Markstein's correction (P. Markstein, "Computation of elementary functions
+// on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990; also
+// Cornea-Hasegan, Golliver & Markstein, ARITH-14, 1999): with yh = RN(1/K),
+// q0 = RN(d*yh), the remainder r = d - q0*K is exact in one fused
+// multiply-add and q = RN(q0 + r*yh) is RN(d/K).  The exact remainder needs
+// d/K clear of the subnormal range: exhaustively, on this GPU, the fast form
+// equals div.rn.f32 for every K and every d with |d| >= 2^-100 and for
+// d = +0 (mbx_selftest(3)); the guarded form sends |d| < 2^-90 (zeros
+// included) to div.rn and equals it for every finite d (mbx_selftest(0)).
+// (A non-finite d only occurs in a row whose mean and M2 are already inf/NaN;
+// every output of such a row is the canonical NaN whatever the quotient.)
 template <int K>
 struct Recip {
     static_assert(K >= 1 && K <= 64, "Welford counts are 1..64");
     static constexpr float yh = 1.0f / (float)K;
-    static constexpr float yl = (float)(1.0 / (double)K - (double)yh);
     static constexpr float negk = -(float)K;
 };
 
 constexpr float kDivTiny = 0x1p-90f;
 
 template <int K>
-__device__ __forceinline__ float div_k(float d) {
-    if (fabsf(d) < kDivTiny) return __fdiv_rn(d, (float)K);
-    float q0 = __fmaf_rn(d, Recip<K>::yh, __fmul_rn(d, Recip<K>::yl));
+__device__ __forceinline__ float div_k_fast(float d) {
+    float q0 = __fmul_rn(d, Recip<K>::yh);
     float r = __fmaf_rn(q0, Recip<K>::negk, d);
     return __fmaf_rn(r, Recip<K>::yh, q0);
+}
+
+template <int K>
+__device__ __forceinline__ float div_k(float d) {
+    if (fabsf(d) < kDivTiny) return __fdiv_rn(d, (float)K);
+    return div_k_fast<K>(d);
+}
+
+template <int K>
+__device__ __forceinline__ u64 div_k2_fast(u64 d) {
+    const u64 yh = f2(Recip<K>::yh, Recip<K>::yh);
+    const u64 nk = f2(Recip<K>::negk, Recip<K>::negk);
+    u64 q0 = mul2(d, yh);
+    u64 r = fma2(q0, nk, d);
+    return fma2(r, yh, q0);
 }
 
 template <int K>
 __device__ __forceinline__ u64 div_k2(u64 d) {
     const float dl = f2lo(d), dh = f2hi(d);
     if (fminf(fabsf(dl), fabsf(dh)) < kDivTiny) return f2(__fdiv_rn(dl, (float)K), __fdiv_rn(dh, (float)K));
-    const u64 yh = f2(Recip<K>::yh, Recip<K>::yh);
-    const u64 yl = f2(Recip<K>::yl, Recip<K>::yl);
-    const u64 nk = f2(Recip<K>::negk, Recip<K>::negk);
-    u64 q0 = fma2(d, yh, mul2(d, yl));
-    u64 r = fma2(q0, nk, d);
-    return fma2(r, yh, q0);
+    return div_k2_fast<K>(d);
 }
 
 // ---------------------------------------------------------------- compile-time loops
@@ -167,10 +177,13 @@ __device__ __forceinline__ void static_for(F&& f) {
 
 // One Welford step of count K on two lanes at once (x, mean, m2 as f32x2):
 //   d = x - mean; mean += d / K; m2 += d * (x - mean)
-template <int K>
+// GUARD = false is the fast division, valid for a lane whose nonzero
+// elements all have |x| >= 2^-60 (see lane_is_plain in rowops.cuh).
+template <int K, bool GUARD>
 __device__ __forceinline__ void welford_step2(u64 x, u64& mean, u64& m2) {
     u64 d = sub2(x, mean);
-    mean = add2(mean, div_k2<K>(d));
+    if constexpr (GUARD) mean = add2(mean, div_k2<K>(d));
+    else mean = add2(mean, div_k2_fast<K>(d));
     // The product feeding the sum uses the scalar __fmul_rn/__fadd_rn, which
     // are never merged into a fused multiply-add; ptxas does fuse a packed
     // mul.rn.f32x2 into a following add.rn.f32x2.
@@ -179,10 +192,11 @@ __device__ __forceinline__ void welford_step2(u64 x, u64& mean, u64& m2) {
             __fadd_rn(f2hi(m2), __fmul_rn(f2hi(d), f2hi(t))));
 }
 
-template <int K>
+template <int K, bool GUARD>
 __device__ __forceinline__ void welford_step(float x, float& mean, float& m2) {
     float d = __fsub_rn(x, mean);
-    mean = __fadd_rn(mean, div_k<K>(d));
+    if constexpr (GUARD) mean = __fadd_rn(mean, div_k<K>(d));
+    else mean = __fadd_rn(mean, div_k_fast<K>(d));
     m2 = __fadd_rn(m2, __fmul_rn(d, __fsub_rn(x, mean)));
 }
 

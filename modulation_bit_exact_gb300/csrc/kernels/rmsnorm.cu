@@ -236,12 +236,12 @@ static cudaError_t launch_rms(const P& p, bool vec, bool high, cudaStream_t s) {
     switch (chunks_per_lane(p.D)) {
         case 1: return launch_j<P, 32, 1>(p, vec, high, s);
         case 2: return launch_j<P, 32, 2>(p, vec, high, s);
-        case 3: return launch_j<P, 32, 3>(p, vec, high, s);
-        case 4: return launch_j<P, 32, 4>(p, vec, high, s);
+        case 3: return launch_j<P, 64, 3>(p, vec, high, s);
+        case 4: return launch_j<P, 64, 4>(p, vec, high, s);
         case 5: return launch_j<P, 64, 5>(p, vec, high, s);
-        case 6: return launch_j<P, 64, 6>(p, vec, high, s);
-        case 7: return launch_j<P, 64, 7>(p, vec, high, s);
-        case 8: return launch_j<P, 64, 8>(p, vec, high, s);
+        case 6: return launch_j<P, 128, 6>(p, vec, high, s);
+        case 7: return launch_j<P, 128, 7>(p, vec, high, s);
+        case 8: return launch_j<P, 128, 8>(p, vec, high, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -110,6 +110,33 @@ __device__ __forceinline__ void load_row(uint4 (&v)[C::M][C::J], const uint16_t*
         }
 }
 
+// True when every element this thread owns has |x| >= 2^-60 (bfloat16
+// exponent field >= 67; inf and NaN pass).  Then, in each of its lanes, every
+// Welford difference d = x - mean is +0 or |d| >= 2^-85: x is a multiple of
+// 2^-67; if |mean| >= 2^-62 both are multiples of 2^-85 and x - mean is 0 or
+// at least 2^-85 (exact below 2^-62), else |x - mean| > 2^-61.  That is the
+// range where the unguarded division by the count is exact.
+template <class C>
+__device__ __forceinline__ bool lanes_plain(const uint4 (&v)[C::M][C::J], int t, int nch) {
+    if constexpr (!C::VEC) {
+        return false;  // the scalar path zero-fills partial chunks: use the guard
+    } else {
+        uint32_t acc = 0xffffffffu;
+#pragma unroll
+        for (int j = 0; j < C::J; ++j)
+#pragma unroll
+            for (int m = 0; m < C::M; ++m) {
+                int c = t + C::TPR * m + kLanes * j;
+                if (c < nch) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc = min_u16x2(acc, w_of(v[m][j], i) & 0x7f807f80u);
+                }
+            }
+        uint32_t lo = acc & 0xffffu, hi = acc >> 16;
+        return (lo < hi ? lo : hi) >= 0x2180u;
+    }
+}
+
 // ------------------------------------------------------------------ tree
 
 __device__ __forceinline__ float sum_combine(float a, float b) { return __fadd_rn(a, b); }
@@ -141,8 +168,6 @@ __device__ __forceinline__ T tree_reduce(T (&L)[C::M], int t, TreeSmem& sm, int 
     // levels inside the thread: lane t+TPR*m with lane t+TPR*(m + s/TPR)
 #pragma unroll
     for (int s = 64; s >= C::TPR; s /= 2) {
-        constexpr int dummy = 0;
-        (void)dummy;
 #pragma unroll
         for (int m = 0; m < s / C::TPR; ++m) L[m] = comb(L[m], L[m + s / C::TPR]);
     }

@@ -4,7 +4,9 @@
 //   0: div_k<K>(d) (double-word reciprocal + Markstein correction) ==
 //      div.rn(d, K) for K = 1..64 and every finite binary32 d;
 //   1: mul.rn.bf16x2 == binary32 multiply then round, every operand pair;
-//   2: add.rn.bf16x2 == binary32 add then round, every operand pair.
+//   2: add.rn.bf16x2 == binary32 add then round, every operand pair;
+//   3: div_k_fast<K>(d) (no guard) == div.rn(d, K) for K = 1..64, every
+//      binary32 d with |d| >= 2^-100, and d = +0.
 // A mismatch where either result is a NaN is counted apart from the others:
 // NaN payloads never reach a bfloat16 output except as the canonical NaN.
 #include "launch.h"
@@ -15,6 +17,7 @@ namespace mbx {
 __device__ __forceinline__ bool is_nan32(uint32_t u) { return (u & 0x7fffffffu) > 0x7f800000u; }
 __device__ __forceinline__ bool is_nan16(uint32_t h) { return (h & 0x7fffu) > 0x7f80u; }
 
+template <bool FAST>
 __global__ void selftest_div_kernel(unsigned long long* counts) {
     unsigned long long bad = 0, bad_nan = 0;
     const uint64_t total = 1ull << 32;
@@ -22,9 +25,10 @@ __global__ void selftest_div_kernel(unsigned long long* counts) {
          i += (uint64_t)gridDim.x * blockDim.x) {
         const float d = __uint_as_float((uint32_t)i);
         if (!isfinite(d)) continue;  // finite numerators only (see numerics.cuh)
+        if (FAST && fabsf(d) < 0x1p-100f && (uint32_t)i != 0u) continue;  // fast form: |d| >= 2^-100 or +0
         static_for<1, 65>([&](auto kc) {
             constexpr int K = decltype(kc)::value;
-            uint32_t got = __float_as_uint(div_k<K>(d));
+            uint32_t got = __float_as_uint(FAST ? div_k_fast<K>(d) : div_k<K>(d));
             uint32_t want = __float_as_uint(__fdiv_rn(d, (float)K));
             if (got != want) {
                 if (is_nan32(got) || is_nan32(want)) ++bad_nan;
@@ -72,7 +76,8 @@ cudaError_t launch_selftest(int which, unsigned long long* counts, cudaStream_t 
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int grid = sms * 8, block = 256;
     switch (which) {
-        case 0: selftest_div_kernel<<<grid, block, 0, s>>>(counts); break;
+        case 0: selftest_div_kernel<false><<<grid, block, 0, s>>>(counts); break;
+        case 3: selftest_div_kernel<true><<<grid, block, 0, s>>>(counts); break;
         case 1: selftest_bf16x2_kernel<true><<<grid, block, 0, s>>>(counts); break;
         case 2: selftest_bf16x2_kernel<false><<<grid, block, 0, s>>>(counts); break;
         default: return cudaErrorInvalidValue;

@@ -511,7 +511,7 @@ MBX_API int mbx_qk_norm_rope_qkv_epilogue(const mbx_view* joint, const mbx_cview
 
 MBX_API int mbx_selftest(int which, unsigned long long* counts, void* stream) {
     if (!counts) return MBX_E_NULL;
-    if (which < 0 || which > 2) return MBX_E_ARG;
+    if (which < 0 || which > 3) return MBX_E_ARG;
     if (reinterpret_cast<uintptr_t>(counts) % 8) return MBX_E_ALIGN;
     MBX_TRY(raw_on_device(counts, 16));
     return cuda_status(mbx::launch_selftest(which, counts, (cudaStream_t)stream));

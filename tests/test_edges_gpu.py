@@ -27,7 +27,8 @@ def bf(bits: np.ndarray) -> torch.Tensor:
 
 
 @pytest.mark.parametrize("which,what", [(0, "division by counts 1..64"),
-                                        (1, "bf16x2 multiply"), (2, "bf16x2 add")])
+                                        (1, "bf16x2 multiply"), (2, "bf16x2 add"),
+                                        (3, "unguarded division, |d| >= 2^-100")])
 def test_exhaustive_building_blocks(mbx, which, what):
     bad, bad_nan = mbx.selftest(which)
     assert bad == 0, f"{what}: {bad} non-NaN mismatches"
