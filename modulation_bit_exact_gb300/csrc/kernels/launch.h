@@ -86,6 +86,18 @@ inline int chunks_per_lane(int D) { return ((D + 7) / 8 + 127) / 128; }
 // blocks of `kernel` at `block` threads); -1 if the runtime cannot tell.
 int grid_for_rows(const void* kernel, int64_t units, int units_per_block, int block);
 
+// Launch shape of a pipelined row kernel: one CTA per SM, each owning a
+// contiguous block of rows_per_cta rows, with as many row groups of `tpr`
+// threads as shared memory allows (smem_fixed bytes per CTA plus
+// smem_per_group per group), at most 512 threads (and at most 15 groups when
+// a group spans several warps: one named barrier each).
+struct PipeShape {
+    int grid, groups, smem;
+    int64_t rows_per_cta;
+};
+int64_t pipe_rows_per_cta(int64_t rows);
+bool pipe_shape(const void* kernel, int tpr, int smem_per_group, int smem_fixed, int64_t rows, PipeShape* out);
+
 cudaError_t launch_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_rmsnorm_scale(const RmsScaleParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_rmsnorm_tanh_residual(const RmsTanhParams& p, bool vec, bool high, cudaStream_t s);

@@ -193,6 +193,311 @@ __global__ void __launch_bounds__(kBlock) ln_modulate_kernel(LnModParams p) {
     }
 }
 
+// ------------------------------------------------------------------ pipelined path
+//
+// For 16-byte-aligned rows (D % 8 == 0): one CTA per SM holds several row
+// groups; each group streams its next rows into a ring of shared-memory
+// stages with cp.async (each thread copies exactly the chunks it will read),
+// so loads stay in flight while the group computes.  Same lanes, same order,
+// same tree as above: the results are the same bits.
+
+// Every element of the chunk has |x| >= 2^-60 (bf16 exponent field >= 67).
+__device__ __forceinline__ bool chunk_plain(const uint4& v) {
+    uint32_t a = min_u16x2(min_u16x2(v.x & 0x7f807f80u, v.y & 0x7f807f80u),
+                           min_u16x2(v.z & 0x7f807f80u, v.w & 0x7f807f80u));
+    uint32_t lo = a & 0xffffu, hi = a >> 16;
+    return (lo < hi ? lo : hi) >= 0x2180u;
+}
+
+struct WPair {
+    u64 mean, m2;
+};
+
+// Welford over one chunk of lane A (low halves) and one of lane B (high
+// halves), counts k0+1..k0+8, with plain correctly rounded division: the rare
+// path for chunks holding zeros or values below 2^-60.  na / nb: elements of
+// each chunk that exist (0 or 8).
+__device__ __noinline__ WPair welford_chunk_exact(uint4 a, uint4 b, int k0, int na, int nb, WPair st) {
+    float ma = f2lo(st.mean), qa = f2lo(st.m2), mb = f2hi(st.mean), qb = f2hi(st.m2);
+    for (int e = 0; e < kChunk; ++e) {
+        const float k = (float)(k0 + e + 1);
+        const uint32_t wa = w_of(a, e >> 1), wb = w_of(b, e >> 1);
+        const float xa = (e & 1) ? hi_f(wa) : lo_f(wa), xb = (e & 1) ? hi_f(wb) : lo_f(wb);
+        if (e < na) {
+            float d = __fsub_rn(xa, ma);
+            ma = __fadd_rn(ma, __fdiv_rn(d, k));
+            qa = __fadd_rn(qa, __fmul_rn(d, __fsub_rn(xa, ma)));
+        }
+        if (e < nb) {
+            float d = __fsub_rn(xb, mb);
+            mb = __fadd_rn(mb, __fdiv_rn(d, k));
+            qb = __fadd_rn(qb, __fmul_rn(d, __fsub_rn(xb, mb)));
+        }
+    }
+    return WPair{f2(ma, mb), f2(qa, qb)};
+}
+
+// Welford of every lane this thread owns, reading its chunks from ring stage
+// s.  For each chunk index j one branch decides, for all the thread's lanes at
+// once, between the fast division (every element plain) and the exact one,
+// so the lane pairs' dependency chains interleave.  `full` (every lane has
+// all J chunks) removes the per-step selects of the last chunk.
+template <class C, class RingT>
+__device__ __forceinline__ void welford_stage(const RingT& ring, int s, int t, int nch, bool full,
+                                              Wf (&L)[C::M]) {
+    if constexpr (C::M >= 2) {
+        constexpr int P = C::M / 2;
+        u64 mean[P], m2[P];
+#pragma unroll
+        for (int p = 0; p < P; ++p) mean[p] = m2[p] = f2(0.0f, 0.0f);
+        static_for<0, C::J>([&](auto jc) {
+            constexpr int j = decltype(jc)::value;
+            uint4 A[P], B[P];
+            bool va[P], vb[P];
+            bool plain = true;
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                const int ca = t + C::TPR * p + kLanes * j, cb = ca + C::TPR * P;
+                va[p] = ca < nch;
+                vb[p] = cb < nch;
+                A[p] = va[p] ? lds16(ring.at(s, 0, ca)) : make_uint4(0, 0, 0, 0);
+                B[p] = vb[p] ? lds16(ring.at(s, 0, cb)) : make_uint4(0, 0, 0, 0);
+                plain = plain && (!va[p] || chunk_plain(A[p])) && (!vb[p] || chunk_plain(B[p]));
+            }
+            if (plain && (j < C::J - 1 || full)) {
+                static_for<0, kChunk>([&](auto ec) {
+                    constexpr int e = decltype(ec)::value;
+                    constexpr int K = kChunk * j + e + 1;
+#pragma unroll
+                    for (int p = 0; p < P; ++p)
+                        welford_step2<K, false>(pair_elem(w_of(A[p], e / 2), w_of(B[p], e / 2), e & 1), mean[p], m2[p]);
+                });
+            } else if (plain) {  // last chunk, some lanes without it
+                static_for<0, kChunk>([&](auto ec) {
+                    constexpr int e = decltype(ec)::value;
+                    constexpr int K = kChunk * j + e + 1;
+#pragma unroll
+                    for (int p = 0; p < P; ++p) {
+                        u64 mn = mean[p], q = m2[p];
+                        welford_step2<K, false>(pair_elem(w_of(A[p], e / 2), w_of(B[p], e / 2), e & 1), mn, q);
+                        mean[p] = sel2(va[p], vb[p], mn, mean[p]);
+                        m2[p] = sel2(va[p], vb[p], q, m2[p]);
+                    }
+                });
+            } else {
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    WPair r = welford_chunk_exact(A[p], B[p], kChunk * j, va[p] ? kChunk : 0, vb[p] ? kChunk : 0,
+                                                  WPair{mean[p], m2[p]});
+                    mean[p] = r.mean;
+                    m2[p] = r.m2;
+                }
+            }
+        });
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            L[p].mean = f2lo(mean[p]);
+            L[p].m2 = f2lo(m2[p]);
+            L[p + P].mean = f2hi(mean[p]);
+            L[p + P].m2 = f2hi(m2[p]);
+        }
+    } else {
+        u64 st = f2(0.0f, 0.0f), sq = f2(0.0f, 0.0f);  // lane in the low halves
+        static_for<0, C::J>([&](auto jc) {
+            constexpr int j = decltype(jc)::value;
+            const int c = t + kLanes * j;
+            if (c >= nch) return;
+            const uint4 A = lds16(ring.at(s, 0, c));
+            if (chunk_plain(A)) {
+                float mean = f2lo(st), m2 = f2lo(sq);
+                static_for<0, kChunk>([&](auto ec) {
+                    constexpr int e = decltype(ec)::value;
+                    constexpr int K = kChunk * j + e + 1;
+                    const uint32_t w = w_of(A, e / 2);
+                    welford_step<K, false>((e & 1) ? hi_f(w) : lo_f(w), mean, m2);
+                });
+                st = f2(mean, 0.0f);
+                sq = f2(m2, 0.0f);
+            } else {
+                WPair r = welford_chunk_exact(A, make_uint4(0, 0, 0, 0), kChunk * j, kChunk, 0, WPair{st, sq});
+                st = r.mean;
+                sq = r.m2;
+            }
+        });
+        L[0].mean = f2lo(st);
+        L[0].m2 = f2lo(sq);
+    }
+#pragma unroll
+    for (int m = 0; m < C::M; ++m) {
+        const int c_last = t + C::TPR * m + kLanes * (C::J - 1);
+        L[m].n = (float)(kChunk * (C::J - 1) + (c_last < nch ? kChunk : 0));
+    }
+}
+
+// Modulation modes of the pipelined kernel:
+//   kModRing:   the modulation rows travel in the ring with x (per-token
+//               modulation, or samples that change within a CTA's rows);
+//   kModStaged: a CTA's rows span at most two samples; their bf16(1+scale)
+//               (lossless) or scale (high) and shift are staged in shared
+//               memory once.
+enum { kModRing = 0, kModStaged = 1 };
+
+template <int TPR, int J, int NS, bool HIGH, int MODE>
+__global__ void __launch_bounds__(512) ln_modulate_pipe_kernel(LnModParams p, int64_t rows_per_cta) {
+    using C = RowCfg<TPR, J, true>;
+    constexpr int NOPS = MODE == kModRing ? 3 : 1;
+    using R = Ring<C, NS, NOPS>;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int groups = blockDim.x / TPR;
+    const int g = threadIdx.x / TPR, t = threadIdx.x % TPR;
+    const int D = p.D;
+    const int nch = D / kChunk;
+    TreeSmem& sm = reinterpret_cast<TreeSmem*>(smem_raw)[g];
+    uint4* mod = reinterpret_cast<uint4*>(smem_raw + groups * sizeof(TreeSmem));  // [2 slots][t|shift][nch]
+    const int mod_chunks = MODE == kModStaged ? 2 * 2 * nch : 0;
+    const R ring{mod + mod_chunks + (size_t)g * (R::kBytes / 16)};
+    const int bar_id = 1 + g;
+    const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
+    const int64_t r1 = r0 + rows_per_cta < p.rows ? r0 + rows_per_cta : p.rows;
+    const int64_t m0 = r0 / p.seq;
+
+    auto issue = [&](int s, int64_t row) {
+        ring.issue(s, 0, p.x + row * p.x_stride, t, nch);
+        if constexpr (MODE == kModRing) {
+            const int64_t mrow = row / p.seq;
+            ring.issue(s, 1, p.scale + mrow * p.scale_stride, t, nch);
+            ring.issue(s, 2, p.shift + mrow * p.shift_stride, t, nch);
+        }
+    };
+    const int64_t first = r0 + g;
+#pragma unroll
+    for (int s = 0; s < NS - 1; ++s) {
+        const int64_t r = first + s * groups;
+        if (r < r1) issue(s, r);
+        cp_async_commit();
+    }
+    // the first rows are on their way; stage the modulation meanwhile
+    if constexpr (MODE == kModStaged) {
+        const int64_t m_last = (r1 - 1) / p.seq;
+        const int slots = (int)(m_last - m0 + 1);  // 1 or 2 (host guarantees)
+        for (int i = threadIdx.x; i < slots * nch; i += blockDim.x) {
+            const int slot = i / nch, c = i - slot * nch;
+            const uint4 sc = ld_shared_row(p.scale + (m0 + slot) * p.scale_stride + (int64_t)c * kChunk);
+            const uint4 sh = ld_shared_row(p.shift + (m0 + slot) * p.shift_stride + (int64_t)c * kChunk);
+            uint4 tv;
+            if constexpr (!HIGH) {
+                tv.x = badd(0x3f803f80u, sc.x);  // bf16(1 + scale), as the eager chain rounds it
+                tv.y = badd(0x3f803f80u, sc.y);
+                tv.z = badd(0x3f803f80u, sc.z);
+                tv.w = badd(0x3f803f80u, sc.w);
+            } else {
+                tv = sc;
+            }
+            mod[(slot * 2 + 0) * nch + c] = tv;
+            mod[(slot * 2 + 1) * nch + c] = sh;
+        }
+        __syncthreads();
+    }
+
+    int cur = 0;
+    for (int64_t row = first; row < r1; row += groups) {
+        const int64_t rn = row + (NS - 1) * groups;
+        const int sn = cur == 0 ? NS - 1 : cur - 1;
+        if (rn < r1) issue(sn, rn);
+        cp_async_commit();
+        cp_async_wait<NS - 1>();
+
+        float mean = 0.0f, rstd = 0.0f;
+        if constexpr (!HIGH) {
+            Wf L[C::M];
+            const bool full = nch == kLanes * C::J;
+            welford_stage<C>(ring, cur, t, nch, full, L);
+            const Wf s = full ? tree_reduce<C>(L, t, sm, bar_id, wf_combine_eq)
+                              : tree_reduce<C>(L, t, sm, bar_id, wf_combine);
+            mean = s.mean;
+            if (t == 0) {
+                const float var = __fdiv_rn(s.m2, (float)D);
+                rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, p.eps)));
+            }
+        } else {
+            float acc[C::M];
+#pragma unroll
+            for (int m = 0; m < C::M; ++m) {
+                acc[m] = 0.0f;
+#pragma unroll
+                for (int j = 0; j < C::J; ++j) {
+                    const int c = t + C::TPR * m + kLanes * j;
+                    if (c >= nch) continue;
+                    const uint4 v = lds16(ring.at(cur, 0, c));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[m] += lo_f(w_of(v, i)) + hi_f(w_of(v, i));
+                }
+            }
+            float dummy = 0.0f;
+            mean = tree_reduce<C>(acc, t, sm, bar_id, sum_combine) / (float)D;
+            group_bcast<C>(mean, dummy, t, sm, bar_id);
+#pragma unroll
+            for (int m = 0; m < C::M; ++m) {
+                acc[m] = 0.0f;
+#pragma unroll
+                for (int j = 0; j < C::J; ++j) {
+                    const int c = t + C::TPR * m + kLanes * j;
+                    if (c >= nch) continue;
+                    const uint4 v = lds16(ring.at(cur, 0, c));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float d0 = lo_f(w_of(v, i)) - mean, d1 = hi_f(w_of(v, i)) - mean;
+                        acc[m] += d0 * d0 + d1 * d1;
+                    }
+                }
+            }
+            const float q = tree_reduce<C>(acc, t, sm, bar_id, sum_combine);
+            if (t == 0) rstd = rsqrtf(q / (float)D + p.eps);
+        }
+        group_bcast<C>(mean, rstd, t, sm, bar_id);
+
+        const uint4* tm = MODE == kModStaged ? mod + ((row / p.seq - m0) * 2 + 0) * nch : nullptr;
+        const uint4* sh = MODE == kModStaged ? tm + nch : nullptr;
+        uint16_t* out_row = p.out + row * p.out_stride;
+        const u64 mean2 = f2(mean, mean), rstd2 = f2(rstd, rstd);
+#pragma unroll
+        for (int j = 0; j < C::J; ++j)
+#pragma unroll
+            for (int m = 0; m < C::M; ++m) {
+                const int c = t + C::TPR * m + kLanes * j;
+                if (c >= nch) continue;
+                const uint4 X = lds16(ring.at(cur, 0, c));
+                uint4 T, SH;
+                if constexpr (MODE == kModStaged) {
+                    T = lds16(tm + c);
+                    SH = lds16(sh + c);
+                } else {
+                    T = lds16(ring.at(cur, 1, c));
+                    SH = lds16(ring.at(cur, 2, c));
+                }
+                uint4 o;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t xw = w_of(X, i), tw = w_of(T, i), hw = w_of(SH, i);
+                    uint32_t ow;
+                    if constexpr (!HIGH) {
+                        const uint32_t nrm = pack2_rn(mul2(sub2(widen2(xw), mean2), rstd2));
+                        // ring mode carries scale itself: round 1 + scale here
+                        const uint32_t tt = MODE == kModStaged ? tw : badd(0x3f803f80u, tw);
+                        ow = badd(bmul(nrm, tt), hw);
+                    } else {
+                        ow = pack_rn(fmaf((lo_f(xw) - mean) * rstd, 1.0f + lo_f(tw), lo_f(hw)),
+                                     fmaf((hi_f(xw) - mean) * rstd, 1.0f + hi_f(tw), hi_f(hw)));
+                    }
+                    w_set(o, i, ow);
+                }
+                st_v4(out_row + (int64_t)c * kChunk, o);
+            }
+        cur = cur + 1 == NS ? 0 : cur + 1;
+    }
+    cp_async_wait<0>();
+}
+
 // ------------------------------------------------------------------ host
 
 template <int TPR, int J, bool VEC, bool HIGH>
@@ -205,13 +510,49 @@ static cudaError_t launch_one(const LnModParams& p, cudaStream_t s) {
 }
 
 template <int TPR, int J>
-static cudaError_t launch_j(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
-    if (vec) return high ? launch_one<TPR, J, true, true>(p, s) : launch_one<TPR, J, true, false>(p, s);
+static cudaError_t launch_j(const LnModParams& p, bool, bool high, cudaStream_t s) {
     return high ? launch_one<TPR, J, false, true>(p, s) : launch_one<TPR, J, false, false>(p, s);
+}
+
+template <int TPR, int J, int NS, bool HIGH, int MODE>
+static cudaError_t launch_pipe(const LnModParams& p, cudaStream_t s) {
+    auto k = ln_modulate_pipe_kernel<TPR, J, NS, HIGH, MODE>;
+    using C = RowCfg<TPR, J, true>;
+    using R = Ring<C, NS, MODE == kModRing ? 3 : 1>;
+    const int fixed = MODE == kModStaged ? 2 * 2 * (p.D / kChunk) * 16 : 0;
+    PipeShape sh;
+    if (!pipe_shape(reinterpret_cast<const void*>(k), TPR, (int)sizeof(TreeSmem) + R::kBytes, fixed, p.rows, &sh))
+        return cudaErrorInvalidConfiguration;
+    k<<<sh.grid, sh.groups * TPR, sh.smem, s>>>(p, sh.rows_per_cta);
+    return cudaGetLastError();
+}
+
+template <int TPR, int J, int NS>
+static cudaError_t launch_pipe_v(const LnModParams& p, bool high, cudaStream_t s) {
+    // stage the modulation when each CTA's block of rows spans at most two
+    // samples (rows per CTA <= seq); otherwise carry it in the ring
+    const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
+    if (high) return staged ? launch_pipe<TPR, J, NS, true, kModStaged>(p, s) : launch_pipe<TPR, J, NS, true, kModRing>(p, s);
+    return staged ? launch_pipe<TPR, J, NS, false, kModStaged>(p, s) : launch_pipe<TPR, J, NS, false, kModRing>(p, s);
 }
 
 cudaError_t launch_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
     const int J = chunks_per_lane(p.D);
+    if (vec) {
+        // pipelined path: one warp per row up to 2048 elements, two up to
+        // 4096 (measured fastest at 3072: fewer, longer row rounds), four above
+        switch (J) {
+            case 1: return launch_pipe_v<32, 1, 2>(p, high, s);
+            case 2: return launch_pipe_v<32, 2, 2>(p, high, s);
+            case 3: return launch_pipe_v<64, 3, 2>(p, high, s);
+            case 4: return launch_pipe_v<64, 4, 2>(p, high, s);
+            case 5: return launch_pipe_v<128, 5, 2>(p, high, s);
+            case 6: return launch_pipe_v<128, 6, 2>(p, high, s);
+            case 7: return launch_pipe_v<128, 7, 2>(p, high, s);
+            case 8: return launch_pipe_v<128, 8, 2>(p, high, s);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (J) {
         // threads per row: enough that a thread holds at most ~5 chunks of x
         case 1: return launch_j<32, 1>(p, vec, high, s);

@@ -212,9 +212,22 @@ __device__ __forceinline__ Wf wf_combine(Wf a, Wf b) {
     Wf c;
     c.n = __fadd_rn(a.n, b.n);
     float d = __fsub_rn(b.mean, a.mean);
-    float r = __fdiv_rn(b.n, c.n);
+    // nb/(na+nb) is exactly 0.5 when the counts are equal (the common case)
+    float r = a.n == b.n ? 0.5f : __fdiv_rn(b.n, c.n);
     c.mean = __fadd_rn(a.mean, __fmul_rn(d, r));
     c.m2 = __fadd_rn(__fadd_rn(a.m2, b.m2), __fmul_rn(__fmul_rn(d, d), __fmul_rn(a.n, r)));
+    return c;
+}
+
+// The same combine when both sides hold the same nonzero count (every lane
+// full): r = nb/(na+nb) = 0.5 exactly, no empty side.  Same operations, same
+// bits, no branches.
+__device__ __forceinline__ Wf wf_combine_eq(Wf a, Wf b) {
+    Wf c;
+    c.n = __fadd_rn(a.n, b.n);
+    float d = __fsub_rn(b.mean, a.mean);
+    c.mean = __fadd_rn(a.mean, __fmul_rn(d, 0.5f));
+    c.m2 = __fadd_rn(__fadd_rn(a.m2, b.m2), __fmul_rn(__fmul_rn(d, d), __fmul_rn(a.n, 0.5f)));
     return c;
 }
 

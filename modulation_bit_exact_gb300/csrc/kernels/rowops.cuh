@@ -137,6 +137,49 @@ __device__ __forceinline__ bool lanes_plain(const uint4 (&v)[C::M][C::J], int t,
     }
 }
 
+// ------------------------------------------------------------------ cp.async ring
+
+// 16-byte asynchronous global -> shared copy, L1 bypassed (streamed data).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ uint4 lds16(const uint4* p) {
+    uint4 v;
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
+// A row group's ring of NS stages; a stage holds NOPS rows (x and the
+// per-token operands), each laid out by chunk index (16 bytes per chunk, 128*J
+// chunks).  Thread t of the group copies exactly the chunks it later reads
+// (t + TPR*m + 128*j), so its own cp.async.wait_group is the only
+// synchronisation the ring needs.
+template <class C, int NS, int NOPS>
+struct Ring {
+    static constexpr int kRowChunks = kLanes * C::J;
+    static constexpr int kBytes = NS * NOPS * kRowChunks * 16;
+    uint4* base;
+    __device__ __forceinline__ uint4* at(int s, int o, int c) const {
+        return base + ((s * NOPS + o) * kRowChunks + c);
+    }
+    // copy this thread's chunks of `src` into stage s, operand o
+    __device__ __forceinline__ void issue(int s, int o, const uint16_t* src, int t, int nch) const {
+#pragma unroll
+        for (int j = 0; j < C::J; ++j)
+#pragma unroll
+            for (int m = 0; m < C::M; ++m) {
+                int c = t + C::TPR * m + kLanes * j;
+                if (c < nch) cp_async16(at(s, o, c), src + (int64_t)c * kChunk);
+            }
+    }
+};
+
 // ------------------------------------------------------------------ tree
 
 __device__ __forceinline__ float sum_combine(float a, float b) { return __fadd_rn(a, b); }

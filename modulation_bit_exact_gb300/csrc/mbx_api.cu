@@ -17,7 +17,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/mbx.h"
+#include "mbx.h"
 #include "kernels/launch.h"
 
 namespace {
@@ -350,6 +350,60 @@ int grid_for_rows(const void* kernel, int64_t units, int units_per_block, int bl
     int64_t need = (units + units_per_block - 1) / units_per_block;
     int64_t cap = (int64_t)nsm * per_sm;
     return (int)(need < cap ? need : cap);
+}
+
+static int device_sms() {
+    static int sms[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (sms[dev] == 0) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    return sms[dev];
+}
+
+int64_t pipe_rows_per_cta(int64_t rows) {
+    const int sms = device_sms();
+    if (sms < 1) return rows;
+    return (rows + sms - 1) / sms;
+}
+
+bool pipe_shape(const void* kernel, int tpr, int smem_per_group, int smem_fixed, int64_t rows,
+                PipeShape* out) {
+    struct Entry {
+        const void* k;
+        int dev, smem;
+    };
+    static Entry done[256];
+    static int n_done = 0;
+    static std::mutex mu;
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const int sms = device_sms();
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    const int64_t per_cta = pipe_rows_per_cta(rows);
+    const int budget = optin - 8 * 1024 - smem_fixed;  // leave some shared memory to L1
+    int groups = budget / smem_per_group;
+    const int cap = tpr > 32 ? 15 : 512 / tpr;
+    if (groups > cap) groups = cap;
+    if (groups * tpr > 512) groups = 512 / tpr;  // pipelined kernels launch <= 512 threads
+    if ((int64_t)groups > per_cta) groups = (int)per_cta;
+    if (groups < 1 || sms < 1) return false;
+    const int smem = smem_fixed + groups * smem_per_group;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        bool seen = false;
+        for (int i = 0; i < n_done; ++i)
+            if (done[i].k == kernel && done[i].dev == dev && done[i].smem >= smem) seen = true;
+        if (!seen) {
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+                return false;
+            if (n_done < 256) done[n_done++] = Entry{kernel, dev, smem};
+        }
+    }
+    out->grid = (int)((rows + per_cta - 1) / per_cta);
+    out->groups = groups;
+    out->smem = smem;
+    out->rows_per_cta = per_cta;
+    return true;
 }
 
 }  // namespace mbx
