@@ -211,6 +211,261 @@ __global__ void __launch_bounds__(kBlock) rmsnorm_tanh_residual_kernel(RmsTanhPa
     }
 }
 
+// ------------------------------------------------------------------ pipelined path
+//
+// 16-byte-aligned rows: the same lanes, order and roundings as above, with x
+// (and every per-row operand) streamed through a per-row-group ring of
+// shared-memory stages by cp.async, and the weight row (plus per-sample
+// modulation rows, when a CTA's block of rows spans at most two samples)
+// staged once per CTA.  OP 0: rmsnorm_scale (mod = scale);
+// OP 1: rmsnorm_tanh_residual (mod = gate, plus the residual in the ring).
+enum { kRmsScale = 0, kRmsTanh = 1 };
+enum { kRmsModRing = 0, kRmsModStaged = 1 };
+
+template <int OP>
+struct RmsPipeArgs;
+template <>
+struct RmsPipeArgs<kRmsScale> {
+    using P = RmsScaleParams;
+    static __device__ const uint16_t* mod(const P& p) { return p.scale; }
+    static __device__ int64_t mod_stride(const P& p) { return p.scale_stride; }
+};
+template <>
+struct RmsPipeArgs<kRmsTanh> {
+    using P = RmsTanhParams;
+    static __device__ const uint16_t* mod(const P& p) { return p.gate; }
+    static __device__ int64_t mod_stride(const P& p) { return p.gate_stride; }
+};
+
+// Sum of bf16(x*x) per lane, chunks read from ring stage s (absent chunks
+// add nothing).
+template <class C, class RingT>
+__device__ __forceinline__ void sumsq_stage(const RingT& ring, int s, int t, int nch, float (&L)[C::M]) {
+    if constexpr (C::M >= 2) {
+        constexpr int P = C::M / 2;
+        u64 acc[P];
+#pragma unroll
+        for (int p = 0; p < P; ++p) acc[p] = f2(0.0f, 0.0f);
+#pragma unroll
+        for (int j = 0; j < C::J; ++j)
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                const int ca = t + C::TPR * p + kLanes * j, cb = ca + C::TPR * P;
+                const uint4 A = ca < nch ? lds16(ring.at(s, 0, ca)) : make_uint4(0, 0, 0, 0);
+                const uint4 B = cb < nch ? lds16(ring.at(s, 0, cb)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t a = w_of(A, i), b = w_of(B, i), sa = bmul(a, a), sb = bmul(b, b);
+                    acc[p] = add2(acc[p], pair_elem(sa, sb, 0));
+                    acc[p] = add2(acc[p], pair_elem(sa, sb, 1));
+                }
+            }
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            L[p] = f2lo(acc[p]);
+            L[p + P] = f2hi(acc[p]);
+        }
+    } else {
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < C::J; ++j) {
+            const int c = t + kLanes * j;
+            if (c >= nch) continue;
+            const uint4 A = lds16(ring.at(s, 0, c));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t a = w_of(A, i), sa = bmul(a, a);
+                acc = __fadd_rn(acc, lo_f(sa));
+                acc = __fadd_rn(acc, hi_f(sa));
+            }
+        }
+        L[0] = acc;
+    }
+}
+
+template <class C, class RingT>
+__device__ __forceinline__ void sumsq_stage_f32(const RingT& ring, int s, int t, int nch, float (&L)[C::M]) {
+#pragma unroll
+    for (int m = 0; m < C::M; ++m) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < C::J; ++j) {
+            const int c = t + C::TPR * m + kLanes * j;
+            if (c >= nch) continue;
+            const uint4 A = lds16(ring.at(s, 0, c));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t w = w_of(A, i);
+                acc = fmaf(lo_f(w), lo_f(w), acc);
+                acc = fmaf(hi_f(w), hi_f(w), acc);
+            }
+        }
+        L[m] = acc;
+    }
+}
+
+template <int TPR, int J, int NS, bool HIGH, int OP, int MODE>
+__global__ void __launch_bounds__(512) rmsnorm_pipe_kernel(typename RmsPipeArgs<OP>::P p, int64_t rows_per_cta) {
+    using A = RmsPipeArgs<OP>;
+    using C = RowCfg<TPR, J, true>;
+    // ring operands: x, [mod when not staged], [residual for the tanh op]
+    constexpr int OP_MOD = MODE == kRmsModRing ? 1 : -1;
+    constexpr int OP_RES = OP == kRmsTanh ? (MODE == kRmsModRing ? 2 : 1) : -1;
+    constexpr int NOPS = 1 + (MODE == kRmsModRing ? 1 : 0) + (OP == kRmsTanh ? 1 : 0);
+    using R = Ring<C, NS, NOPS>;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int groups = blockDim.x / TPR;
+    const int g = threadIdx.x / TPR, t = threadIdx.x % TPR;
+    const int D = p.D;
+    const int nch = D / kChunk;
+    TreeSmem& sm = reinterpret_cast<TreeSmem*>(smem_raw)[g];
+    uint4* wsm = reinterpret_cast<uint4*>(smem_raw + groups * sizeof(TreeSmem));  // weight [nch]
+    uint4* msm = wsm + nch;                                                       // mod [2][nch]
+    unsigned short* tab = reinterpret_cast<unsigned short*>(msm + (MODE == kRmsModStaged ? 2 * nch : 0));
+    constexpr int kTab = OP == kRmsTanh ? (MBX_TANH_HI - MBX_TANH_LO) : 0;
+    const R ring{reinterpret_cast<uint4*>(tab + ((kTab + 7) / 8) * 8) + (size_t)g * (R::kBytes / 16)};
+    const int bar_id = 1 + g;
+    const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
+    const int64_t r1 = r0 + rows_per_cta < p.rows ? r0 + rows_per_cta : p.rows;
+    const int64_t m0 = r0 / p.seq;
+    const uint16_t* modp = A::mod(p);
+    const int64_t mod_stride = A::mod_stride(p);
+
+    auto issue = [&](int s, int64_t row) {
+        ring.issue(s, 0, p.x + row * p.x_stride, t, nch);
+        if constexpr (OP_MOD >= 0) ring.issue(s, OP_MOD, modp + (row / p.seq) * mod_stride, t, nch);
+        if constexpr (OP_RES >= 0) ring.issue(s, OP_RES, p.residual + row * p.res_stride, t, nch);
+    };
+    const int64_t first = r0 + g;
+#pragma unroll
+    for (int s = 0; s < NS - 1; ++s) {
+        const int64_t r = first + s * groups;
+        if (r < r1) issue(s, r);
+        cp_async_commit();
+    }
+    // the first rows are on their way; stage the per-CTA data meanwhile
+    for (int c = threadIdx.x; c < nch; c += blockDim.x) wsm[c] = ld_shared_row(p.weight + (int64_t)c * kChunk);
+    if constexpr (MODE == kRmsModStaged) {
+        const int slots = (int)((r1 - 1) / p.seq - m0 + 1);
+        for (int i = threadIdx.x; i < slots * nch; i += blockDim.x) {
+            const int slot = i / nch, c = i - slot * nch;
+            msm[slot * nch + c] = ld_shared_row(modp + (m0 + slot) * mod_stride + (int64_t)c * kChunk);
+        }
+    }
+    if constexpr (OP == kRmsTanh && !HIGH)
+        for (int i = threadIdx.x; i < kTab; i += blockDim.x) tab[i] = kTanhBf16[i];
+    __syncthreads();
+
+    int cur = 0;
+    for (int64_t row = first; row < r1; row += groups) {
+        const int64_t rn = row + (NS - 1) * groups;
+        const int sn = cur == 0 ? NS - 1 : cur - 1;
+        if (rn < r1) issue(sn, rn);
+        cp_async_commit();
+        cp_async_wait<NS - 1>();
+
+        float L[C::M];
+        if constexpr (!HIGH) sumsq_stage<C>(ring, cur, t, nch, L);
+        else sumsq_stage_f32<C>(ring, cur, t, nch, L);
+        const float S = tree_reduce<C>(L, t, sm, bar_id, sum_combine);
+        float rstd = 0.0f, unused = 0.0f;
+        if (t == 0) {
+            if constexpr (!HIGH) {
+                const float ms = lo_f(pack_rn(__fdiv_rn(S, (float)D), 0.0f));
+                const float inner = lo_f(pack_rn(__fadd_rn(ms, p.eps), 0.0f));
+                rstd = lo_f(pack_rn(__fdiv_rn(1.0f, __fsqrt_rn(inner)), 0.0f));
+            } else {
+                rstd = rsqrtf(S / (float)D + p.eps);
+            }
+        }
+        group_bcast<C>(rstd, unused, t, sm, bar_id);
+        const uint32_t r2 = bf16_bits(rstd);
+        const uint4* mrow = MODE == kRmsModStaged ? msm + (row / p.seq - m0) * nch : nullptr;
+        uint16_t* out_row = p.out + row * p.out_stride;
+#pragma unroll
+        for (int j = 0; j < C::J; ++j)
+#pragma unroll
+            for (int m = 0; m < C::M; ++m) {
+                const int c = t + C::TPR * m + kLanes * j;
+                if (c >= nch) continue;
+                const uint4 X = lds16(ring.at(cur, 0, c));
+                const uint4 W = lds16(wsm + c);
+                uint4 MD;
+                if constexpr (MODE == kRmsModStaged) MD = lds16(mrow + c);
+                else MD = lds16(ring.at(cur, OP_MOD > 0 ? OP_MOD : 0, c));
+                uint4 RS = make_uint4(0, 0, 0, 0);
+                if constexpr (OP_RES >= 0) RS = lds16(ring.at(cur, OP_RES, c));
+                uint4 o;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t xw = w_of(X, i), ww = w_of(W, i), mw = w_of(MD, i);
+                    uint32_t ow;
+                    if constexpr (OP == kRmsScale) {
+                        if constexpr (!HIGH) {
+                            ow = bmul(bmul(bmul(xw, r2), ww), mw);
+                        } else {
+                            ow = pack_rn(lo_f(xw) * rstd * lo_f(ww) * lo_f(mw), hi_f(xw) * rstd * hi_f(ww) * hi_f(mw));
+                        }
+                    } else {
+                        const uint32_t rw = w_of(RS, i);
+                        if constexpr (!HIGH) {
+                            const uint32_t n = bmul(bmul(xw, r2), ww);
+                            ow = badd(rw, bmul(tanh2(mw, tab), n));
+                        } else {
+                            ow = pack_rn(fmaf(tanhf(lo_f(mw)), lo_f(xw) * rstd * lo_f(ww), lo_f(rw)),
+                                         fmaf(tanhf(hi_f(mw)), hi_f(xw) * rstd * hi_f(ww), hi_f(rw)));
+                        }
+                    }
+                    w_set(o, i, ow);
+                }
+                st_v4(out_row + (int64_t)c * kChunk, o);
+            }
+        cur = cur + 1 == NS ? 0 : cur + 1;
+    }
+    cp_async_wait<0>();
+}
+
+template <int TPR, int J, int NS, bool HIGH, int OP, int MODE>
+static cudaError_t launch_rms_pipe(const typename RmsPipeArgs<OP>::P& p, cudaStream_t s) {
+    auto k = rmsnorm_pipe_kernel<TPR, J, NS, HIGH, OP, MODE>;
+    using C = RowCfg<TPR, J, true>;
+    constexpr int NOPS = 1 + (MODE == kRmsModRing ? 1 : 0) + (OP == kRmsTanh ? 1 : 0);
+    using R = Ring<C, NS, NOPS>;
+    const int nch = p.D / kChunk;
+    const int tab_bytes = OP == kRmsTanh ? (((MBX_TANH_HI - MBX_TANH_LO) + 7) / 8) * 16 : 0;
+    const int fixed = nch * 16 + (MODE == kRmsModStaged ? 2 * nch * 16 : 0) + tab_bytes;
+    PipeShape sh;
+    if (!pipe_shape(reinterpret_cast<const void*>(k), TPR, (int)sizeof(TreeSmem) + R::kBytes, fixed, p.rows, &sh))
+        return cudaErrorInvalidConfiguration;
+    k<<<sh.grid, sh.groups * TPR, sh.smem, s>>>(p, sh.rows_per_cta);
+    return cudaGetLastError();
+}
+
+template <int OP, int TPR, int J, int NS>
+static cudaError_t launch_rms_pipe_v(const typename RmsPipeArgs<OP>::P& p, bool high, cudaStream_t s) {
+    const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
+    if (high)
+        return staged ? launch_rms_pipe<TPR, J, NS, true, OP, kRmsModStaged>(p, s)
+                      : launch_rms_pipe<TPR, J, NS, true, OP, kRmsModRing>(p, s);
+    return staged ? launch_rms_pipe<TPR, J, NS, false, OP, kRmsModStaged>(p, s)
+                  : launch_rms_pipe<TPR, J, NS, false, OP, kRmsModRing>(p, s);
+}
+
+template <int OP>
+static cudaError_t launch_rms_pipe_d(const typename RmsPipeArgs<OP>::P& p, bool high, cudaStream_t s) {
+    switch (chunks_per_lane(p.D)) {
+        case 1: return launch_rms_pipe_v<OP, 32, 1, 2>(p, high, s);
+        case 2: return launch_rms_pipe_v<OP, 32, 2, 2>(p, high, s);
+        case 3: return launch_rms_pipe_v<OP, 64, 3, 2>(p, high, s);
+        case 4: return launch_rms_pipe_v<OP, 64, 4, 2>(p, high, s);
+        case 5: return launch_rms_pipe_v<OP, 128, 5, 2>(p, high, s);
+        case 6: return launch_rms_pipe_v<OP, 128, 6, 2>(p, high, s);
+        case 7: return launch_rms_pipe_v<OP, 128, 7, 2>(p, high, s);
+        case 8: return launch_rms_pipe_v<OP, 128, 8, 2>(p, high, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 // ------------------------------------------------------------------ host
 
 template <class P, int TPR, int J, bool VEC, bool HIGH>
@@ -225,9 +480,7 @@ static cudaError_t launch_one(const P& p, cudaStream_t s) {
 }
 
 template <class P, int TPR, int J>
-static cudaError_t launch_j(const P& p, bool vec, bool high, cudaStream_t s) {
-    if (vec)
-        return high ? launch_one<P, TPR, J, true, true>(p, s) : launch_one<P, TPR, J, true, false>(p, s);
+static cudaError_t launch_j(const P& p, bool, bool high, cudaStream_t s) {
     return high ? launch_one<P, TPR, J, false, true>(p, s) : launch_one<P, TPR, J, false, false>(p, s);
 }
 
@@ -247,9 +500,11 @@ static cudaError_t launch_rms(const P& p, bool vec, bool high, cudaStream_t s) {
 }
 
 cudaError_t launch_rmsnorm_scale(const RmsScaleParams& p, bool vec, bool high, cudaStream_t s) {
+    if (vec) return launch_rms_pipe_d<kRmsScale>(p, high, s);
     return launch_rms(p, vec, high, s);
 }
 cudaError_t launch_rmsnorm_tanh_residual(const RmsTanhParams& p, bool vec, bool high, cudaStream_t s) {
+    if (vec) return launch_rms_pipe_d<kRmsTanh>(p, high, s);
     return launch_rms(p, vec, high, s);
 }
 

@@ -235,3 +235,11 @@ def test_device_rejections(mbx):
                                  ctypes.byref(mbx._view(sc)), ctypes.byref(mbx._view(sc)),
                                  ctypes.c_float(1e-6), 0)
     assert st == 0
+
+
+@pytest.mark.parametrize("rows,mrows,D", [(4096, 512, 1024), (6000, 3000, 3072), (2048, 1024, 5120)])
+def test_modulation_changing_within_a_cta(mbx, rows, mrows, D):
+    """Samples change every few rows (seq = rows / mod_rows is smaller than a
+    CTA's block of rows), so the modulation rows travel with x instead of being
+    staged once per CTA."""
+    _all_ops(mbx, _inputs(rows, D, mrows, seed=rows + D))
