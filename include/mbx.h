@@ -171,7 +171,8 @@ MBX_API int mbx_residual_gate_add(const mbx_view* out, const mbx_cview* x, const
  *     (cos[s][i], sin[s][i]): o0 = n0*c - n1*s, o1 = n0*s + n1*c.
  *   lossless: Q/K heads use the mbx_rmsnorm_scale chain without the scale
  *     (n = bf16(bf16(x*rstd)*w)), then o = bf16 of the binary32 rotation.
- *   hd must be 64, 128 or 256; branch rows must be 16-byte aligned.
+ *   hd must be 64, 128 or 256; branch rows must be 16-byte aligned;
+ *   batch * (S_txt + S_img) * heads must stay below 2^31 (MBX_E_ARG).
  */
 MBX_API int mbx_qk_norm_rope_qkv_epilogue(const mbx_view* joint, const mbx_cview* txt_qkv,
                                           const mbx_cview* img_qkv, int64_t batch, int64_t heads,
@@ -216,7 +217,10 @@ MBX_API int mbx_check_qk_norm_rope_qkv_epilogue(
  *   which = 3: the unguarded division the kernels use for lanes whose
  *              elements all have |x| >= 2^-60, vs div.rn, for every count
  *              k = 1..64 and every binary32 numerator with |d| >= 2^-100,
- *              and +0.
+ *              and +0;
+ *   which = 4: the reciprocal-square-root table of the QKV epilogue vs
+ *              bf16(div.rn(1, sqrt.rn(v))) for every non-negative bfloat16 v
+ *              (finite and +inf).
  * counts: device pointer to 2 uint64 counters (caller-owned), overwritten
  * with {mismatches between non-NaN results, mismatches where either is NaN}.
  * Enqueued on `stream`; the caller synchronises before reading counts.

@@ -66,6 +66,22 @@ struct GateAddParams {
     int64_t seq;
 };
 
+// Exact unsigned division by a runtime constant for numerators below 2^31
+// (Granlund & Montgomery, PLDI 1994): q = (n * m) >> shift with
+// shift = 31 + ceil(log2 d) and m = ceil(2^shift / d).
+struct FastDiv {
+    unsigned long long m;
+    unsigned shift;
+};
+inline FastDiv make_fastdiv(unsigned d) {
+    unsigned l = 0;
+    while ((1ull << l) < d) ++l;
+    FastDiv f;
+    f.shift = 31 + l;
+    f.m = ((1ull << f.shift) + d - 1) / d;
+    return f;
+}
+
 struct QkvParams {
     uint16_t* joint;
     const uint16_t* txt;
@@ -77,6 +93,10 @@ struct QkvParams {
     const uint16_t *wq_txt, *wk_txt, *wq_img, *wk_img;
     const float *cos_txt, *sin_txt, *cos_img, *sin_img;
     float eps;
+    // filled by the launcher
+    int hpasses;       // head passes per token
+    FastDiv by_stot;   // token -> batch index
+    FastDiv by_hpass;  // unit -> token
 };
 
 // ceil(ceil(D / 8) / 128): chunks per lane of a row of D elements.

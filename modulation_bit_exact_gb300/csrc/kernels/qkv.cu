@@ -7,14 +7,15 @@
 // reading the GEMM output through strided row views, so no intermediate
 // tensor is materialised.
 //
-// Work decomposition: a CTA owns one token at a time (persistent loop over
-// tokens).  Its threads form `slots` head units of hd/8 threads; thread l of a
-// unit holds the 8-element chunk l of the head, which is also logical lane l
-// of the 128-lane order (a head has at most 32 chunks, so the levels s >= 32
-// of the fixed tree only add empty lanes and the remaining levels are warp
-// shuffles within the unit).  All three parts of the token are loaded before
-// any is processed; every warp works on heads of a single part, so the
-// shuffles of a Q/K head never meet a V unit.
+// Work decomposition: a CTA owns one (token, head-pass) unit at a time
+// (persistent loop; a head pass is `slots` heads, all H heads when they fit in
+// 512 threads).  Its threads form `slots` head units of hd/8 threads; thread l
+// of a unit holds the 8-element chunk l of the head, which is also logical
+// lane l of the 128-lane order (a head has at most 32 chunks, so the levels
+// s >= 32 of the fixed tree only add empty lanes and the remaining levels are
+// warp shuffles within the unit).  The Q, K and V chunks of the next unit and
+// its table entries are loaded while the current unit is computed (a register
+// double buffer); a thread's Q and K sums travel together in one f32x2.
 //
 // Lossless Q/K head: the BF16-native RMSNorm chain without the scale
 // (sq = bf16(x*x), S over the lanes, ms = bf16(S/hd),
@@ -23,6 +24,7 @@
 // with c, s the token's table entries for pair i.  V is a bit copy.
 #include "launch.h"
 #include "rowops.cuh"
+#include "rstd_bf16_table.inc"
 
 namespace mbx {
 
@@ -34,110 +36,164 @@ __device__ __forceinline__ float4 ld_f4(const float* p) {
     return v;
 }
 
+__device__ __forceinline__ unsigned fast_div(unsigned n, const FastDiv& f) {
+    return (unsigned)(((unsigned long long)n * f.m) >> f.shift);
+}
+
+// bf16(1 / sqrt(inner)) for a bfloat16 `inner` (binary32 sqrt and division,
+// each correctly rounded): a lookup in a table generated from exactly that
+// definition and compared with div.rn(1, sqrt.rn(v)) on this GPU for every
+// bfloat16 v (mbx_selftest(4)).  NaN gives the canonical NaN.
+__device__ __forceinline__ float rstd_bf16(float inner) {
+    const uint32_t ib = __float_as_uint(inner) >> 16;
+    const uint32_t r = ib <= 0x7f80u ? (uint32_t)kRstdBf16[ib] : 0x7fffu;
+    return __uint_as_float(r << 16);
+}
+
+// One unit of work: the heads [hp*slots, hp*slots + slots) of one token.
+struct QkvUnit {
+    int64_t b, s, sb;
+    bool txt;
+    const uint16_t* src;
+    const float* cos_row;
+    const float* sin_row;
+};
+
+template <int HD>
+__device__ __forceinline__ QkvUnit qkv_unit(const QkvParams& p, int64_t tok) {
+    QkvUnit u;
+    const int64_t s_tot = p.s_txt + p.s_img;
+    u.b = fast_div((unsigned)tok, p.by_stot);
+    u.s = tok - u.b * s_tot;  // position in the joint sequence
+    u.txt = u.s < p.s_txt;
+    u.sb = u.txt ? u.s : u.s - p.s_txt;  // position within the branch
+    u.src = u.txt ? p.txt + (u.b * p.s_txt + u.sb) * p.txt_stride : p.img + (u.b * p.s_img + u.sb) * p.img_stride;
+    u.cos_row = (u.txt ? p.cos_txt : p.cos_img) + u.sb * (HD / 2);
+    u.sin_row = (u.txt ? p.sin_txt : p.sin_img) + u.sb * (HD / 2);
+    return u;
+}
+
 template <int TPH, bool HIGH>
-__global__ void __launch_bounds__(1024) qkv_epilogue_kernel(QkvParams p) {
+__global__ void __launch_bounds__(512) qkv_epilogue_kernel(QkvParams p) {
     constexpr int HD = TPH * kChunk;
     const int l = threadIdx.x % TPH;     // chunk / lane within the head
     const int slot = threadIdx.x / TPH;  // head unit within the CTA
     const int slots = blockDim.x / TPH;
     const int H = p.heads;
     const int64_t s_tot = p.s_txt + p.s_img;
-    const int64_t tokens = p.batch * s_tot;
-    const int hpasses = (H + slots - 1) / slots;
+    const int hpasses = p.hpasses;
+    const int64_t units = p.batch * s_tot * hpasses;
     const int64_t part_stride = (int64_t)H * HD;  // columns between Q, K and V
 
-    for (int64_t tok = blockIdx.x; tok < tokens; tok += gridDim.x) {
-        const int64_t b = tok / s_tot;
-        const int64_t s = tok - b * s_tot;  // position in the joint sequence
-        const bool txt = s < p.s_txt;
-        const int64_t sb = txt ? s : s - p.s_txt;  // position within the branch
-        const uint16_t* src = txt ? p.txt + (b * p.s_txt + sb) * p.txt_stride
-                                  : p.img + (b * p.s_img + sb) * p.img_stride;
-        const float* cos_row = (txt ? p.cos_txt : p.cos_img) + sb * (HD / 2);
-        const float* sin_row = (txt ? p.sin_txt : p.sin_img) + sb * (HD / 2);
-        const uint16_t* wq = txt ? p.wq_txt : p.wq_img;
-        const uint16_t* wk = txt ? p.wk_txt : p.wk_img;
+    // software pipeline: the next unit's chunks and table entries are in
+    // flight while the current one is computed
+    uint4 nx[3];
+    float4 nc, ns;
+    auto fetch = [&](int64_t unit) {
+        const int64_t tok = hpasses == 1 ? unit : fast_div((unsigned)unit, p.by_hpass);
+        const int hp = (int)(unit - tok * hpasses);
+        const QkvUnit u = qkv_unit<HD>(p, tok);
+        const int h = hp * slots + slot;
+#pragma unroll
+        for (int part = 0; part < 3; ++part)
+            nx[part] = h < H ? ld_stream(u.src + part * part_stride + (int64_t)h * HD + l * kChunk)
+                             : make_uint4(0, 0, 0, 0);
+        nc = ld_f4(u.cos_row + 4 * l);
+        ns = ld_f4(u.sin_row + 4 * l);
+    };
+    int64_t unit = blockIdx.x;
+    if (unit < units) fetch(unit);
+    for (; unit < units; unit += gridDim.x) {
+        const uint4 xq = nx[0], xk = nx[1], xv = nx[2];
+        const float4 c4 = nc, s4 = ns;
+        if (unit + gridDim.x < units) fetch(unit + gridDim.x);
 
-        for (int hp = 0; hp < hpasses; ++hp) {
-            const int h = hp * slots + slot;
-            const bool active = h < H;
-            // all three parts of this head first (more bytes in flight)
-            uint4 xv[3];
+        const int64_t tok = hpasses == 1 ? unit : fast_div((unsigned)unit, p.by_hpass);
+        const int hp = (int)(unit - tok * hpasses);
+        const QkvUnit u = qkv_unit<HD>(p, tok);
+        const int h = hp * slots + slot;
+        const bool active = h < H;
+        auto dst = [&](int part) {
+            return p.joint + ((((u.b * 3 + part) * H + h) * s_tot + u.s) * HD) + l * kChunk;
+        };
+        if (active) st_v4(dst(2), xv);  // V: bit copy
+
+        const uint4 wq = ld_shared_row((u.txt ? p.wq_txt : p.wq_img) + l * kChunk);
+        const uint4 wk = ld_shared_row((u.txt ? p.wk_txt : p.wk_img) + l * kChunk);
+        // lane sums of squares of the Q and K heads side by side (f32x2:
+        // Q in the low half, K in the high half), element order
+        u64 acc = f2(0.0f, 0.0f);
 #pragma unroll
-            for (int part = 0; part < 3; ++part)
-                xv[part] = active ? ld_stream(src + part * part_stride + (int64_t)h * HD + l * kChunk)
-                                  : make_uint4(0, 0, 0, 0);
-            const float4 c4 = ld_f4(cos_row + 4 * l);
-            const float4 s4 = ld_f4(sin_row + 4 * l);
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t a = w_of(xq, i), b = w_of(xk, i);
+            if constexpr (!HIGH) {
+                const uint32_t sa = bmul(a, a), sb = bmul(b, b);
+                acc = add2(acc, pair_elem(sa, sb, 0));
+                acc = add2(acc, pair_elem(sa, sb, 1));
+            } else {
+                acc = fma2(pair_elem(a, b, 0), pair_elem(a, b, 0), acc);
+                acc = fma2(pair_elem(a, b, 1), pair_elem(a, b, 1), acc);
+            }
+        }
 #pragma unroll
-            for (int part = 0; part < 3; ++part) {
-                uint16_t* dst = p.joint + ((((b * 3 + part) * H + h) * s_tot + s) * HD) + l * kChunk;
-                if (part == 2) {
-                    if (active) st_v4(dst, xv[2]);
-                    continue;
-                }
-                const uint4 x = xv[part];
-                const uint4 w = ld_shared_row((part == 0 ? wq : wk) + l * kChunk);
-                // lane sum of squares, element order
-                float acc = 0.0f;
+        for (int sh = TPH / 2; sh >= 1; sh /= 2)
+            acc = add2(acc, f2(__shfl_down_sync(0xffffffffu, f2lo(acc), sh, TPH),
+                               __shfl_down_sync(0xffffffffu, f2hi(acc), sh, TPH)));
+        const float Sq = __shfl_sync(0xffffffffu, f2lo(acc), 0, TPH);
+        const float Sk = __shfl_sync(0xffffffffu, f2hi(acc), 0, TPH);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            const uint4 x = part == 0 ? xq : xk, w = part == 0 ? wq : wk;
+            const float S = part == 0 ? Sq : Sk;
+            uint4 o;
+            if constexpr (!HIGH) {
+                // S / HD: HD is a power of two, so the product is the correctly
+                // rounded quotient
+                const float ms = lo_f(pack_rn(__fmul_rn(S, 1.0f / HD), 0.0f));
+                const float inner = lo_f(pack_rn(__fadd_rn(ms, p.eps), 0.0f));
+                const uint32_t r2 = bf16_bits(rstd_bf16(inner));
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    uint32_t xw = w_of(x, i);
-                    if constexpr (!HIGH) {
-                        uint32_t sq = bmul(xw, xw);
-                        acc = __fadd_rn(acc, lo_f(sq));
-                        acc = __fadd_rn(acc, hi_f(sq));
-                    } else {
-                        acc = fmaf(lo_f(xw), lo_f(xw), acc);
-                        acc = fmaf(hi_f(xw), hi_f(xw), acc);
-                    }
+                    const uint32_t n = bmul(bmul(w_of(x, i), r2), w_of(w, i));
+                    const float c = i == 0 ? c4.x : i == 1 ? c4.y : i == 2 ? c4.z : c4.w;
+                    const float sn = i == 0 ? s4.x : i == 1 ? s4.y : i == 2 ? s4.z : s4.w;
+                    // two roundings per product, one per sum: scalar
+                    // intrinsics, never merged into a fused multiply-add
+                    const float n0 = lo_f(n), n1 = hi_f(n);
+                    const float o0 = __fsub_rn(__fmul_rn(n0, c), __fmul_rn(n1, sn));
+                    const float o1 = __fadd_rn(__fmul_rn(n0, sn), __fmul_rn(n1, c));
+                    w_set(o, i, pack_rn(o0, o1));
                 }
+            } else {
+                const float rstd = rsqrtf(S / (float)HD + p.eps);
 #pragma unroll
-                for (int sh = TPH / 2; sh >= 1; sh /= 2)
-                    acc = __fadd_rn(acc, __shfl_down_sync(0xffffffffu, acc, sh, TPH));
-                const float S = __shfl_sync(0xffffffffu, acc, 0, TPH);
-                uint4 o;
-                if constexpr (!HIGH) {
-                    float ms = lo_f(pack_rn(__fdiv_rn(S, (float)HD), 0.0f));
-                    float inner = lo_f(pack_rn(__fadd_rn(ms, p.eps), 0.0f));
-                    float rstd = lo_f(pack_rn(__fdiv_rn(1.0f, __fsqrt_rn(inner)), 0.0f));
-                    const uint32_t r2 = bf16_bits(rstd);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint32_t n = bmul(bmul(w_of(x, i), r2), w_of(w, i));
-                        float c = i == 0 ? c4.x : i == 1 ? c4.y : i == 2 ? c4.z : c4.w;
-                        float sn = i == 0 ? s4.x : i == 1 ? s4.y : i == 2 ? s4.z : s4.w;
-                        // two roundings per product, one per sum: scalar
-                        // intrinsics, never merged into a fused multiply-add
-                        const float n0 = lo_f(n), n1 = hi_f(n);
-                        const float o0 = __fsub_rn(__fmul_rn(n0, c), __fmul_rn(n1, sn));
-                        const float o1 = __fadd_rn(__fmul_rn(n0, sn), __fmul_rn(n1, c));
-                        w_set(o, i, pack_rn(o0, o1));
-                    }
-                } else {
-                    float rstd = rsqrtf(S / (float)HD + p.eps);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint32_t xw = w_of(x, i), ww = w_of(w, i);
-                        float n0 = lo_f(xw) * rstd * lo_f(ww), n1 = hi_f(xw) * rstd * hi_f(ww);
-                        float c = i == 0 ? c4.x : i == 1 ? c4.y : i == 2 ? c4.z : c4.w;
-                        float sn = i == 0 ? s4.x : i == 1 ? s4.y : i == 2 ? s4.z : s4.w;
-                        w_set(o, i, pack_rn(fmaf(n0, c, -n1 * sn), fmaf(n0, sn, n1 * c)));
-                    }
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t xw = w_of(x, i), ww = w_of(w, i);
+                    const float n0 = lo_f(xw) * rstd * lo_f(ww), n1 = hi_f(xw) * rstd * hi_f(ww);
+                    const float c = i == 0 ? c4.x : i == 1 ? c4.y : i == 2 ? c4.z : c4.w;
+                    const float sn = i == 0 ? s4.x : i == 1 ? s4.y : i == 2 ? s4.z : s4.w;
+                    w_set(o, i, pack_rn(fmaf(n0, c, -n1 * sn), fmaf(n0, sn, n1 * c)));
                 }
-                if (active) st_v4(dst, o);
             }
+            if (active) st_v4(dst(part), o);
         }
     }
 }
 
 template <int TPH, bool HIGH>
-static cudaError_t launch_one(const QkvParams& p, cudaStream_t s) {
+static cudaError_t launch_one(const QkvParams& p0, cudaStream_t s) {
     auto k = qkv_epilogue_kernel<TPH, HIGH>;
-    int slots = p.heads < 1024 / TPH ? (int)p.heads : 1024 / TPH;
+    int slots = p0.heads < 512 / TPH ? (int)p0.heads : 512 / TPH;
     int block = slots * TPH;
     if (block % 32) block += 32 - block % 32;  // whole warps (extra units idle)
-    int grid = grid_for_rows(reinterpret_cast<const void*>(k), p.batch * (p.s_txt + p.s_img), 1, block);
+    slots = block / TPH;
+    QkvParams p = p0;
+    p.hpasses = (p.heads + slots - 1) / slots;
+    const int64_t tokens = p.batch * (p.s_txt + p.s_img);
+    if (tokens * p.hpasses >= (1ll << 31)) return cudaErrorInvalidValue;
+    p.by_stot = make_fastdiv((unsigned)(p.s_txt + p.s_img));
+    p.by_hpass = make_fastdiv((unsigned)p.hpasses);
+    int grid = grid_for_rows(reinterpret_cast<const void*>(k), tokens * p.hpasses, 1, block);
     if (grid < 0) return cudaErrorUnknown;
     k<<<grid, block, 0, s>>>(p);
     return cudaGetLastError();

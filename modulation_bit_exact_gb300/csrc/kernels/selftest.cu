@@ -6,11 +6,14 @@
 //   1: mul.rn.bf16x2 == binary32 multiply then round, every operand pair;
 //   2: add.rn.bf16x2 == binary32 add then round, every operand pair;
 //   3: div_k_fast<K>(d) (no guard) == div.rn(d, K) for K = 1..64, every
-//      binary32 d with |d| >= 2^-100, and d = +0.
+//      binary32 d with |d| >= 2^-100, and d = +0;
+//   4: the QKV epilogue's rstd table == bf16(div.rn(1, sqrt.rn(v))) for every
+//      non-negative bfloat16 v (finite and +inf).
 // A mismatch where either result is a NaN is counted apart from the others:
 // NaN payloads never reach a bfloat16 output except as the canonical NaN.
 #include "launch.h"
 #include "numerics.cuh"
+#include "rstd_bf16_table.inc"
 
 namespace mbx {
 
@@ -68,6 +71,18 @@ __global__ void selftest_bf16x2_kernel(unsigned long long* counts) {
     if (bad_nan) atomicAdd(&counts[1], bad_nan);
 }
 
+// The rstd table of the QKV epilogue vs bf16(div.rn(1, sqrt.rn(v))) for
+// every bfloat16 pattern v with a non-negative finite or +inf value.
+__global__ void selftest_rstd_kernel(unsigned long long* counts) {
+    unsigned long long bad = 0;
+    for (uint32_t v = blockIdx.x * blockDim.x + threadIdx.x; v <= 0x7f80u; v += gridDim.x * blockDim.x) {
+        const float x = __uint_as_float(v << 16);
+        const uint32_t want = pack_rn(__fdiv_rn(1.0f, __fsqrt_rn(x)), 0.0f) & 0xffffu;
+        if ((uint32_t)kRstdBf16[v] != want) ++bad;
+    }
+    if (bad) atomicAdd(&counts[0], bad);
+}
+
 cudaError_t launch_selftest(int which, unsigned long long* counts, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(counts, 0, 2 * sizeof(unsigned long long), s);
     if (e != cudaSuccess) return e;
@@ -78,6 +93,7 @@ cudaError_t launch_selftest(int which, unsigned long long* counts, cudaStream_t 
     switch (which) {
         case 0: selftest_div_kernel<false><<<grid, block, 0, s>>>(counts); break;
         case 3: selftest_div_kernel<true><<<grid, block, 0, s>>>(counts); break;
+        case 4: selftest_rstd_kernel<<<grid, block, 0, s>>>(counts); break;
         case 1: selftest_bf16x2_kernel<true><<<grid, block, 0, s>>>(counts); break;
         case 2: selftest_bf16x2_kernel<false><<<grid, block, 0, s>>>(counts); break;
         default: return cudaErrorInvalidValue;

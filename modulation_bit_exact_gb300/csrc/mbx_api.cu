@@ -272,6 +272,7 @@ int check_qkv(const mbx_view* joint, const mbx_cview* txt, const mbx_cview* img,
     if (has_t && (t.cols != width || t.rows % batch)) return MBX_E_SHAPE;
     if (has_i && (im.cols != width || im.rows % batch)) return MBX_E_SHAPE;
     const int64_t s_txt = t.rows / batch, s_img = im.rows / batch;
+    if ((s_txt + s_img) * batch * heads >= (int64_t(1) << 31)) return MBX_E_ARG;  // 32-bit unit index
     if (j.rows != batch * 3 * heads * (s_txt + s_img)) return MBX_E_SHAPE;
     if (j.rows > 1 && j.stride != hd) return MBX_E_STRIDE;  // joint is contiguous
     // 128-bit paths only: every row start 16-byte aligned
@@ -565,7 +566,7 @@ MBX_API int mbx_qk_norm_rope_qkv_epilogue(const mbx_view* joint, const mbx_cview
 
 MBX_API int mbx_selftest(int which, unsigned long long* counts, void* stream) {
     if (!counts) return MBX_E_NULL;
-    if (which < 0 || which > 3) return MBX_E_ARG;
+    if (which < 0 || which > 4) return MBX_E_ARG;
     if (reinterpret_cast<uintptr_t>(counts) % 8) return MBX_E_ALIGN;
     MBX_TRY(raw_on_device(counts, 16));
     return cuda_status(mbx::launch_selftest(which, counts, (cudaStream_t)stream));

@@ -198,6 +198,7 @@ def test_selftest_rejections(mbx):
     L = mbx.lib()
     assert L.mbx_selftest(0, None, None) == -1
     assert L.mbx_selftest(7, BASE, None) == -12
+    assert L.mbx_selftest(5, BASE, None) == -12
     assert L.mbx_selftest(-1, BASE, None) == -12
     assert L.mbx_selftest(0, BASE + 4, None) == -7
 

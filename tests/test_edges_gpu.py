@@ -28,7 +28,8 @@ def bf(bits: np.ndarray) -> torch.Tensor:
 
 @pytest.mark.parametrize("which,what", [(0, "division by counts 1..64"),
                                         (1, "bf16x2 multiply"), (2, "bf16x2 add"),
-                                        (3, "unguarded division, |d| >= 2^-100")])
+                                        (3, "unguarded division, |d| >= 2^-100"),
+                                        (4, "reciprocal square root table")])
 def test_exhaustive_building_blocks(mbx, which, what):
     bad, bad_nan = mbx.selftest(which)
     assert bad == 0, f"{what}: {bad} non-NaN mismatches"
