@@ -387,6 +387,96 @@ def run_gpu(args):
     return 0
 
 
+# ---------------------------------------------------------------------- suite
+
+
+def run_suite(args):
+    """Every operation x variant on the configurations' shapes, one JSON line
+    per case: device time per call (CUDA events, median of 5 repeats of a
+    rotating loop over buffer sets whose total exceeds L2), GB/s of the
+    algorithmic bytes and the fraction of the measured HBM peak."""
+    import torch
+
+    import modulation_bit_exact_gb300 as mbx
+    import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, _ = peaks()
+    L2 = 129 * 2 ** 20
+
+    def time_cases(make, nbytes, fn):
+        per_set = max(1, nbytes)
+        nsets = max(2, min(8, int(3 * L2 // per_set) + 1))
+        sets = [make(i) for i in range(nsets)]
+        for i in range(3 * nsets):
+            fn(sets[i % nsets])
+        torch.cuda.synchronize(dev)
+        reps = max(10, min(200, int(2e9 // per_set)))
+        times = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for i in range(reps):
+                fn(sets[i % nsets])
+            b.record()
+            torch.cuda.synchronize(dev)
+            times.append(a.elapsed_time(b) / reps * 1e3)
+        times.sort()
+        return times[2]
+
+    def row_case(name, B, S, D, tok):
+        rows = B * S
+        mrows = rows if tok else B
+
+        def make(i):
+            g = torch.Generator(device=dev).manual_seed(1000 + i)
+            r = lambda *sh, std=1.0, mean=0.0: (torch.randn(*sh, generator=g, device=dev) * std + mean).to(torch.bfloat16)
+            return dict(x=r(rows, D), y=r(rows, D), res=r(rows, D), g=r(mrows, D) if tok else r(mrows, D, std=0.1),
+                        sc=r(mrows, D, std=0.1), sh=r(mrows, D, std=0.1), w=r(D, std=0.05, mean=1.0),
+                        out=torch.empty(rows, D, dtype=torch.bfloat16, device=dev))
+        T = rows * D * 2
+        M = mrows * D * 2
+        ops = {
+            "ln_modulate": (2 * T + 2 * M, lambda s, v: mbx.ln_modulate(s["x"], s["sc"], s["sh"], variant=v, out=s["out"])),
+            "rmsnorm_scale": (2 * T + M + D * 2, lambda s, v: mbx.rmsnorm_scale(s["x"], s["w"], s["sc"], variant=v, out=s["out"])),
+            "rmsnorm_tanh_residual": (3 * T + M + D * 2, lambda s, v: mbx.rmsnorm_tanh_residual(s["x"], s["g"], s["res"], s["w"], variant=v, out=s["out"])),
+            "residual_gate_add": (3 * T + M, lambda s, v: mbx.residual_gate_add(s["x"], s["g"], s["y"], variant=v, out=s["out"])),
+        }
+        for op, (nb, fn) in ops.items():
+            for v in ("lossless", "high"):
+                us = time_cases(make, nb, lambda st: fn(st, v))
+                gbs = nb / (us * 1e-6) / 1e9
+                print(json.dumps({"case": name, "shape": [rows, D], "modulation": "per-token" if tok else "per-sample",
+                                  "op": op, "variant": v, "us_per_call": round(us, 2), "bytes": nb,
+                                  "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}), flush=True)
+
+    def qkv_case(name, B, s_txt, gh, gw, H):
+        hd = 128
+
+        def make(i):
+            return synth.qkv_epilogue_case(seed=2000 + i, device=dev, batch=B, s_txt=s_txt, grid_h=gh, grid_w=gw, heads=H)
+        nb = 2 * B * (s_txt + gh * gw) * 3 * H * hd * 2
+        for v in ("lossless", "high"):
+            fn = lambda q: mbx.qk_norm_rope_qkv_epilogue(q["txt"], q["img"], B, H, hd, q["wq_txt"], q["wk_txt"],
+                                                         q["wq_img"], q["wk_img"], q["cos_txt"], q["sin_txt"],
+                                                         q["cos_img"], q["sin_img"], variant=v)
+            us = time_cases(make, nb, fn)
+            gbs = nb / (us * 1e-6) / 1e9
+            print(json.dumps({"case": name, "shape": [B, s_txt, gh * gw, H, hd], "op": "qk_norm_rope_qkv_epilogue",
+                              "variant": v, "us_per_call": round(us, 2), "bytes": nb, "gbs": round(gbs, 1),
+                              "frac_of_peak": round(gbs / peak, 4)}), flush=True)
+
+    row_case("tiny [2,256,512]", 2, 256, 512, False)
+    row_case("image-DiT [2,4352,3072]", 2, 4352, 3072, False)
+    qkv_case("QKV epilogue [2,256+64x64,24x128]", 2, 256, 64, 64, 24)
+    row_case("video-DiT [1,32760,5120] per-token", 1, 32760, 5120, True)
+    for D in (1024, 4096, 8192):
+        for T in (4096, 65536):
+            row_case(f"sweep [{T},{D}]", 1, T, D, False)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -394,7 +484,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", default="mbx", choices=["mbx", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--suite", action="store_true",
+                    help="time every operation and variant on the configurations' shapes "
+                         "(one JSON line per case) instead of the benchmark step")
     args = ap.parse_args()
+    if args.suite:
+        return run_suite(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

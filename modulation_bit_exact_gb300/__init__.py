@@ -67,6 +67,8 @@ _lib = None
 
 def _load() -> ctypes.CDLL:
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -141,8 +143,13 @@ def _rows_cols(t: torch.Tensor) -> tuple[int, int, int]:
 
 
 def _view(t: torch.Tensor) -> _View:
-    rows, cols, stride = _rows_cols(t)
     dtype = MBX_BF16 if t.dtype == torch.bfloat16 else 0
+    if t.is_contiguous() and t.dim() > 0:  # the common case, without the general walk
+        cols = t.shape[-1]
+        n = t.numel()
+        if n:
+            return _View(t.data_ptr(), n // cols, cols, cols, dtype)
+    rows, cols, stride = _rows_cols(t)
     return _View(t.data_ptr() if t.numel() else None, rows, cols, stride, dtype)
 
 
@@ -150,10 +157,17 @@ def _ref(v: _View):
     return ctypes.byref(v)
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(t: torch.Tensor) -> int:
-    if t.is_cuda:
-        return torch.cuda.current_stream(t.device).cuda_stream
-    return 0
+    """The caller's current CUDA stream on t's device (0 for host tensors,
+    which the library then refuses)."""
+    if not t.is_cuda:
+        return 0
+    if _raw_stream is not None:
+        return _raw_stream(t.get_device())
+    return torch.cuda.current_stream(t.device).cuda_stream
 
 
 def _variant(v) -> int:

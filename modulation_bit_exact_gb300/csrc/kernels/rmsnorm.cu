@@ -217,7 +217,8 @@ __global__ void __launch_bounds__(kBlock) rmsnorm_tanh_residual_kernel(RmsTanhPa
 // (and every per-row operand) streamed through a per-row-group ring of
 // shared-memory stages by cp.async, and the weight row (plus per-sample
 // modulation rows, when a CTA's block of rows spans at most two samples)
-// staged once per CTA.  OP 0: rmsnorm_scale (mod = scale);
+// staged once per CTA (for the tanh op, tanh of a per-sample gate is staged
+// instead of the gate).  OP 0: rmsnorm_scale (mod = scale);
 // OP 1: rmsnorm_tanh_residual (mod = gate, plus the residual in the ring).
 enum { kRmsScale = 0, kRmsTanh = 1 };
 enum { kRmsModRing = 0, kRmsModStaged = 1 };
@@ -322,7 +323,7 @@ __global__ void __launch_bounds__(512) rmsnorm_pipe_kernel(typename RmsPipeArgs<
     uint4* wsm = reinterpret_cast<uint4*>(smem_raw + groups * sizeof(TreeSmem));  // weight [nch]
     uint4* msm = wsm + nch;                                                       // mod [2][nch]
     unsigned short* tab = reinterpret_cast<unsigned short*>(msm + (MODE == kRmsModStaged ? 2 * nch : 0));
-    constexpr int kTab = OP == kRmsTanh ? (MBX_TANH_HI - MBX_TANH_LO) : 0;
+    constexpr int kTab = OP == kRmsTanh && MODE == kRmsModRing ? (MBX_TANH_HI - MBX_TANH_LO) : 0;
     const R ring{reinterpret_cast<uint4*>(tab + ((kTab + 7) / 8) * 8) + (size_t)g * (R::kBytes / 16)};
     const int bar_id = 1 + g;
     const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
@@ -349,10 +350,18 @@ __global__ void __launch_bounds__(512) rmsnorm_pipe_kernel(typename RmsPipeArgs<
         const int slots = (int)((r1 - 1) / p.seq - m0 + 1);
         for (int i = threadIdx.x; i < slots * nch; i += blockDim.x) {
             const int slot = i / nch, c = i - slot * nch;
-            msm[slot * nch + c] = ld_shared_row(modp + (m0 + slot) * mod_stride + (int64_t)c * kChunk);
+            uint4 v = ld_shared_row(modp + (m0 + slot) * mod_stride + (int64_t)c * kChunk);
+            if constexpr (OP == kRmsTanh && !HIGH) {
+                // a per-sample gate is shared by all its rows: stage tanh(gate)
+                v.x = tanh2(v.x, kTanhBf16);
+                v.y = tanh2(v.y, kTanhBf16);
+                v.z = tanh2(v.z, kTanhBf16);
+                v.w = tanh2(v.w, kTanhBf16);
+            }
+            msm[slot * nch + c] = v;
         }
     }
-    if constexpr (OP == kRmsTanh && !HIGH)
+    if constexpr (OP == kRmsTanh && !HIGH && MODE == kRmsModRing)
         for (int i = threadIdx.x; i < kTab; i += blockDim.x) tab[i] = kTanhBf16[i];
     __syncthreads();
 
@@ -410,7 +419,8 @@ __global__ void __launch_bounds__(512) rmsnorm_pipe_kernel(typename RmsPipeArgs<
                         const uint32_t rw = w_of(RS, i);
                         if constexpr (!HIGH) {
                             const uint32_t n = bmul(bmul(xw, r2), ww);
-                            ow = badd(rw, bmul(tanh2(mw, tab), n));
+                            const uint32_t tg = MODE == kRmsModStaged ? mw : tanh2(mw, tab);
+                            ow = badd(rw, bmul(tg, n));
                         } else {
                             ow = pack_rn(fmaf(tanhf(lo_f(mw)), lo_f(xw) * rstd * lo_f(ww), lo_f(rw)),
                                          fmaf(tanhf(hi_f(mw)), hi_f(xw) * rstd * hi_f(ww), hi_f(rw)));
@@ -432,7 +442,7 @@ static cudaError_t launch_rms_pipe(const typename RmsPipeArgs<OP>::P& p, cudaStr
     constexpr int NOPS = 1 + (MODE == kRmsModRing ? 1 : 0) + (OP == kRmsTanh ? 1 : 0);
     using R = Ring<C, NS, NOPS>;
     const int nch = p.D / kChunk;
-    const int tab_bytes = OP == kRmsTanh ? (((MBX_TANH_HI - MBX_TANH_LO) + 7) / 8) * 16 : 0;
+    const int tab_bytes = OP == kRmsTanh && MODE == kRmsModRing ? (((MBX_TANH_HI - MBX_TANH_LO) + 7) / 8) * 16 : 0;
     const int fixed = nch * 16 + (MODE == kRmsModStaged ? 2 * nch * 16 : 0) + tab_bytes;
     PipeShape sh;
     if (!pipe_shape(reinterpret_cast<const void*>(k), TPR, (int)sizeof(TreeSmem) + R::kBytes, fixed, p.rows, &sh))
