@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
                 "orc_rmsnorm_tanh_residual": [_p, _i64, _p, _i64, _i64, _i64, _p, _i64, _i64,
                                               _p, _i64, _p, _f32],
                 "orc_residual_gate_add": [_p, _i64, _p, _i64, _i64, _i64, _p, _i64, _i64, _p, _i64],
+                "orc_gated_residual_ln_modulate": [_p, _p, _p, _i64, _i64, _i64, _p, _i64, _p, _p,
+                                                   _i64, _p, _i64, _p, _i64, _i64, _f32],
                 "orc_qkv_epilogue": [_p, _p, _i64, _i64, _p, _i64, _i64, _i64, _i64, _i64,
                                      _p, _p, _p, _p, _p, _p, _p, _p, _f32],
                 "orc_ln_modulate_f64": [_p, _p, _p, _i64, _i64, _i64, _p, _i64, _p, _i64, _i64, _f32],
@@ -228,6 +230,37 @@ def residual_gate_add(x: np.ndarray, gate: np.ndarray, y: np.ndarray) -> np.ndar
     out = np.empty((rows, D), dtype=np.uint16)
     lib().orc_residual_gate_add(_ptr(out), D, _ptr(x2), xs, rows, D, _ptr(g2), gs, grows, _ptr(y2), ys)
     return out
+
+
+def gated_residual_ln_modulate(residual: np.ndarray, gate: np.ndarray, update: np.ndarray,
+                               bias, scale: np.ndarray, shift: np.ndarray,
+                               eps: float = 1e-6) -> tuple[np.ndarray, np.ndarray]:
+    """Gated residual update fused into LN + AdaLN modulate; returns (r', out).
+
+    tahou.com SGLang diffusion article, section Qwen-Image FP8和NVFP4优化 (the
+    ``residual = residual + gate * (attention + bias)`` chain, then layer_norm
+    and ``* (1 + scale) + shift``), each step rounded to bfloat16 as the eager
+    chain rounds it; r' is the new residual stream, out the modulated norm.
+    """
+    r2, rs = _rows(residual)
+    rows, D = r2.shape
+    u2, us = _rows(update)
+    if u2.shape != (rows, D):
+        raise ValueError("update must match residual")
+    g2, gs, mrows = _mod_rows(r2, gate, D)
+    sc, scs, m2 = _mod_rows(r2, scale, D)
+    sh, shs, m3 = _mod_rows(r2, shift, D)
+    if not (mrows == m2 == m3):
+        raise ValueError("gate, scale and shift must share their rows")
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.uint16).reshape(-1)
+    if b is not None and b.size != D:
+        raise ValueError("bias must have D elements")
+    res_out = np.empty((rows, D), dtype=np.uint16)
+    out = np.empty((rows, D), dtype=np.uint16)
+    lib().orc_gated_residual_ln_modulate(_ptr(res_out), _ptr(out), _ptr(r2), rs, rows, D, _ptr(u2), us,
+                                         None if b is None else _ptr(b), _ptr(g2), gs, _ptr(sc), scs,
+                                         _ptr(sh), shs, mrows, eps)
+    return res_out, out
 
 
 def qkv_epilogue(txt: np.ndarray | None, img: np.ndarray | None, batch: int, heads: int,

@@ -302,6 +302,33 @@ void orc_residual_gate_add(uint16_t* out, int64_t out_stride, const uint16_t* x,
     }
 }
 
+/* Gated residual fused into LayerNorm + AdaLN modulate [NVFP4 producer chain]:
+ * tahou.com article, section Qwen-Image FP8和NVFP4优化 (the chain PR #37129
+ * fuses, without its FP4 quantisation):
+ *   a   = update, or bf16(update + bias) when a bias row is given
+ *   r'  = bf16(residual + bf16(gate * a))        the new residual stream
+ *   out = the LN + modulate chain of orc_ln_modulate applied to r'
+ * gate, scale and shift share mod_rows.  Writes r' and out. */
+void orc_gated_residual_ln_modulate(uint16_t* res_out, uint16_t* out, const uint16_t* residual,
+                                    int64_t res_stride, int64_t rows, int64_t D,
+                                    const uint16_t* update, int64_t upd_stride,
+                                    const uint16_t* bias, const uint16_t* gate,
+                                    int64_t gate_stride, const uint16_t* scale,
+                                    int64_t scale_stride, const uint16_t* shift,
+                                    int64_t shift_stride, int64_t mod_rows, float eps) {
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t* gr = gate + mod_row(r, rows, mod_rows) * gate_stride;
+        uint16_t* dst = res_out + r * D;
+        for (int64_t e = 0; e < D; ++e) {
+            float a = f_of(update[r * upd_stride + e]);
+            if (bias) a = fb(a + f_of(bias[e]));
+            float ga = fb(f_of(gr[e]) * a);
+            dst[e] = bf16_of(f_of(residual[r * res_stride + e]) + ga);
+        }
+    }
+    orc_ln_modulate(out, D, res_out, D, rows, D, scale, scale_stride, shift, shift_stride, mod_rows, eps);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Fused QKV epilogue [QKV]                                                 */
 /* ------------------------------------------------------------------------ */

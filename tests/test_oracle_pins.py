@@ -548,3 +548,29 @@ def test_qk_head_f64_reference(orc):
     c, s = d["cos_txt"][3].double(), d["sin_txt"][3].double()
     want = torch.stack([n[0::2] * c - n[1::2] * s, n[0::2] * s + n[1::2] * c], -1).reshape(-1)
     assert np.allclose(out, want.numpy(), rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- gated residual + LN + modulate
+
+
+def test_gated_residual_ln_modulate_is_the_composition(orc):
+    """Without a bias the fused chain is residual_gate_add followed by
+    ln_modulate on its result; with one, the bias add is the eager bf16
+    `update + bias` (PyTorch CPU) feeding the same composition."""
+    g = torch.Generator().manual_seed(41)
+    rows, D = 48, 1000
+    r = torch.randn(rows, D, generator=g).to(torch.bfloat16)
+    u = torch.randn(rows, D, generator=g).to(torch.bfloat16)
+    b = (0.1 * torch.randn(D, generator=g)).to(torch.bfloat16)
+    gate = (0.1 * torch.randn(3, D, generator=g)).to(torch.bfloat16)
+    sc = (0.1 * torch.randn(3, D, generator=g)).to(torch.bfloat16)
+    sh = (0.1 * torch.randn(3, D, generator=g)).to(torch.bfloat16)
+    R, U, G, SC, SH = u16(r), u16(u), u16(gate), u16(sc), u16(sh)
+    for bias, a in ((None, U), (u16(b), u16(u + b))):
+        res, out = orc.gated_residual_ln_modulate(R, G, U, bias, SC, SH, 1e-6)
+        want_res = orc.residual_gate_add(R, G, a)
+        assert np.array_equal(res, want_res)
+        assert np.array_equal(out, orc.ln_modulate(want_res, SC, SH, 1e-6))
+    # the residual stream itself against PyTorch CPU eager bf16 ops
+    res, _ = orc.gated_residual_ln_modulate(R, G, U, u16(b), SC, SH, 1e-6)
+    assert np.array_equal(res, u16(r + gate.repeat_interleave(16, 0) * (u + b)))
