@@ -434,7 +434,8 @@ def run_suite(args):
             r = lambda *sh, std=1.0, mean=0.0: (torch.randn(*sh, generator=g, device=dev) * std + mean).to(torch.bfloat16)
             return dict(x=r(rows, D), y=r(rows, D), res=r(rows, D), g=r(mrows, D) if tok else r(mrows, D, std=0.1),
                         sc=r(mrows, D, std=0.1), sh=r(mrows, D, std=0.1), w=r(D, std=0.05, mean=1.0),
-                        out=torch.empty(rows, D, dtype=torch.bfloat16, device=dev))
+                        b=r(1, D, std=0.5), out=torch.empty(rows, D, dtype=torch.bfloat16, device=dev),
+                        out2=torch.empty(rows, D, dtype=torch.bfloat16, device=dev))
         T = rows * D * 2
         M = mrows * D * 2
         ops = {
@@ -442,6 +443,8 @@ def run_suite(args):
             "rmsnorm_scale": (2 * T + M + D * 2, lambda s, v: mbx.rmsnorm_scale(s["x"], s["w"], s["sc"], variant=v, out=s["out"])),
             "rmsnorm_tanh_residual": (3 * T + M + D * 2, lambda s, v: mbx.rmsnorm_tanh_residual(s["x"], s["g"], s["res"], s["w"], variant=v, out=s["out"])),
             "residual_gate_add": (3 * T + M, lambda s, v: mbx.residual_gate_add(s["x"], s["g"], s["y"], variant=v, out=s["out"])),
+            "gated_residual_ln_modulate": (4 * T + 3 * M + D * 2, lambda s, v: mbx.gated_residual_ln_modulate(
+                s["res"], s["g"], s["y"], s["sc"], s["sh"], bias=s["b"], variant=v, out=s["out"], residual_out=s["out2"])),
         }
         for op, (nb, fn) in ops.items():
             for v in ("lossless", "high"):

@@ -154,6 +154,29 @@ MBX_API int mbx_residual_gate_add(const mbx_view* out, const mbx_cview* x, const
                                   const mbx_cview* y, int variant, void* stream);
 
 /*
+ * Gated residual update fused into LayerNorm + AdaLN modulate.
+ * Defined in: tahou.com SGLang diffusion article, section
+ * Qwen-Image FP8和NVFP4优化 -- residual = residual + gate * (attention + bias);
+ * hidden = layer_norm(residual); hidden = hidden * (1 + scale) + shift -- the
+ * chain the pages fuse into one producer (here without the FP4 quantisation).
+ *   r'  = bf16(residual + bf16(gate * a)), a = update, or bf16(update + bias)
+ *   out = the mbx_ln_modulate chain of r' (lossless or high)
+ * r' is written to residual_out in both variants with the eager rounding
+ * (it is the residual stream the next layer reads); `variant` applies to the
+ * norm.  One pass reads residual and update and writes r' and out (8 bytes per
+ * element, against 10 for mbx_residual_gate_add then mbx_ln_modulate).
+ * residual_out, out, residual, update [rows, D]; gate, scale, shift
+ * [mod_rows, D] with the same mod_rows; bias [1, D] or NULL.
+ * residual_out may be exactly residual (in-place update of the stream); out
+ * overlaps nothing; any other overlap is MBX_E_ALIAS.
+ */
+MBX_API int mbx_gated_residual_ln_modulate(const mbx_view* residual_out, const mbx_view* out,
+                                           const mbx_cview* residual, const mbx_cview* gate,
+                                           const mbx_cview* update, const mbx_cview* bias,
+                                           const mbx_cview* scale, const mbx_cview* shift,
+                                           float eps, int variant, void* stream);
+
+/*
  * Fused post-GEMM QKV epilogue.
  * Defined in: tahou.com SGLang diffusion article, section 合并QKV投影时的数值问题:
  * after the merged QKV GEMM one kernel does Q/K RMSNorm, interleaved RoPE,
@@ -198,6 +221,11 @@ MBX_API int mbx_check_rmsnorm_tanh_residual(const mbx_view* out, const mbx_cview
                                             const mbx_cview* weight, float eps, int variant);
 MBX_API int mbx_check_residual_gate_add(const mbx_view* out, const mbx_cview* x,
                                         const mbx_cview* gate, const mbx_cview* y, int variant);
+MBX_API int mbx_check_gated_residual_ln_modulate(const mbx_view* residual_out,
+                                                 const mbx_view* out, const mbx_cview* residual,
+                                                 const mbx_cview* gate, const mbx_cview* update,
+                                                 const mbx_cview* bias, const mbx_cview* scale,
+                                                 const mbx_cview* shift, float eps, int variant);
 MBX_API int mbx_check_qk_norm_rope_qkv_epilogue(
     const mbx_view* joint, const mbx_cview* txt_qkv, const mbx_cview* img_qkv, int64_t batch,
     int64_t heads, const mbx_cview* wq_txt, const mbx_cview* wk_txt, const mbx_cview* wq_img,

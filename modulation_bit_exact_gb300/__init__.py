@@ -24,7 +24,8 @@ import torch
 
 __all__ = [
     "ln_modulate", "rmsnorm_scale", "rmsnorm_tanh_residual", "residual_gate_add",
-    "qk_norm_rope_qkv_epilogue", "check_ln_modulate", "check_rmsnorm_scale",
+    "qk_norm_rope_qkv_epilogue", "gated_residual_ln_modulate", "check_gated_residual_ln_modulate",
+    "check_ln_modulate", "check_rmsnorm_scale",
     "check_rmsnorm_tanh_residual", "check_residual_gate_add",
     "check_qk_norm_rope_qkv_epilogue", "selftest", "status_string", "MbxError",
     "LOSSLESS", "HIGH", "library_path",
@@ -83,6 +84,8 @@ def _load() -> ctypes.CDLL:
             "mbx_rmsnorm_scale": [_P, _P, _P, _P, _f32, _int, _vp],
             "mbx_rmsnorm_tanh_residual": [_P, _P, _P, _P, _P, _f32, _int, _vp],
             "mbx_residual_gate_add": [_P, _P, _P, _P, _int, _vp],
+            "mbx_gated_residual_ln_modulate": [_P, _P, _P, _P, _P, _P, _P, _P, _f32, _int, _vp],
+            "mbx_check_gated_residual_ln_modulate": [_P, _P, _P, _P, _P, _P, _P, _P, _f32, _int],
             "mbx_qk_norm_rope_qkv_epilogue": [_P, _P, _P, _i64, _i64, _P, _P, _P, _P,
                                               _vp, _vp, _vp, _vp, _f32, _int, _vp],
             "mbx_check_ln_modulate": [_P, _P, _P, _P, _f32, _int],
@@ -228,6 +231,33 @@ def residual_gate_add(x, gate, y, variant="lossless", out=None):
     _raise(L.mbx_residual_gate_add(_ref(o), _ref(xv), _ref(g), _ref(yv), _variant(variant),
                                    _stream(x)))
     return out
+
+
+def gated_residual_ln_modulate(residual, gate, update, scale, shift, bias=None, eps: float = 1e-6,
+                               variant="lossless", out=None, residual_out=None):
+    """Gated residual update fused into LN + AdaLN modulate (see
+    mbx_gated_residual_ln_modulate).  Returns (residual_out, out);
+    ``residual_out=residual`` updates the residual stream in place."""
+    L = _load()
+    out = _empty_like_rows(residual) if out is None else out
+    residual_out = _empty_like_rows(residual) if residual_out is None else residual_out
+    ro, o, r, g, u = _view(residual_out), _view(out), _view(residual), _view(gate), _view(update)
+    sc, sh = _view(scale), _view(shift)
+    b = None if bias is None else _view(bias)
+    _raise(L.mbx_gated_residual_ln_modulate(_ref(ro), _ref(o), _ref(r), _ref(g), _ref(u),
+                                            None if b is None else _ref(b), _ref(sc), _ref(sh), eps,
+                                            _variant(variant), _stream(residual)))
+    return residual_out, out
+
+
+def check_gated_residual_ln_modulate(residual_out, out, residual, gate, update, scale, shift,
+                                     bias=None, eps=1e-6, variant="lossless") -> int:
+    ro, o, r, g, u = _view(residual_out), _view(out), _view(residual), _view(gate), _view(update)
+    sc, sh = _view(scale), _view(shift)
+    b = None if bias is None else _view(bias)
+    return _load().mbx_check_gated_residual_ln_modulate(
+        _ref(ro), _ref(o), _ref(r), _ref(g), _ref(u), None if b is None else _ref(b), _ref(sc),
+        _ref(sh), eps, _variant(variant))
 
 
 def _ptr(t):

@@ -20,6 +20,15 @@ struct LnModParams {
     int D;
     int64_t seq;  // rows / mod_rows: row r uses modulation row r / seq
     float eps;
+    // gated residual front pass (fused entry point only; x is the residual):
+    // r' = bf16(x + bf16(gate * a)), a = update or bf16(update + bias)
+    const uint16_t* update = nullptr;
+    int64_t update_stride = 0;
+    const uint16_t* gate = nullptr;
+    int64_t gate_stride = 0;
+    const uint16_t* bias = nullptr;  // [D] or null
+    uint16_t* res_out = nullptr;
+    int64_t res_out_stride = 0;
 };
 
 struct RmsScaleParams {
@@ -64,6 +73,7 @@ struct GateAddParams {
     int64_t rows;
     int D;
     int64_t seq;
+    const uint16_t* bias = nullptr;  // internal: y is replaced by bf16(y + bias) when set
 };
 
 // Exact unsigned division by a runtime constant for numerators below 2^31
@@ -122,6 +132,7 @@ cudaError_t launch_ln_modulate(const LnModParams& p, bool vec, bool high, cudaSt
 cudaError_t launch_rmsnorm_scale(const RmsScaleParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_rmsnorm_tanh_residual(const RmsTanhParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_residual_gate_add(const GateAddParams& p, bool vec, bool high, cudaStream_t s);
+cudaError_t launch_gated_residual_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_qkv_epilogue(const QkvParams& p, bool high, cudaStream_t s);
 cudaError_t launch_selftest(int which, unsigned long long* counts, cudaStream_t s);
 

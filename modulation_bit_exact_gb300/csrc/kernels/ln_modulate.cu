@@ -342,10 +342,28 @@ __device__ __forceinline__ void welford_stage(const RingT& ring, int s, int t, i
 //               memory once.
 enum { kModRing = 0, kModStaged = 1 };
 
-template <int TPR, int J, int NS, bool HIGH, int MODE>
+// Ring operands of the pipelined kernel: x (the residual when FUSED), then
+// the update (FUSED), then, in ring mode, scale, shift and the gate (FUSED).
+template <bool FUSED, int MODE>
+struct LnOps {
+    static constexpr int U = FUSED ? 1 : -1;
+    static constexpr int SC = MODE == kModRing ? (FUSED ? 2 : 1) : -1;
+    static constexpr int SH = MODE == kModRing ? SC + 1 : -1;
+    static constexpr int G = MODE == kModRing && FUSED ? SH + 1 : -1;
+    static constexpr int N = 1 + (FUSED ? 1 : 0) + (MODE == kModRing ? (FUSED ? 3 : 2) : 0);
+    static constexpr int SLOT = FUSED ? 3 : 2;  // staged arrays per sample: t, shift[, gate]
+};
+
+__device__ __forceinline__ void sts16(uint4* p, uint4 v) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+template <int TPR, int J, int NS, bool HIGH, int MODE, bool FUSED>
 __global__ void __launch_bounds__(512) ln_modulate_pipe_kernel(LnModParams p, int64_t rows_per_cta) {
     using C = RowCfg<TPR, J, true>;
-    constexpr int NOPS = MODE == kModRing ? 3 : 1;
+    using O = LnOps<FUSED, MODE>;
+    constexpr int NOPS = O::N;
     using R = Ring<C, NS, NOPS>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int groups = blockDim.x / TPR;
@@ -353,9 +371,11 @@ __global__ void __launch_bounds__(512) ln_modulate_pipe_kernel(LnModParams p, in
     const int D = p.D;
     const int nch = D / kChunk;
     TreeSmem& sm = reinterpret_cast<TreeSmem*>(smem_raw)[g];
-    uint4* mod = reinterpret_cast<uint4*>(smem_raw + groups * sizeof(TreeSmem));  // [2 slots][t|shift][nch]
-    const int mod_chunks = MODE == kModStaged ? 2 * 2 * nch : 0;
-    const R ring{mod + mod_chunks + (size_t)g * (R::kBytes / 16)};
+    uint4* mod = reinterpret_cast<uint4*>(smem_raw + groups * sizeof(TreeSmem));  // [2 slots][t|shift[|gate]][nch]
+    const int mod_chunks = MODE == kModStaged ? 2 * O::SLOT * nch : 0;
+    uint4* bias_sm = mod + mod_chunks;  // [nch] when FUSED with a bias
+    const int bias_chunks = FUSED && p.bias != nullptr ? nch : 0;
+    const R ring{bias_sm + bias_chunks + (size_t)g * (R::kBytes / 16)};
     const int bar_id = 1 + g;
     const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
     const int64_t r1 = r0 + rows_per_cta < p.rows ? r0 + rows_per_cta : p.rows;
@@ -363,10 +383,12 @@ __global__ void __launch_bounds__(512) ln_modulate_pipe_kernel(LnModParams p, in
 
     auto issue = [&](int s, int64_t row) {
         ring.issue(s, 0, p.x + row * p.x_stride, t, nch);
+        if constexpr (FUSED) ring.issue(s, O::U, p.update + row * p.update_stride, t, nch);
         if constexpr (MODE == kModRing) {
             const int64_t mrow = row / p.seq;
-            ring.issue(s, 1, p.scale + mrow * p.scale_stride, t, nch);
-            ring.issue(s, 2, p.shift + mrow * p.shift_stride, t, nch);
+            ring.issue(s, O::SC, p.scale + mrow * p.scale_stride, t, nch);
+            ring.issue(s, O::SH, p.shift + mrow * p.shift_stride, t, nch);
+            if constexpr (FUSED) ring.issue(s, O::G, p.gate + mrow * p.gate_stride, t, nch);
         }
     };
     const int64_t first = r0 + g;
@@ -393,11 +415,17 @@ __global__ void __launch_bounds__(512) ln_modulate_pipe_kernel(LnModParams p, in
             } else {
                 tv = sc;
             }
-            mod[(slot * 2 + 0) * nch + c] = tv;
-            mod[(slot * 2 + 1) * nch + c] = sh;
+            mod[(slot * O::SLOT + 0) * nch + c] = tv;
+            mod[(slot * O::SLOT + 1) * nch + c] = sh;
+            if constexpr (FUSED)
+                mod[(slot * O::SLOT + 2) * nch + c] = ld_shared_row(p.gate + (m0 + slot) * p.gate_stride + (int64_t)c * kChunk);
         }
-        __syncthreads();
     }
+    if constexpr (FUSED) {
+        for (int c = threadIdx.x; c < bias_chunks; c += blockDim.x)
+            bias_sm[c] = ld_shared_row(p.bias + (int64_t)c * kChunk);
+    }
+    if constexpr (MODE == kModStaged || FUSED) __syncthreads();
 
     int cur = 0;
     for (int64_t row = first; row < r1; row += groups) {
@@ -406,6 +434,33 @@ __global__ void __launch_bounds__(512) ln_modulate_pipe_kernel(LnModParams p, in
         if (rn < r1) issue(sn, rn);
         cp_async_commit();
         cp_async_wait<NS - 1>();
+
+        if constexpr (FUSED) {
+            // front pass: the new residual r' = bf16(x + bf16(gate * a)), written
+            // out and back over x in this thread's own ring chunks
+            const uint4* gm = MODE == kModStaged ? mod + ((row / p.seq - m0) * O::SLOT + 2) * nch : nullptr;
+            uint16_t* res_row = p.res_out + row * p.res_out_stride;
+#pragma unroll
+            for (int j = 0; j < C::J; ++j)
+#pragma unroll
+                for (int m = 0; m < C::M; ++m) {
+                    const int c = t + C::TPR * m + kLanes * j;
+                    if (c >= nch) continue;
+                    const uint4 X = lds16(ring.at(cur, 0, c));
+                    uint4 U = lds16(ring.at(cur, O::U, c));
+                    if (bias_chunks) {
+                        const uint4 B = lds16(bias_sm + c);
+                        U = make_uint4(badd(U.x, B.x), badd(U.y, B.y), badd(U.z, B.z), badd(U.w, B.w));
+                    }
+                    uint4 G;
+                    if constexpr (MODE == kModStaged) G = lds16(gm + c);
+                    else G = lds16(ring.at(cur, O::G > 0 ? O::G : 0, c));
+                    const uint4 Y = make_uint4(badd(X.x, bmul(G.x, U.x)), badd(X.y, bmul(G.y, U.y)),
+                                               badd(X.z, bmul(G.z, U.z)), badd(X.w, bmul(G.w, U.w)));
+                    st_v4(res_row + (int64_t)c * kChunk, Y);
+                    sts16(ring.at(cur, 0, c), Y);
+                }
+        }
 
         float mean = 0.0f, rstd = 0.0f;
         if constexpr (!HIGH) {
@@ -456,7 +511,7 @@ __global__ void __launch_bounds__(512) ln_modulate_pipe_kernel(LnModParams p, in
         }
         group_bcast<C>(mean, rstd, t, sm, bar_id);
 
-        const uint4* tm = MODE == kModStaged ? mod + ((row / p.seq - m0) * 2 + 0) * nch : nullptr;
+        const uint4* tm = MODE == kModStaged ? mod + ((row / p.seq - m0) * O::SLOT + 0) * nch : nullptr;
         const uint4* sh = MODE == kModStaged ? tm + nch : nullptr;
         uint16_t* out_row = p.out + row * p.out_stride;
         const u64 mean2 = f2(mean, mean), rstd2 = f2(rstd, rstd);
@@ -472,8 +527,8 @@ __global__ void __launch_bounds__(512) ln_modulate_pipe_kernel(LnModParams p, in
                     T = lds16(tm + c);
                     SH = lds16(sh + c);
                 } else {
-                    T = lds16(ring.at(cur, 1, c));
-                    SH = lds16(ring.at(cur, 2, c));
+                    T = lds16(ring.at(cur, O::SC > 0 ? O::SC : 0, c));
+                    SH = lds16(ring.at(cur, O::SH > 0 ? O::SH : 0, c));
                 }
                 uint4 o;
 #pragma unroll
@@ -514,12 +569,14 @@ static cudaError_t launch_j(const LnModParams& p, bool, bool high, cudaStream_t 
     return high ? launch_one<TPR, J, false, true>(p, s) : launch_one<TPR, J, false, false>(p, s);
 }
 
-template <int TPR, int J, int NS, bool HIGH, int MODE>
+template <int TPR, int J, int NS, bool HIGH, int MODE, bool FUSED>
 static cudaError_t launch_pipe(const LnModParams& p, cudaStream_t s) {
-    auto k = ln_modulate_pipe_kernel<TPR, J, NS, HIGH, MODE>;
+    auto k = ln_modulate_pipe_kernel<TPR, J, NS, HIGH, MODE, FUSED>;
     using C = RowCfg<TPR, J, true>;
-    using R = Ring<C, NS, MODE == kModRing ? 3 : 1>;
-    const int fixed = MODE == kModStaged ? 2 * 2 * (p.D / kChunk) * 16 : 0;
+    using O = LnOps<FUSED, MODE>;
+    using R = Ring<C, NS, O::N>;
+    const int nch = p.D / kChunk;
+    const int fixed = (MODE == kModStaged ? 2 * O::SLOT * nch * 16 : 0) + (FUSED && p.bias ? nch * 16 : 0);
     PipeShape sh;
     if (!pipe_shape(reinterpret_cast<const void*>(k), TPR, (int)sizeof(TreeSmem) + R::kBytes, fixed, p.rows, &sh))
         return cudaErrorInvalidConfiguration;
@@ -527,32 +584,63 @@ static cudaError_t launch_pipe(const LnModParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int TPR, int J, int NS>
+template <int TPR, int J, int NS, bool FUSED>
 static cudaError_t launch_pipe_v(const LnModParams& p, bool high, cudaStream_t s) {
     // stage the modulation when each CTA's block of rows spans at most two
     // samples (rows per CTA <= seq); otherwise carry it in the ring
     const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
-    if (high) return staged ? launch_pipe<TPR, J, NS, true, kModStaged>(p, s) : launch_pipe<TPR, J, NS, true, kModRing>(p, s);
-    return staged ? launch_pipe<TPR, J, NS, false, kModStaged>(p, s) : launch_pipe<TPR, J, NS, false, kModRing>(p, s);
+    if (high)
+        return staged ? launch_pipe<TPR, J, NS, true, kModStaged, FUSED>(p, s)
+                      : launch_pipe<TPR, J, NS, true, kModRing, FUSED>(p, s);
+    return staged ? launch_pipe<TPR, J, NS, false, kModStaged, FUSED>(p, s)
+                  : launch_pipe<TPR, J, NS, false, kModRing, FUSED>(p, s);
+}
+
+template <bool FUSED>
+static cudaError_t launch_pipe_d(const LnModParams& p, bool high, cudaStream_t s) {
+    // one warp per row up to 2048 elements, two up to 4096 (measured fastest
+    // at 3072: fewer, longer row rounds), four above
+    switch (chunks_per_lane(p.D)) {
+        case 1: return launch_pipe_v<32, 1, 2, FUSED>(p, high, s);
+        case 2: return launch_pipe_v<32, 2, 2, FUSED>(p, high, s);
+        case 3: return launch_pipe_v<64, 3, 2, FUSED>(p, high, s);
+        case 4: return launch_pipe_v<64, 4, 2, FUSED>(p, high, s);
+        case 5: return launch_pipe_v<128, 5, 2, FUSED>(p, high, s);
+        case 6: return launch_pipe_v<128, 6, 2, FUSED>(p, high, s);
+        case 7: return launch_pipe_v<128, 7, 2, FUSED>(p, high, s);
+        case 8: return launch_pipe_v<128, 8, 2, FUSED>(p, high, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_gated_residual_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
+    if (vec) return launch_pipe_d<true>(p, high, s);
+    // unaligned or ragged rows: the same definition as two steps, the gated
+    // residual into res_out, then LayerNorm + modulate of res_out
+    GateAddParams g;
+    g.out = p.res_out;
+    g.out_stride = p.res_out_stride;
+    g.x = p.x;
+    g.x_stride = p.x_stride;
+    g.gate = p.gate;
+    g.gate_stride = p.gate_stride;
+    g.y = p.update;
+    g.y_stride = p.update_stride;
+    g.rows = p.rows;
+    g.D = p.D;
+    g.seq = p.seq;
+    g.bias = p.bias;
+    cudaError_t e = launch_residual_gate_add(g, false, false, s);
+    if (e != cudaSuccess) return e;
+    LnModParams q = p;
+    q.x = p.res_out;
+    q.x_stride = p.res_out_stride;
+    return launch_ln_modulate(q, false, high, s);
 }
 
 cudaError_t launch_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
     const int J = chunks_per_lane(p.D);
-    if (vec) {
-        // pipelined path: one warp per row up to 2048 elements, two up to
-        // 4096 (measured fastest at 3072: fewer, longer row rounds), four above
-        switch (J) {
-            case 1: return launch_pipe_v<32, 1, 2>(p, high, s);
-            case 2: return launch_pipe_v<32, 2, 2>(p, high, s);
-            case 3: return launch_pipe_v<64, 3, 2>(p, high, s);
-            case 4: return launch_pipe_v<64, 4, 2>(p, high, s);
-            case 5: return launch_pipe_v<128, 5, 2>(p, high, s);
-            case 6: return launch_pipe_v<128, 6, 2>(p, high, s);
-            case 7: return launch_pipe_v<128, 7, 2>(p, high, s);
-            case 8: return launch_pipe_v<128, 8, 2>(p, high, s);
-            default: return cudaErrorInvalidValue;
-        }
-    }
+    if (vec) return launch_pipe_d<false>(p, high, s);
     switch (J) {
         // threads per row: enough that a thread holds at most ~5 chunks of x
         case 1: return launch_j<32, 1>(p, vec, high, s);

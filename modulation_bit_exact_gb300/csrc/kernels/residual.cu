@@ -32,6 +32,13 @@ __global__ void __launch_bounds__(kBlock) residual_gate_add_kernel(GateAddParams
                 xv[j] = load_chunk<VEC>(x_row, c, D, true);
                 yv[j] = load_chunk<VEC>(y_row, c, D, true);
                 gv[j] = load_chunk<VEC>(g_row, c, D, per_token);
+                if (p.bias) {  // internal use: the fused entry point's fallback
+                    const uint4 b = load_chunk<VEC>(p.bias, c, D, false);
+                    yv[j].x = badd(yv[j].x, b.x);
+                    yv[j].y = badd(yv[j].y, b.y);
+                    yv[j].z = badd(yv[j].z, b.z);
+                    yv[j].w = badd(yv[j].w, b.w);
+                }
             }
         }
 #pragma unroll

@@ -240,6 +240,44 @@ int check_residual_gate_add(const mbx_view* out, const mbx_cview* x, const mbx_c
     return MBX_OK;
 }
 
+int check_gated(const mbx_view* res_out, const mbx_view* out, const mbx_cview* residual,
+                const mbx_cview* gate, const mbx_cview* update, const mbx_cview* bias,
+                const mbx_cview* scale, const mbx_cview* shift, float eps, int variant, bool dev) {
+    if (!res_out || !out || !residual || !gate || !update || !scale || !shift) return MBX_E_NULL;
+    V ro = of(res_out), o = of(out), r = of(residual), g = of(gate), u = of(update), sc = of(scale),
+      sh = of(shift);
+    const bool has_b = bias != nullptr;
+    V b = has_b ? of(bias) : V{nullptr, 0, 0, 0, MBX_BF16};
+    if (!ro.data || !o.data || !r.data || !g.data || !u.data || !sc.data || !sh.data) return MBX_E_NULL;
+    if (has_b && !b.data) return MBX_E_NULL;
+    for (const V* v : {&ro, &o, &r, &g, &u, &sc, &sh})
+        if (v->dtype != MBX_BF16) return MBX_E_DTYPE;
+    if (has_b && b.dtype != MBX_BF16) return MBX_E_DTYPE;
+    for (const V* v : {&ro, &o, &r, &g, &u, &sc, &sh}) MBX_TRY(basic(*v));
+    if (has_b) MBX_TRY(basic(b));
+    if (r.cols > kMaxHidden) return MBX_E_DIM_TOO_LARGE;
+    for (const V* v : {&ro, &o, &u})
+        if (v->rows != r.rows || v->cols != r.cols) return MBX_E_SHAPE;
+    MBX_TRY(check_mod(g, r));
+    MBX_TRY(check_mod(sc, r));
+    MBX_TRY(check_mod(sh, r));
+    if (g.rows != sc.rows || sc.rows != sh.rows) return MBX_E_SHAPE;
+    if (has_b) MBX_TRY(check_weight(b, r));
+    MBX_TRY(check_variant_eps(variant, eps));
+    for (const V* v : {&r, &g, &u, &sc, &sh, &ro})
+        if (overlaps(o, *v)) return MBX_E_ALIAS;
+    if (has_b && overlaps(o, b)) return MBX_E_ALIAS;
+    for (const V* v : {&g, &u, &sc, &sh})
+        if (overlaps(ro, *v)) return MBX_E_ALIAS;
+    if (has_b && overlaps(ro, b)) return MBX_E_ALIAS;
+    if (overlaps(ro, r) && !same_view(ro, r)) return MBX_E_ALIAS;  // in place on the residual only
+    if (dev) {
+        V all[8] = {ro, o, r, g, u, sc, sh, b};
+        MBX_TRY(views_on_device(all, has_b ? 8 : 7));
+    }
+    return MBX_OK;
+}
+
 int check_qkv(const mbx_view* joint, const mbx_cview* txt, const mbx_cview* img, int64_t batch,
               int64_t heads, const mbx_cview* wq_txt, const mbx_cview* wk_txt,
               const mbx_cview* wq_img, const mbx_cview* wk_img, const float* cos_txt,
@@ -520,6 +558,46 @@ MBX_API int mbx_residual_gate_add(const mbx_view* out, const mbx_cview* x, const
                      aligned16(of(y));
     return cuda_status(
         mbx::launch_residual_gate_add(p, vec, variant == MBX_HIGH, (cudaStream_t)stream));
+}
+
+MBX_API int mbx_check_gated_residual_ln_modulate(const mbx_view* residual_out,
+                                                 const mbx_view* out, const mbx_cview* residual,
+                                                 const mbx_cview* gate, const mbx_cview* update,
+                                                 const mbx_cview* bias, const mbx_cview* scale,
+                                                 const mbx_cview* shift, float eps, int variant) {
+    return check_gated(residual_out, out, residual, gate, update, bias, scale, shift, eps, variant, true);
+}
+
+MBX_API int mbx_gated_residual_ln_modulate(const mbx_view* residual_out, const mbx_view* out,
+                                           const mbx_cview* residual, const mbx_cview* gate,
+                                           const mbx_cview* update, const mbx_cview* bias,
+                                           const mbx_cview* scale, const mbx_cview* shift,
+                                           float eps, int variant, void* stream) {
+    MBX_TRY(check_gated(residual_out, out, residual, gate, update, bias, scale, shift, eps, variant, true));
+    mbx::LnModParams p;
+    p.out = static_cast<uint16_t*>(out->data);
+    p.out_stride = out->row_stride;
+    p.x = static_cast<const uint16_t*>(residual->data);
+    p.x_stride = residual->row_stride;
+    p.scale = static_cast<const uint16_t*>(scale->data);
+    p.scale_stride = scale->row_stride;
+    p.shift = static_cast<const uint16_t*>(shift->data);
+    p.shift_stride = shift->row_stride;
+    p.rows = residual->rows;
+    p.D = (int)residual->cols;
+    p.seq = residual->rows / scale->rows;
+    p.eps = eps;
+    p.update = static_cast<const uint16_t*>(update->data);
+    p.update_stride = update->row_stride;
+    p.gate = static_cast<const uint16_t*>(gate->data);
+    p.gate_stride = gate->row_stride;
+    p.bias = bias ? static_cast<const uint16_t*>(bias->data) : nullptr;
+    p.res_out = static_cast<uint16_t*>(residual_out->data);
+    p.res_out_stride = residual_out->row_stride;
+    bool vec = p.D % 8 == 0 && aligned16(of(residual_out)) && aligned16(of(out)) && aligned16(of(residual)) &&
+               aligned16(of(gate)) && aligned16(of(update)) && aligned16(of(scale)) && aligned16(of(shift));
+    if (bias) vec = vec && aligned16(of(bias));
+    return cuda_status(mbx::launch_gated_residual_ln_modulate(p, vec, variant == MBX_HIGH, (cudaStream_t)stream));
 }
 
 MBX_API int mbx_check_qk_norm_rope_qkv_epilogue(

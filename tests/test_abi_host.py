@@ -33,7 +33,8 @@ def declared_symbols():
 def test_header_declares_the_boundary():
     names = declared_symbols()
     for op in ("mbx_ln_modulate", "mbx_rmsnorm_scale", "mbx_rmsnorm_tanh_residual",
-               "mbx_residual_gate_add", "mbx_qk_norm_rope_qkv_epilogue"):
+               "mbx_residual_gate_add", "mbx_qk_norm_rope_qkv_epilogue",
+               "mbx_gated_residual_ln_modulate"):
         assert op in names and op.replace("mbx_", "mbx_check_") in names
 
 
@@ -237,3 +238,31 @@ def test_binding_names_match_the_header(mbx):
             continue
         py = name[len("mbx_"):]
         assert hasattr(mbx, py), py
+
+
+def test_gated_residual_ln_modulate_rejections(mbx):
+    L = mbx.lib()
+    rows, D = 8, 64
+    ro, o, r, u = (V(BASE + i * 0x100000, rows, D) for i in range(4))
+    g, sc, sh = (V(BASE + (4 + i) * 0x100000, 2, D) for i in range(3))
+    b = V(BASE + 0x800000, 1, D)
+
+    def st(ro, o, r, g, u, b, sc, sh, eps=1e-6, variant=0):
+        args = [ref(ro), ref(o), ref(r), ref(g), ref(u), None if b is None else ref(b), ref(sc), ref(sh),
+                ctypes.c_float(eps), variant]
+        a = L.mbx_check_gated_residual_ln_modulate(*args)
+        assert a == L.mbx_gated_residual_ln_modulate(*args, None)
+        return a
+
+    assert st(ro, o, r, g, u, b, sc, sh) == -9                        # host checks pass
+    assert st(ro, o, r, g, u, None, sc, sh) == -9                     # bias is optional
+    assert st(V(BASE + 0x200000, rows, D), o, r, g, u, b, sc, sh) == -9  # in place on the residual
+    assert st(V(BASE + 0x200002, rows, D), o, r, g, u, b, sc, sh) == -8  # shifted: partial overlap
+    assert st(ro, V(BASE + 0x200000, rows, D), r, g, u, b, sc, sh) == -8  # out over the residual
+    assert st(ro, o, r, g, V(BASE, rows, D), b, sc, sh) == -8          # residual_out over the update
+    assert st(ro, o, r, V(BASE + 0x400000, 4, D), u, b, sc, sh) == -5  # gate rows differ
+    assert st(ro, o, r, g, u, V(BASE + 0x800000, 2, D), sc, sh) == -5  # bias must be [1, D]
+    assert st(ro, o, r, g, V(BASE + 0x300000, rows, 32), b, sc, sh) == -5
+    assert st(ro, o, r, g, u, V(BASE + 0x800000, 1, D, dtype=0), sc, sh) == -2
+    assert st(ro, o, r, g, u, b, sc, sh, variant=3) == -11
+    assert st(ro, o, r, g, u, V(0, 1, D), sc, sh) == -1
