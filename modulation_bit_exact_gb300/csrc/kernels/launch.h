@@ -29,6 +29,9 @@ struct LnModParams {
     const uint16_t* bias = nullptr;  // [D] or null
     uint16_t* res_out = nullptr;
     int64_t res_out_stride = 0;
+    // -0.0f as a kernel argument: the packed Welford update takes its product
+    // as fma(d, t, neg_zero), which the compiler cannot turn into a multiply
+    float neg_zero = -0.0f;
 };
 
 struct RmsScaleParams {

@@ -26,7 +26,7 @@ __device__ __forceinline__ u64 sel2(bool a, bool b, u64 n, u64 o) {
 // any d; otherwise the fast division, for lanes that pass lanes_plain).
 template <class C, bool GUARD>
 __device__ __forceinline__ void welford_lanes(const uint4 (&v)[C::M][C::J], int t, int D,
-                                              Wf (&L)[C::M]) {
+                                              Wf (&L)[C::M], u64 nz) {
     // elements left in the last chunk of each lane (<= 0: no last chunk)
     int lim[C::M];
 #pragma unroll
@@ -46,10 +46,10 @@ __device__ __forceinline__ void welford_lanes(const uint4 (&v)[C::M][C::J], int 
                 for (int p = 0; p < P; ++p) {
                     u64 x = pair_elem(w_of(v[p][j], e / 2), w_of(v[p + P][j], e / 2), e & 1);
                     if constexpr (j < C::J - 1) {
-                        welford_step2<K, GUARD>(x, mean[p], m2[p]);
+                        welford_step2<K, GUARD>(x, mean[p], m2[p], nz);
                     } else {
                         u64 mn = mean[p], q = m2[p];
-                        welford_step2<K, GUARD>(x, mn, q);
+                        welford_step2<K, GUARD>(x, mn, q, nz);
                         bool va = e < lim[p], vb = e < lim[p + P];
                         mean[p] = sel2(va, vb, mn, mean[p]);
                         m2[p] = sel2(va, vb, q, m2[p]);
@@ -112,8 +112,9 @@ __global__ void __launch_bounds__(kBlock) ln_modulate_kernel(LnModParams p) {
         float mean, rstd;
         if constexpr (!HIGH) {
             Wf L[C::M];
-            if (lanes_plain<C>(v, rl.t, nch)) welford_lanes<C, false>(v, rl.t, D, L);
-            else welford_lanes<C, true>(v, rl.t, D, L);
+            const u64 nz = f2(p.neg_zero, p.neg_zero);
+            if (lanes_plain<C>(v, rl.t, nch)) welford_lanes<C, false>(v, rl.t, D, L, nz);
+            else welford_lanes<C, true>(v, rl.t, D, L, nz);
             Wf s = tree_reduce<C>(L, rl.t, sm, rl.bar_id, wf_combine);
             mean = s.mean;
             if (rl.t == 0) {
@@ -244,7 +245,7 @@ __device__ __noinline__ WPair welford_chunk_exact(uint4 a, uint4 b, int k0, int 
 // all J chunks) removes the per-step selects of the last chunk.
 template <class C, class RingT>
 __device__ __forceinline__ void welford_stage(const RingT& ring, int s, int t, int nch, bool full,
-                                              Wf (&L)[C::M]) {
+                                              Wf (&L)[C::M], u64 nz) {
     if constexpr (C::M >= 2) {
         constexpr int P = C::M / 2;
         u64 mean[P], m2[P];
@@ -270,7 +271,7 @@ __device__ __forceinline__ void welford_stage(const RingT& ring, int s, int t, i
                     constexpr int K = kChunk * j + e + 1;
 #pragma unroll
                     for (int p = 0; p < P; ++p)
-                        welford_step2<K, false>(pair_elem(w_of(A[p], e / 2), w_of(B[p], e / 2), e & 1), mean[p], m2[p]);
+                        welford_step2<K, false>(pair_elem(w_of(A[p], e / 2), w_of(B[p], e / 2), e & 1), mean[p], m2[p], nz);
                 });
             } else if (plain) {  // last chunk, some lanes without it
                 static_for<0, kChunk>([&](auto ec) {
@@ -279,7 +280,7 @@ __device__ __forceinline__ void welford_stage(const RingT& ring, int s, int t, i
 #pragma unroll
                     for (int p = 0; p < P; ++p) {
                         u64 mn = mean[p], q = m2[p];
-                        welford_step2<K, false>(pair_elem(w_of(A[p], e / 2), w_of(B[p], e / 2), e & 1), mn, q);
+                        welford_step2<K, false>(pair_elem(w_of(A[p], e / 2), w_of(B[p], e / 2), e & 1), mn, q, nz);
                         mean[p] = sel2(va[p], vb[p], mn, mean[p]);
                         m2[p] = sel2(va[p], vb[p], q, m2[p]);
                     }
@@ -360,7 +361,7 @@ __device__ __forceinline__ void sts16(uint4* p, uint4 v) {
 }
 
 template <int TPR, int J, int NS, bool HIGH, int MODE, bool FUSED>
-__global__ void __launch_bounds__(512) ln_modulate_pipe_kernel(LnModParams p, int64_t rows_per_cta) {
+__global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p, int64_t rows_per_cta) {
     using C = RowCfg<TPR, J, true>;
     using O = LnOps<FUSED, MODE>;
     constexpr int NOPS = O::N;
@@ -380,22 +381,25 @@ __global__ void __launch_bounds__(512) ln_modulate_pipe_kernel(LnModParams p, in
     const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
     const int64_t r1 = r0 + rows_per_cta < p.rows ? r0 + rows_per_cta : p.rows;
     const int64_t m0 = r0 / p.seq;
+    const int64_t split = (m0 + 1) * p.seq;  // staged: rows from here use slot 1
+    const int64_t first = r0 + g;
+    RowDiv next(first, groups, p.seq);  // modulation row of the next row to issue
 
     auto issue = [&](int s, int64_t row) {
         ring.issue(s, 0, p.x + row * p.x_stride, t, nch);
         if constexpr (FUSED) ring.issue(s, O::U, p.update + row * p.update_stride, t, nch);
         if constexpr (MODE == kModRing) {
-            const int64_t mrow = row / p.seq;
+            const int64_t mrow = next.q;
             ring.issue(s, O::SC, p.scale + mrow * p.scale_stride, t, nch);
             ring.issue(s, O::SH, p.shift + mrow * p.shift_stride, t, nch);
             if constexpr (FUSED) ring.issue(s, O::G, p.gate + mrow * p.gate_stride, t, nch);
         }
     };
-    const int64_t first = r0 + g;
 #pragma unroll
     for (int s = 0; s < NS - 1; ++s) {
         const int64_t r = first + s * groups;
         if (r < r1) issue(s, r);
+        if constexpr (MODE == kModRing) next.advance();
         cp_async_commit();
     }
     // the first rows are on their way; stage the modulation meanwhile
@@ -432,13 +436,15 @@ __global__ void __launch_bounds__(512) ln_modulate_pipe_kernel(LnModParams p, in
         const int64_t rn = row + (NS - 1) * groups;
         const int sn = cur == 0 ? NS - 1 : cur - 1;
         if (rn < r1) issue(sn, rn);
+        if constexpr (MODE == kModRing) next.advance();
         cp_async_commit();
         cp_async_wait<NS - 1>();
+        const int slot = row >= split ? 1 : 0;
 
         if constexpr (FUSED) {
             // front pass: the new residual r' = bf16(x + bf16(gate * a)), written
             // out and back over x in this thread's own ring chunks
-            const uint4* gm = MODE == kModStaged ? mod + ((row / p.seq - m0) * O::SLOT + 2) * nch : nullptr;
+            const uint4* gm = MODE == kModStaged ? mod + (slot * O::SLOT + 2) * nch : nullptr;
             uint16_t* res_row = p.res_out + row * p.res_out_stride;
 #pragma unroll
             for (int j = 0; j < C::J; ++j)
@@ -466,7 +472,7 @@ __global__ void __launch_bounds__(512) ln_modulate_pipe_kernel(LnModParams p, in
         if constexpr (!HIGH) {
             Wf L[C::M];
             const bool full = nch == kLanes * C::J;
-            welford_stage<C>(ring, cur, t, nch, full, L);
+            welford_stage<C>(ring, cur, t, nch, full, L, f2(p.neg_zero, p.neg_zero));
             const Wf s = full ? tree_reduce<C>(L, t, sm, bar_id, wf_combine_eq)
                               : tree_reduce<C>(L, t, sm, bar_id, wf_combine);
             mean = s.mean;
@@ -511,7 +517,7 @@ __global__ void __launch_bounds__(512) ln_modulate_pipe_kernel(LnModParams p, in
         }
         group_bcast<C>(mean, rstd, t, sm, bar_id);
 
-        const uint4* tm = MODE == kModStaged ? mod + ((row / p.seq - m0) * O::SLOT + 0) * nch : nullptr;
+        const uint4* tm = MODE == kModStaged ? mod + (slot * O::SLOT + 0) * nch : nullptr;
         const uint4* sh = MODE == kModStaged ? tm + nch : nullptr;
         uint16_t* out_row = p.out + row * p.out_stride;
         const u64 mean2 = f2(mean, mean), rstd2 = f2(rstd, rstd);

@@ -134,8 +134,15 @@ struct Recip {
 
 constexpr float kDivTiny = 0x1p-90f;
 
+// K a power of two: d/K and d*(1/K) are the same correctly rounded value
+// (1/K is exact), for every d including subnormal results; K = 1 is d itself.
+template <int K>
+constexpr bool kPow2 = (K & (K - 1)) == 0;
+
 template <int K>
 __device__ __forceinline__ float div_k_fast(float d) {
+    if constexpr (K == 1) return d;
+    if constexpr (kPow2<K>) return __fmul_rn(d, Recip<K>::yh);
     float q0 = __fmul_rn(d, Recip<K>::yh);
     float r = __fmaf_rn(q0, Recip<K>::negk, d);
     return __fmaf_rn(r, Recip<K>::yh, q0);
@@ -143,12 +150,15 @@ __device__ __forceinline__ float div_k_fast(float d) {
 
 template <int K>
 __device__ __forceinline__ float div_k(float d) {
+    if constexpr (kPow2<K>) return div_k_fast<K>(d);
     if (fabsf(d) < kDivTiny) return __fdiv_rn(d, (float)K);
     return div_k_fast<K>(d);
 }
 
 template <int K>
 __device__ __forceinline__ u64 div_k2_fast(u64 d) {
+    if constexpr (K == 1) return d;
+    if constexpr (kPow2<K>) return mul2(d, f2(Recip<K>::yh, Recip<K>::yh));
     const u64 yh = f2(Recip<K>::yh, Recip<K>::yh);
     const u64 nk = f2(Recip<K>::negk, Recip<K>::negk);
     u64 q0 = mul2(d, yh);
@@ -158,6 +168,7 @@ __device__ __forceinline__ u64 div_k2_fast(u64 d) {
 
 template <int K>
 __device__ __forceinline__ u64 div_k2(u64 d) {
+    if constexpr (kPow2<K>) return div_k2_fast<K>(d);
     const float dl = f2lo(d), dh = f2hi(d);
     if (fminf(fabsf(dl), fabsf(dh)) < kDivTiny) return f2(__fdiv_rn(dl, (float)K), __fdiv_rn(dh, (float)K));
     return div_k2_fast<K>(d);
@@ -179,17 +190,18 @@ __device__ __forceinline__ void static_for(F&& f) {
 //   d = x - mean; mean += d / K; m2 += d * (x - mean)
 // GUARD = false is the fast division, valid for a lane whose nonzero
 // elements all have |x| >= 2^-60 (see lane_is_plain in rowops.cuh).
+// nz holds -0.0f in both halves, passed in at run time (see LnModParams):
+// fma(d, t, -0) is the correctly rounded product d*t for every d and t (adding
+// -0 changes neither a nonzero product nor the sign of a zero one), and as the
+// compiler cannot see the constant it cannot fold the fma back into a multiply
+// and contract that with the add that follows.
 template <int K, bool GUARD>
-__device__ __forceinline__ void welford_step2(u64 x, u64& mean, u64& m2) {
+__device__ __forceinline__ void welford_step2(u64 x, u64& mean, u64& m2, u64 nz) {
     u64 d = sub2(x, mean);
     if constexpr (GUARD) mean = add2(mean, div_k2<K>(d));
     else mean = add2(mean, div_k2_fast<K>(d));
-    // The product feeding the sum uses the scalar __fmul_rn/__fadd_rn, which
-    // are never merged into a fused multiply-add; ptxas does fuse a packed
-    // mul.rn.f32x2 into a following add.rn.f32x2.
     const u64 t = sub2(x, mean);
-    m2 = f2(__fadd_rn(f2lo(m2), __fmul_rn(f2lo(d), f2lo(t))),
-            __fadd_rn(f2hi(m2), __fmul_rn(f2hi(d), f2hi(t))));
+    m2 = add2(m2, fma2(d, t, nz));
 }
 
 template <int K, bool GUARD>

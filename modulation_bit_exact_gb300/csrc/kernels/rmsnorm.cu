@@ -306,7 +306,7 @@ __device__ __forceinline__ void sumsq_stage_f32(const RingT& ring, int s, int t,
 }
 
 template <int TPR, int J, int NS, bool HIGH, int OP, int MODE>
-__global__ void __launch_bounds__(512) rmsnorm_pipe_kernel(typename RmsPipeArgs<OP>::P p, int64_t rows_per_cta) {
+__global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeArgs<OP>::P p, int64_t rows_per_cta) {
     using A = RmsPipeArgs<OP>;
     using C = RowCfg<TPR, J, true>;
     // ring operands: x, [mod when not staged], [residual for the tanh op]
@@ -329,19 +329,22 @@ __global__ void __launch_bounds__(512) rmsnorm_pipe_kernel(typename RmsPipeArgs<
     const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
     const int64_t r1 = r0 + rows_per_cta < p.rows ? r0 + rows_per_cta : p.rows;
     const int64_t m0 = r0 / p.seq;
+    const int64_t split = (m0 + 1) * p.seq;  // staged: rows from here use slot 1
     const uint16_t* modp = A::mod(p);
     const int64_t mod_stride = A::mod_stride(p);
+    const int64_t first = r0 + g;
+    RowDiv next(first, groups, p.seq);  // modulation row of the next row to issue
 
     auto issue = [&](int s, int64_t row) {
         ring.issue(s, 0, p.x + row * p.x_stride, t, nch);
-        if constexpr (OP_MOD >= 0) ring.issue(s, OP_MOD, modp + (row / p.seq) * mod_stride, t, nch);
+        if constexpr (OP_MOD >= 0) ring.issue(s, OP_MOD, modp + next.q * mod_stride, t, nch);
         if constexpr (OP_RES >= 0) ring.issue(s, OP_RES, p.residual + row * p.res_stride, t, nch);
     };
-    const int64_t first = r0 + g;
 #pragma unroll
     for (int s = 0; s < NS - 1; ++s) {
         const int64_t r = first + s * groups;
         if (r < r1) issue(s, r);
+        if constexpr (MODE == kRmsModRing) next.advance();
         cp_async_commit();
     }
     // the first rows are on their way; stage the per-CTA data meanwhile
@@ -370,6 +373,7 @@ __global__ void __launch_bounds__(512) rmsnorm_pipe_kernel(typename RmsPipeArgs<
         const int64_t rn = row + (NS - 1) * groups;
         const int sn = cur == 0 ? NS - 1 : cur - 1;
         if (rn < r1) issue(sn, rn);
+        if constexpr (MODE == kRmsModRing) next.advance();
         cp_async_commit();
         cp_async_wait<NS - 1>();
 
@@ -389,7 +393,7 @@ __global__ void __launch_bounds__(512) rmsnorm_pipe_kernel(typename RmsPipeArgs<
         }
         group_bcast<C>(rstd, unused, t, sm, bar_id);
         const uint32_t r2 = bf16_bits(rstd);
-        const uint4* mrow = MODE == kRmsModStaged ? msm + (row / p.seq - m0) * nch : nullptr;
+        const uint4* mrow = MODE == kRmsModStaged ? msm + (row >= split ? nch : 0) : nullptr;
         uint16_t* out_row = p.out + row * p.out_stride;
 #pragma unroll
         for (int j = 0; j < C::J; ++j)

@@ -180,6 +180,26 @@ struct Ring {
     }
 };
 
+// row / seq along a sequence of rows advancing by a fixed step, without a
+// 64-bit division per row: the quotient and remainder are carried along.
+struct RowDiv {
+    int64_t q, r, seq, dq, dr;
+    __device__ __forceinline__ RowDiv(int64_t row, int64_t step, int64_t seq_) : seq(seq_) {
+        q = row / seq;
+        r = row - q * seq;
+        dq = step / seq;
+        dr = step - dq * seq;
+    }
+    __device__ __forceinline__ void advance() {
+        q += dq;
+        r += dr;
+        if (r >= seq) {
+            r -= seq;
+            ++q;
+        }
+    }
+};
+
 // ------------------------------------------------------------------ tree
 
 __device__ __forceinline__ float sum_combine(float a, float b) { return __fadd_rn(a, b); }
