@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
                 "orc_residual_gate_add": [_p, _i64, _p, _i64, _i64, _i64, _p, _i64, _i64, _p, _i64],
                 "orc_gated_residual_ln_modulate": [_p, _p, _p, _i64, _i64, _i64, _p, _i64, _p, _p,
                                                    _i64, _p, _i64, _p, _i64, _i64, _f32],
+                "orc_modulation_table_add": [_p, _i64, _p, _i64, ctypes.c_int, _p, _i64,
+                                             ctypes.c_int, _i64, _i64],
                 "orc_qkv_epilogue": [_p, _p, _i64, _i64, _p, _i64, _i64, _i64, _i64, _i64,
                                      _p, _p, _p, _p, _p, _p, _p, _p, _f32],
                 "orc_ln_modulate_f64": [_p, _p, _p, _i64, _i64, _i64, _p, _i64, _p, _i64, _i64, _f32],
@@ -96,6 +98,19 @@ def _rows(a: np.ndarray) -> tuple[np.ndarray, int]:
     if a.strides[1] != 2:
         raise ValueError("last dimension must be contiguous")
     return a, a.strides[0] // 2 if a.shape[0] > 1 else a.shape[1]
+
+
+def _mat(a: np.ndarray) -> tuple[np.ndarray, int, int]:
+    """A 2-D bfloat16 (uint16 bits) or binary32 matrix with a contiguous last
+    dim; returns (array, row stride in elements, 1 if binary32)."""
+    if a.dtype not in (np.uint16, np.float32):
+        raise TypeError("expected bfloat16 bit patterns (uint16) or float32")
+    if a.ndim != 2:
+        a = a.reshape(-1, a.shape[-1])
+    if a.strides[1] != a.itemsize:
+        raise ValueError("last dimension must be contiguous")
+    stride = a.strides[0] // a.itemsize if a.shape[0] > 1 else a.shape[1]
+    return a, stride, int(a.dtype == np.float32)
 
 
 def _ptr(a: np.ndarray) -> int:
@@ -229,6 +244,29 @@ def residual_gate_add(x: np.ndarray, gate: np.ndarray, y: np.ndarray) -> np.ndar
         raise ValueError("y must match x")
     out = np.empty((rows, D), dtype=np.uint16)
     lib().orc_residual_gate_add(_ptr(out), D, _ptr(x2), xs, rows, D, _ptr(g2), gs, grows, _ptr(y2), ys)
+    return out
+
+
+def modulation_table_add(table: np.ndarray, temb: np.ndarray) -> np.ndarray:
+    """Per-token modulation table in the (6, rows, D) layout, binary32.
+
+    tahou.com article, section Wan视频模型的数据搬运优化: the eager
+    ``(table.unsqueeze(0) + temb.float()).chunk(6, dim=2)``, each of the six
+    chunks written as a contiguous plane; one binary32 addition per element.
+    table [6, D] and temb [rows, 6*D] (or [..., 6, D]) are bfloat16 bit
+    patterns (uint16) or float32.
+    """
+    t2, ts, tf = _mat(table)
+    if t2.shape[0] != 6:
+        raise ValueError("table must have 6 rows")
+    D = t2.shape[1]
+    e = temb.reshape(-1, 6 * D) if temb.shape[-1] != 6 * D else temb
+    e2, es, ef = _mat(e)
+    if e2.shape[1] != 6 * D:
+        raise ValueError("temb rows must hold 6*D elements")
+    rows = e2.shape[0]
+    out = np.empty((6, rows, D), dtype=np.float32)
+    lib().orc_modulation_table_add(_ptr(out), D, _ptr(t2), ts, tf, _ptr(e2), es, ef, rows, D)
     return out
 
 

@@ -20,6 +20,10 @@
  *   [QKV]     tahou.com article, section 合并QKV投影时的数值问题 (merged QKV
  *             projection): Q/K RMSNorm, interleaved RoPE, V copy, text and image
  *             tokens written into one joint QKV buffer.
+ *   [WAN]     tahou.com article, section Wan视频模型的数据搬运优化 (Wan data
+ *             movement): the per-token modulation table
+ *             (table.unsqueeze(0) + temb.float()).chunk(6, dim=2), written as six
+ *             contiguous planes with the same binary32 additions.
  *
  * Readings taken where the pages are silent (each is a definition this oracle
  * owns; the CUDA path must reproduce it bit for bit):
@@ -327,6 +331,34 @@ void orc_gated_residual_ln_modulate(uint16_t* res_out, uint16_t* out, const uint
         }
     }
     orc_ln_modulate(out, D, res_out, D, rows, D, scale, scale_stride, shift, shift_stride, mod_rows, eps);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Per-token modulation table [WAN]                                         */
+/* ------------------------------------------------------------------------ */
+
+/* Element (r, e) of a bfloat16 (is_f32 == 0) or binary32 row-major matrix,
+ * widened exactly to binary32. */
+static float elem_f32(const void* base, int is_f32, int64_t stride, int64_t r, int64_t e) {
+    if (is_f32) return ((const float*)base)[r * stride + e];
+    return f_of(((const uint16_t*)base)[r * stride + e]);
+}
+
+/* out[k*rows + r][d] = float(table[k][d]) + float(temb[r][k*D + d]) for the six
+ * chunks k = 0..5 of the eager (table.unsqueeze(0) + temb.float()).chunk(6, 2):
+ * table [6, D], temb [rows, 6*D] (B*S token rows), out binary32 [6*rows, D]
+ * (plane k is rows k*rows .. k*rows + rows - 1).  One binary32 addition per
+ * element, in the eager order (table first). */
+void orc_modulation_table_add(float* out, int64_t out_stride, const void* table,
+                              int64_t table_stride, int table_f32, const void* temb,
+                              int64_t temb_stride, int temb_f32, int64_t rows, int64_t D) {
+    for (int k = 0; k < 6; ++k)
+        for (int64_t r = 0; r < rows; ++r)
+            for (int64_t d = 0; d < D; ++d) {
+                float t = elem_f32(table, table_f32, table_stride, k, d);
+                float e = elem_f32(temb, temb_f32, temb_stride, r, (int64_t)k * D + d);
+                out[((int64_t)k * rows + r) * out_stride + d] = t + e;
+            }
 }
 
 /* ------------------------------------------------------------------------ */

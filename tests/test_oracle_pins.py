@@ -574,3 +574,75 @@ def test_gated_residual_ln_modulate_is_the_composition(orc):
     # the residual stream itself against PyTorch CPU eager bf16 ops
     res, _ = orc.gated_residual_ln_modulate(R, G, U, u16(b), SC, SH, 1e-6)
     assert np.array_equal(res, u16(r + gate.repeat_interleave(16, 0) * (u + b)))
+
+
+# ------------------------------------------------------------ modulation table
+
+
+def _eager_table(table: torch.Tensor, temb: torch.Tensor) -> np.ndarray:
+    """The pages' eager expression, on the CPU, with the model's shapes: the
+    table parameter [1, 6, D], temb [B=1, S, 6, D];
+    (table.unsqueeze(0) + temb.float()).chunk(6, dim=2), stacked into (6, S, D)."""
+    param = table.reshape(1, 6, -1)
+    e = temb.reshape(1, -1, 6, param.shape[-1])
+    chunks = (param.unsqueeze(0) + e.float()).chunk(6, dim=2)
+    return torch.stack([c.reshape(e.shape[1], -1) for c in chunks]).numpy()
+
+
+def f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32)
+
+
+def _bits_or_f32(t: torch.Tensor) -> np.ndarray:
+    return u16(t) if t.dtype == torch.bfloat16 else t.numpy()
+
+
+@pytest.mark.parametrize("tab_dt", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("emb_dt", [torch.bfloat16, torch.float32])
+def test_modulation_table_equals_the_eager_expression(orc, tab_dt, emb_dt):
+    """Bit for bit against PyTorch CPU eager on the pages' own expression,
+    including signed zeros and huge/tiny operands."""
+    g = torch.Generator().manual_seed(71)
+    rows, D = 37, 24
+    table = (torch.randn(6, D, generator=g) / D ** 0.5).to(tab_dt)
+    temb = torch.randn(rows, 6, D, generator=g)
+    temb[0, :, :4] = torch.tensor([0.0, -0.0, 3e38, 1e-40])
+    temb = temb.to(emb_dt)
+    want = _eager_table(table, temb)
+    got = orc.modulation_table_add(_bits_or_f32(table), _bits_or_f32(temb))
+    assert got.shape == (6, rows, D)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_modulation_table_closed_forms(orc):
+    """A zero operand is the identity; bf16 operands whose exponents differ by
+    at most 16 add exactly in binary32, so the result equals the binary64 sum."""
+    g = torch.Generator().manual_seed(72)
+    rows, D = 19, 40
+    table = torch.randn(6, D, generator=g).to(torch.bfloat16)
+    temb = torch.randn(rows, 6 * D, generator=g).to(torch.bfloat16)
+    T, E = u16(table), u16(temb)
+    zero_t = np.zeros_like(T)
+    out = orc.modulation_table_add(zero_t, E)
+    assert np.array_equal(out, f32(E).reshape(rows, 6, D).transpose(1, 0, 2))
+    out = orc.modulation_table_add(T, np.zeros_like(E))
+    assert np.array_equal(out, np.broadcast_to(f32(T)[:, None, :], (6, rows, D)))
+    # exact sums: both operands in [1, 2) as bf16 -> the sum needs at most 9 bits
+    t1 = (1 + torch.rand(6, D, generator=g)).to(torch.bfloat16)
+    e1 = (1 + torch.rand(rows, 6 * D, generator=g)).to(torch.bfloat16)
+    out = orc.modulation_table_add(u16(t1), u16(e1))
+    exact = (f32(u16(t1)).astype(np.float64)[:, None, :]
+             + f32(u16(e1)).astype(np.float64).reshape(rows, 6, D).transpose(1, 0, 2))
+    assert np.array_equal(out.astype(np.float64), exact)
+
+
+def test_modulation_table_layout(orc):
+    """Plane k, row r, column d comes from temb[r, k*D + d] and table[k, d]."""
+    rows, D = 5, 3
+    table = np.arange(6 * D, dtype=np.float32).reshape(6, D) * 1000
+    temb = np.arange(rows * 6 * D, dtype=np.float32).reshape(rows, 6 * D)
+    out = orc.modulation_table_add(table, temb)
+    for k in range(6):
+        for r in range(rows):
+            for d in range(D):
+                assert out[k, r, d] == table[k, d] + temb[r, k * D + d]
