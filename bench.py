@@ -470,6 +470,27 @@ def run_suite(args):
                               "variant": v, "us_per_call": round(us, 2), "bytes": nb, "gbs": round(gbs, 1),
                               "frac_of_peak": round(gbs / peak, 4)}), flush=True)
 
+    def table_case(name, rows, D, tab_dt=torch.float32, emb_dt=torch.bfloat16):
+        def make(i):
+            g = torch.Generator(device=dev).manual_seed(3000 + i)
+            return dict(t=(torch.randn(6, D, generator=g, device=dev) / D ** 0.5).to(tab_dt),
+                        e=torch.randn(rows, 6 * D, generator=g, device=dev).to(emb_dt),
+                        o=torch.empty(6, rows, D, dtype=torch.float32, device=dev))
+        esz = 2 if emb_dt == torch.bfloat16 else 4
+        nb = rows * 6 * D * (esz + 4) + 6 * D * (2 if tab_dt == torch.bfloat16 else 4)
+        us = time_cases(make, nb, lambda st: mbx.modulation_table_add(st["t"], st["e"], out=st["o"]))
+        gbs = nb / (us * 1e-6) / 1e9
+        print(json.dumps({"case": name, "shape": [rows, 6, D], "op": "modulation_table_add",
+                          "variant": "exact", "us_per_call": round(us, 2), "bytes": nb, "gbs": round(gbs, 1),
+                          "frac_of_peak": round(gbs / peak, 4)}), flush=True)
+
+    only = getattr(args, "only", None)
+    if only:
+        if "table" in only:
+            table_case("Wan2.2-TI2V table [1,109120,6,3072] bf16 temb", 31 * 44 * 80, 3072)
+            table_case("video table [1,32760,6,5120] bf16 temb", 32760, 5120)
+            table_case("video table [1,32760,6,5120] f32 temb", 32760, 5120, emb_dt=torch.float32)
+        return 0
     row_case("tiny [2,256,512]", 2, 256, 512, False)
     row_case("image-DiT [2,4352,3072]", 2, 4352, 3072, False)
     qkv_case("QKV epilogue [2,256+64x64,24x128]", 2, 256, 64, 64, 24)
@@ -477,6 +498,8 @@ def run_suite(args):
     for D in (1024, 4096, 8192):
         for T in (4096, 65536):
             row_case(f"sweep [{T},{D}]", 1, T, D, False)
+    table_case("Wan2.2-TI2V table [1,109120,6,3072] bf16 temb", 31 * 44 * 80, 3072)
+    table_case("video table [1,32760,6,5120] bf16 temb", 32760, 5120)
     return 0
 
 
@@ -487,6 +510,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", default="mbx", choices=["mbx", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", default=None, help="with --suite: run only the named group (table)")
     ap.add_argument("--suite", action="store_true",
                     help="time every operation and variant on the configurations' shapes "
                          "(one JSON line per case) instead of the benchmark step")

@@ -59,8 +59,9 @@ extern "C" {
 
 #define MBX_ABI_VERSION 1
 
-/* dtype codes: bfloat16 is the only accepted element type. */
-enum { MBX_BF16 = 1 };
+/* dtype codes.  Every operation takes bfloat16 operands, except that the
+ * modulation-table add also accepts binary32 inputs and writes binary32. */
+enum { MBX_BF16 = 1, MBX_F32 = 2 };
 
 /* variant codes */
 enum { MBX_LOSSLESS = 0, MBX_HIGH = 1 };
@@ -69,7 +70,7 @@ enum { MBX_LOSSLESS = 0, MBX_HIGH = 1 };
 enum {
     MBX_OK = 0,
     MBX_E_NULL = -1,          /* a required pointer is NULL                       */
-    MBX_E_DTYPE = -2,         /* an operand is not bfloat16                       */
+    MBX_E_DTYPE = -2,         /* an operand has a dtype the operation does not take */
     MBX_E_EMPTY = -3,         /* rows or cols is zero (or negative)               */
     MBX_E_DIM_TOO_LARGE = -4, /* cols (hidden size) above 8192                    */
     MBX_E_SHAPE = -5,         /* shapes disagree, or rows % mod_rows != 0         */
@@ -83,7 +84,8 @@ enum {
     MBX_E_CUDA = -13          /* the CUDA runtime reported an error               */
 };
 
-/* Read-only view of a [rows, cols] bfloat16 array (row_stride in elements). */
+/* Read-only view of a [rows, cols] array of `dtype` elements (row_stride in
+ * elements). */
 typedef struct {
     const void* data;
     int64_t rows;
@@ -177,6 +179,23 @@ MBX_API int mbx_gated_residual_ln_modulate(const mbx_view* residual_out, const m
                                            float eps, int variant, void* stream);
 
 /*
+ * Per-token modulation table, written in the (6, rows, D) layout.
+ * Defined in: tahou.com SGLang diffusion article, section
+ * Wan视频模型的数据搬运优化 -- the eager (table.unsqueeze(0) + temb.float())
+ * .chunk(6, dim=2) of a Wan block builds a binary32 [B, S, 6, D] temporary and
+ * hands out six strided views; here the six chunks are written as contiguous
+ * planes with the same binary32 additions:
+ *   out[k*rows + r][d] = float(table[k][d]) + float(temb[r][k*D + d]),  k = 0..5
+ * table [6, D] and temb [rows, 6*D] (rows = B*S tokens) are MBX_BF16 or
+ * MBX_F32 (each widened exactly); out [6*rows, D] is MBX_F32, plane k being
+ * rows k*rows .. k*rows + rows - 1 (a contiguous (6, B, S, D) tensor).
+ * One addition per element: bit-exact to the eager expression on the GPU.
+ * out may not overlap table or temb (MBX_E_ALIAS); 6*D must be below 2^31.
+ */
+MBX_API int mbx_modulation_table_add(const mbx_view* out, const mbx_cview* table,
+                                     const mbx_cview* temb, void* stream);
+
+/*
  * Fused post-GEMM QKV epilogue.
  * Defined in: tahou.com SGLang diffusion article, section 合并QKV投影时的数值问题:
  * after the merged QKV GEMM one kernel does Q/K RMSNorm, interleaved RoPE,
@@ -221,6 +240,8 @@ MBX_API int mbx_check_rmsnorm_tanh_residual(const mbx_view* out, const mbx_cview
                                             const mbx_cview* weight, float eps, int variant);
 MBX_API int mbx_check_residual_gate_add(const mbx_view* out, const mbx_cview* x,
                                         const mbx_cview* gate, const mbx_cview* y, int variant);
+MBX_API int mbx_check_modulation_table_add(const mbx_view* out, const mbx_cview* table,
+                                           const mbx_cview* temb);
 MBX_API int mbx_check_gated_residual_ln_modulate(const mbx_view* residual_out,
                                                  const mbx_view* out, const mbx_cview* residual,
                                                  const mbx_cview* gate, const mbx_cview* update,

@@ -25,6 +25,7 @@ import torch
 __all__ = [
     "ln_modulate", "rmsnorm_scale", "rmsnorm_tanh_residual", "residual_gate_add",
     "qk_norm_rope_qkv_epilogue", "gated_residual_ln_modulate", "check_gated_residual_ln_modulate",
+    "modulation_table_add", "check_modulation_table_add",
     "check_ln_modulate", "check_rmsnorm_scale",
     "check_rmsnorm_tanh_residual", "check_residual_gate_add",
     "check_qk_norm_rope_qkv_epilogue", "selftest", "status_string", "MbxError",
@@ -32,7 +33,7 @@ __all__ = [
 ]
 
 LOSSLESS, HIGH = 0, 1
-MBX_BF16 = 1
+MBX_BF16, MBX_F32 = 1, 2
 _VARIANTS = {"lossless": LOSSLESS, "high": HIGH, LOSSLESS: LOSSLESS, HIGH: HIGH}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -84,6 +85,8 @@ def _load() -> ctypes.CDLL:
             "mbx_rmsnorm_scale": [_P, _P, _P, _P, _f32, _int, _vp],
             "mbx_rmsnorm_tanh_residual": [_P, _P, _P, _P, _P, _f32, _int, _vp],
             "mbx_residual_gate_add": [_P, _P, _P, _P, _int, _vp],
+            "mbx_modulation_table_add": [_P, _P, _P, _vp],
+            "mbx_check_modulation_table_add": [_P, _P, _P],
             "mbx_gated_residual_ln_modulate": [_P, _P, _P, _P, _P, _P, _P, _P, _f32, _int, _vp],
             "mbx_check_gated_residual_ln_modulate": [_P, _P, _P, _P, _P, _P, _P, _P, _f32, _int],
             "mbx_qk_norm_rope_qkv_epilogue": [_P, _P, _P, _i64, _i64, _P, _P, _P, _P,
@@ -146,7 +149,7 @@ def _rows_cols(t: torch.Tensor) -> tuple[int, int, int]:
 
 
 def _view(t: torch.Tensor) -> _View:
-    dtype = MBX_BF16 if t.dtype == torch.bfloat16 else 0
+    dtype = _DTYPES.get(t.dtype, 0)
     if t.is_contiguous() and t.dim() > 0:  # the common case, without the general walk
         cols = t.shape[-1]
         n = t.numel()
@@ -154,6 +157,9 @@ def _view(t: torch.Tensor) -> _View:
             return _View(t.data_ptr(), n // cols, cols, cols, dtype)
     rows, cols, stride = _rows_cols(t)
     return _View(t.data_ptr() if t.numel() else None, rows, cols, stride, dtype)
+
+
+_DTYPES = {torch.bfloat16: MBX_BF16, torch.float32: MBX_F32}
 
 
 def _ref(v: _View):
@@ -231,6 +237,32 @@ def residual_gate_add(x, gate, y, variant="lossless", out=None):
     _raise(L.mbx_residual_gate_add(_ref(o), _ref(xv), _ref(g), _ref(yv), _variant(variant),
                                    _stream(x)))
     return out
+
+
+def modulation_table_add(table, temb, out=None):
+    """Per-token modulation table in the (6, rows, D) layout (see
+    mbx_modulation_table_add): the eager ``(table.unsqueeze(0) +
+    temb.float()).chunk(6, dim=2)`` with the six chunks written as contiguous
+    binary32 planes.  table [6, D] (any leading size-1 dims), temb [..., 6, D]
+    or [..., 6*D]; bfloat16 or float32.  Returns out [6, *lead, D] float32
+    (``out[k]`` is chunk k)."""
+    L = _load()
+    D = table.shape[-1]
+    if temb.dim() >= 2 and temb.shape[-2] == 6 and temb.shape[-1] == D:
+        lead = tuple(temb.shape[:-2])
+        e = temb.reshape(*lead, 6 * D) if temb.is_contiguous() else temb.flatten(-2)
+    else:
+        lead = tuple(temb.shape[:-1])
+        e = temb
+    if out is None:
+        out = torch.empty((6, *lead, D), dtype=torch.float32, device=temb.device)
+    o, t, ev = _view(out), _view(table), _view(e)
+    _raise(L.mbx_modulation_table_add(_ref(o), _ref(t), _ref(ev), _stream(temb)))
+    return out
+
+
+def check_modulation_table_add(out, table, temb) -> int:
+    return _load().mbx_check_modulation_table_add(_ref(_view(out)), _ref(_view(table)), _ref(_view(temb)))
 
 
 def gated_residual_ln_modulate(residual, gate, update, scale, shift, bias=None, eps: float = 1e-6,

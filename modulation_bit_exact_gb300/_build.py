@@ -20,6 +20,7 @@ SOURCES = [
     os.path.join(KERN, "rmsnorm.cu"),
     os.path.join(KERN, "residual.cu"),
     os.path.join(KERN, "qkv.cu"),
+    os.path.join(KERN, "modtable.cu"),
     os.path.join(KERN, "selftest.cu"),
 ]
 HEADERS = [os.path.join(KERN, f) for f in os.listdir(KERN) if f.endswith((".cuh", ".h", ".inc"))]

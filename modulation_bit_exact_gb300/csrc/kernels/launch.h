@@ -131,6 +131,22 @@ struct PipeShape {
 int64_t pipe_rows_per_cta(int64_t rows);
 bool pipe_shape(const void* kernel, int tpr, int smem_per_group, int smem_fixed, int64_t rows, PipeShape* out);
 
+// Per-token modulation table: out[k*rows + r][d] = table[k][d] + temb[r][k*D + d].
+struct ModTableParams {
+    float* out;
+    int64_t out_stride;
+    const void* table;
+    int64_t table_stride;
+    bool table_f32;
+    const void* temb;
+    int64_t temb_stride;
+    bool temb_f32;
+    int64_t rows;
+    int D;
+    FastDiv by_nch;  // chunk index within a token row -> plane k (vector path)
+};
+cudaError_t launch_modulation_table_add(const ModTableParams& p, bool vec, cudaStream_t s);
+
 cudaError_t launch_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_rmsnorm_scale(const RmsScaleParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_rmsnorm_tanh_residual(const RmsTanhParams& p, bool vec, bool high, cudaStream_t s);

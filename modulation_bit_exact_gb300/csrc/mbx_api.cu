@@ -33,7 +33,9 @@ struct V {  // a view in one form, for the checks
 V of(const mbx_cview* v) { return V{v->data, v->rows, v->cols, v->row_stride, v->dtype}; }
 V of(const mbx_view* v) { return V{v->data, v->rows, v->cols, v->row_stride, v->dtype}; }
 
-int64_t extent_bytes(const V& v) { return ((v.rows - 1) * v.stride + v.cols) * 2; }
+int64_t esize(int32_t dtype) { return dtype == MBX_F32 ? 4 : 2; }
+
+int64_t extent_bytes(const V& v) { return ((v.rows - 1) * v.stride + v.cols) * esize(v.dtype); }
 
 // Step 1 of a view: dtype, non-empty, stride, alignment.
 int basic(const V& v) {
@@ -57,7 +59,17 @@ bool same_view(const V& a, const V& b) {
 }
 
 bool aligned16(const V& v) {
-    return reinterpret_cast<uintptr_t>(v.data) % 16 == 0 && (v.rows == 1 || v.stride % 8 == 0);
+    return reinterpret_cast<uintptr_t>(v.data) % 16 == 0 && (v.rows == 1 || (v.stride * esize(v.dtype)) % 16 == 0);
+}
+
+// basic() for an operand that may be bfloat16 or binary32.
+int basic_any(const V& v) {
+    if (v.data == nullptr) return MBX_E_NULL;
+    if (v.dtype != MBX_BF16 && v.dtype != MBX_F32) return MBX_E_DTYPE;
+    if (v.rows <= 0 || v.cols <= 0) return MBX_E_EMPTY;
+    if (v.rows > 1 && v.stride < v.cols) return MBX_E_STRIDE;
+    if (reinterpret_cast<uintptr_t>(v.data) % esize(v.dtype)) return MBX_E_ALIGN;
+    return MBX_OK;
 }
 
 int check_variant_eps(int variant, float eps) {
@@ -274,6 +286,24 @@ int check_gated(const mbx_view* res_out, const mbx_view* out, const mbx_cview* r
     if (dev) {
         V all[8] = {ro, o, r, g, u, sc, sh, b};
         MBX_TRY(views_on_device(all, has_b ? 8 : 7));
+    }
+    return MBX_OK;
+}
+
+int check_modtable(const mbx_view* out, const mbx_cview* table, const mbx_cview* temb, bool dev) {
+    if (!out || !table || !temb) return MBX_E_NULL;
+    V o = of(out), t = of(table), e = of(temb);
+    MBX_TRY(basic_any(o));
+    MBX_TRY(basic_any(t));
+    MBX_TRY(basic_any(e));
+    if (o.dtype != MBX_F32) return MBX_E_DTYPE;
+    const int64_t D = t.cols;
+    if (D > (int64_t)0x7fffffff / 6) return MBX_E_DIM_TOO_LARGE;
+    if (t.rows != 6 || e.cols != 6 * D || o.cols != D || o.rows != 6 * e.rows) return MBX_E_SHAPE;
+    if (overlaps(o, t) || overlaps(o, e)) return MBX_E_ALIAS;
+    if (dev) {
+        V all[3] = {o, t, e};
+        MBX_TRY(views_on_device(all, 3));
     }
     return MBX_OK;
 }
@@ -558,6 +588,29 @@ MBX_API int mbx_residual_gate_add(const mbx_view* out, const mbx_cview* x, const
                      aligned16(of(y));
     return cuda_status(
         mbx::launch_residual_gate_add(p, vec, variant == MBX_HIGH, (cudaStream_t)stream));
+}
+
+MBX_API int mbx_check_modulation_table_add(const mbx_view* out, const mbx_cview* table,
+                                           const mbx_cview* temb) {
+    return check_modtable(out, table, temb, true);
+}
+
+MBX_API int mbx_modulation_table_add(const mbx_view* out, const mbx_cview* table,
+                                     const mbx_cview* temb, void* stream) {
+    MBX_TRY(check_modtable(out, table, temb, true));
+    mbx::ModTableParams p;
+    p.out = static_cast<float*>(out->data);
+    p.out_stride = out->row_stride;
+    p.table = table->data;
+    p.table_stride = table->row_stride;
+    p.table_f32 = table->dtype == MBX_F32;
+    p.temb = temb->data;
+    p.temb_stride = temb->row_stride;
+    p.temb_f32 = temb->dtype == MBX_F32;
+    p.rows = temb->rows;
+    p.D = (int)table->cols;
+    const bool vec = p.D % 8 == 0 && aligned16(of(out)) && aligned16(of(table)) && aligned16(of(temb));
+    return cuda_status(mbx::launch_modulation_table_add(p, vec, (cudaStream_t)stream));
 }
 
 MBX_API int mbx_check_gated_residual_ln_modulate(const mbx_view* residual_out,

@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
     names = declared_symbols()
     for op in ("mbx_ln_modulate", "mbx_rmsnorm_scale", "mbx_rmsnorm_tanh_residual",
                "mbx_residual_gate_add", "mbx_qk_norm_rope_qkv_epilogue",
-               "mbx_gated_residual_ln_modulate"):
+               "mbx_gated_residual_ln_modulate", "mbx_modulation_table_add"):
         assert op in names and op.replace("mbx_", "mbx_check_") in names
 
 
@@ -266,3 +266,28 @@ def test_gated_residual_ln_modulate_rejections(mbx):
     assert st(ro, o, r, g, u, V(BASE + 0x800000, 1, D, dtype=0), sc, sh) == -2
     assert st(ro, o, r, g, u, b, sc, sh, variant=3) == -11
     assert st(ro, o, r, g, u, V(0, 1, D), sc, sh) == -1
+
+
+def test_modulation_table_add_rejections(mbx):
+    L = mbx.lib()
+    rows, D = 10, 48
+
+    def st(o, t, e):
+        a = L.mbx_check_modulation_table_add(ref(o), ref(t), ref(e))
+        assert a == L.mbx_modulation_table_add(ref(o), ref(t), ref(e), None)
+        return a
+
+    o = V(BASE, 6 * rows, D, dtype=2)
+    t = V(BASE + 0x400000, 6, D, dtype=1)
+    e = V(BASE + 0x800000, rows, 6 * D, dtype=1)
+    assert st(o, t, e) == -9                                        # host checks pass
+    assert st(o, V(BASE + 0x400000, 6, D, dtype=2), V(BASE + 0x800000, rows, 6 * D, dtype=2)) == -9
+    assert st(V(BASE, 6 * rows, D, dtype=1), t, e) == -2            # out must be binary32
+    assert st(o, V(BASE + 0x400000, 6, D, dtype=3), e) == -2        # unknown dtype
+    assert st(o, V(BASE + 0x400000, 5, D), e) == -5                 # table has 6 rows
+    assert st(o, t, V(BASE + 0x800000, rows, 6 * D + 8)) == -5      # temb rows hold 6*D
+    assert st(V(BASE, 6 * rows + 6, D, dtype=2), t, e) == -5        # out holds 6*rows rows
+    assert st(V(BASE + 0x800000, 6 * rows, D, dtype=2), t, e) == -8  # out over temb
+    assert st(V(BASE + 2, 6 * rows, D, dtype=2), t, e) == -7         # f32 misaligned
+    assert st(o, t, V(BASE + 0x800000, rows, 6 * D, 6 * D - 1)) == -6
+    assert st(o, V(0, 6, D), e) == -1
