@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
                 "orc_residual_gate_add": [_p, _i64, _p, _i64, _i64, _i64, _p, _i64, _i64, _p, _i64],
                 "orc_gated_residual_ln_modulate": [_p, _p, _p, _i64, _i64, _i64, _p, _i64, _p, _p,
                                                    _i64, _p, _i64, _p, _i64, _i64, _f32],
+                "orc_f32_to_e4m3": [_p, _p, _i64],
+                "orc_quant_e4m3": [_p, _i64, _p, _i64, _i64, _i64, _f32],
                 "orc_modulation_table_add": [_p, _i64, _p, _i64, ctypes.c_int, _p, _i64,
                                              ctypes.c_int, _i64, _i64],
                 "orc_qkv_epilogue": [_p, _p, _i64, _i64, _p, _i64, _i64, _i64, _i64, _i64,
@@ -245,6 +247,25 @@ def residual_gate_add(x: np.ndarray, gate: np.ndarray, y: np.ndarray) -> np.ndar
     out = np.empty((rows, D), dtype=np.uint16)
     lib().orc_residual_gate_add(_ptr(out), D, _ptr(x2), xs, rows, D, _ptr(g2), gs, grows, _ptr(y2), ys)
     return out
+
+
+def f32_to_e4m3(v: np.ndarray) -> np.ndarray:
+    """binary32 -> FP8 E4M3 bytes: nearest-even, saturating to +-448, NaN -> 0x7F."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    lib().orc_f32_to_e4m3(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def quant_e4m3(y: np.ndarray, scale: float) -> np.ndarray:
+    """Static per-tensor E4M3 copy of a bfloat16 output (tahou.com article,
+    section 将FP8量化融合到前序算子): e4m3(float(y) * (1/scale)), the reciprocal
+    correctly rounded in binary32."""
+    y2, ys = _rows(y)
+    rows, D = y2.shape
+    out = np.empty((rows, D), dtype=np.uint8)
+    lib().orc_quant_e4m3(_ptr(out), D, _ptr(y2), ys, rows, D, float(scale))
+    return out.reshape(y.shape)
 
 
 def modulation_table_add(table: np.ndarray, temb: np.ndarray) -> np.ndarray:

@@ -20,6 +20,10 @@
  *   [QKV]     tahou.com article, section 合并QKV投影时的数值问题 (merged QKV
  *             projection): Q/K RMSNorm, interleaved RoPE, V copy, text and image
  *             tokens written into one joint QKV buffer.
+ *   [FP8]     tahou.com article, section 将FP8量化融合到前序算子 (fusing FP8
+ *             quantisation into the producer): LayerNorm/AdaLN and gated
+ *             residual + LayerNorm/AdaLN write a BF16 output and its static
+ *             (per-tensor scale) E4M3 copy.
  *   [WAN]     tahou.com article, section Wan视频模型的数据搬运优化 (Wan data
  *             movement): the per-token modulation table
  *             (table.unsqueeze(0) + temb.float()).chunk(6, dim=2), written as six
@@ -331,6 +335,54 @@ void orc_gated_residual_ln_modulate(uint16_t* res_out, uint16_t* out, const uint
         }
     }
     orc_ln_modulate(out, D, res_out, D, rows, D, scale, scale_stride, shift, shift_stride, mod_rows, eps);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Static E4M3 quantisation [FP8]                                           */
+/* ------------------------------------------------------------------------ */
+
+/* binary32 -> FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits;
+ * no infinities; S.1111.111 is NaN; largest finite 448 = 1.75 * 2^8).
+ * Round to nearest, ties to even, on the exact value; a finite result beyond
+ * 448 and an infinity saturate to +-448 (the "satfinite" conversion of the
+ * FP8 producers); every NaN becomes 0x7F.  Signed zeros are kept. */
+static uint8_t e4m3_of(float v) {
+    uint32_t u;
+    memcpy(&u, &v, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7f;
+    const uint8_t sign = (uint8_t)((u >> 24) & 0x80u);
+    float a = fabsf(v);
+    if (a >= 448.0f) return (uint8_t)(sign | 0x7e);
+    if (a < 0x1p-6f) {
+        /* subnormal range: multiples of 2^-9; 8 * 2^-9 is the smallest normal,
+         * whose encoding continues the count (exponent field 1, mantissa 0) */
+        float q = rintf(a * 512.0f); /* exact scaling, then nearest-even */
+        return (uint8_t)(sign | (uint8_t)q);
+    }
+    int e;
+    frexpf(a, &e); /* a = f * 2^e, f in [0.5, 1): the binade is [2^(e-1), 2^e) */
+    e -= 1;
+    float q = rintf(ldexpf(a, 3 - e)); /* a / 2^(e-3): 8 <= q <= 16, exact scaling */
+    if (q == 16.0f) {
+        q = 8.0f;
+        e += 1;
+    }
+    return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | (uint8_t)((int)q - 8));
+}
+
+void orc_f32_to_e4m3(const float* in, uint8_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_of(in[i]);
+}
+
+/* The static quantiser applied to a BF16 output: q = e4m3(float(y) * inv) with
+ * inv = 1 / scale, a correctly rounded binary32 division (the pages compute
+ * it with div.full.f32, an approximation that a CPU cannot reproduce; see the
+ * reading in the design notes), and one rounded multiply. */
+void orc_quant_e4m3(uint8_t* out, int64_t out_stride, const uint16_t* y, int64_t y_stride,
+                    int64_t rows, int64_t D, float scale) {
+    const float inv = 1.0f / scale;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t e = 0; e < D; ++e) out[r * out_stride + e] = e4m3_of(f_of(y[r * y_stride + e]) * inv);
 }
 
 /* ------------------------------------------------------------------------ */

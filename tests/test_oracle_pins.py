@@ -646,3 +646,54 @@ def test_modulation_table_layout(orc):
         for r in range(rows):
             for d in range(D):
                 assert out[k, r, d] == table[k, d] + temb[r, k * D + d]
+
+
+# ------------------------------------------------------------ FP8 E4M3
+
+
+def _torch_e4m3(v: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_matches_torch_in_range(orc):
+    """Every bfloat16 value below 448 in magnitude, random binary32 values, and
+    every midpoint between neighbouring E4M3 values (ties to even), against
+    PyTorch's CPU float8_e4m3fn conversion."""
+    b = np.arange(65536, dtype=np.uint32)
+    v = (b << 16).view(np.float32)
+    v = v[np.isfinite(v) & (np.abs(v) < 448)]
+    rng = np.random.default_rng(5)
+    r = (rng.standard_normal(1 << 20) * np.exp2(rng.integers(-12, 9, 1 << 20))).astype(np.float32)
+    r = r[np.abs(r) < 448]
+    codes = np.arange(0x7f, dtype=np.uint8)  # all finite non-negative codes
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    mids = ((vals[:-1].astype(np.float64) + vals[1:]) / 2).astype(np.float32)
+    for x in (v, r, mids, -mids):
+        assert np.array_equal(orc.f32_to_e4m3(x), _torch_e4m3(x))
+
+
+def test_e4m3_closed_forms(orc):
+    f = orc.f32_to_e4m3
+    cases = [(448.0, 0x7E), (-448.0, 0xFE), (464.0, 0x7E), (500.0, 0x7E), (1e30, 0x7E),
+             (float("inf"), 0x7E), (-float("inf"), 0xFE), (0.0, 0x00), (-0.0, 0x80), (2.0 ** -9, 0x01),
+             (2.0 ** -10, 0x00), (3 * 2.0 ** -11, 0x01), (3 * 2.0 ** -10, 0x02), (5 * 2.0 ** -10, 0x02), (2.0 ** -6, 0x08), (1.0, 0x38), (1.0625, 0x38),
+             (1.1875, 0x3A), (240.0, 0x77), (float("nan"), 0x7F), (-float("nan"), 0x7F)]
+    for x, want in cases:
+        assert int(f(np.array([x], np.float32))[0]) == want, (x, hex(want))
+    # every code round-trips through its own value
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(f(vals), codes)
+
+
+def test_quant_e4m3_of_a_bf16_output(orc):
+    """The static quantiser multiplies by the correctly rounded 1/scale once."""
+    g = torch.Generator().manual_seed(81)
+    y = (torch.randn(20, 96, generator=g) * 3).to(torch.bfloat16)
+    for scale in (1.0, 0.0173, 3.3e-3, 0.5, 7.0):
+        inv = np.float32(1.0) / np.float32(scale)
+        prod = y.float().numpy() * inv
+        got = orc.quant_e4m3(u16(y), scale)
+        inr = np.abs(prod) < 448
+        assert np.array_equal(got[inr], _torch_e4m3(prod[inr]))
+        assert np.all(got[~inr] == np.where(prod[~inr] > 0, 0x7E, 0xFE))  # saturated
