@@ -435,7 +435,9 @@ def run_suite(args):
             return dict(x=r(rows, D), y=r(rows, D), res=r(rows, D), g=r(mrows, D) if tok else r(mrows, D, std=0.1),
                         sc=r(mrows, D, std=0.1), sh=r(mrows, D, std=0.1), w=r(D, std=0.05, mean=1.0),
                         b=r(1, D, std=0.5), out=torch.empty(rows, D, dtype=torch.bfloat16, device=dev),
-                        out2=torch.empty(rows, D, dtype=torch.bfloat16, device=dev))
+                        out2=torch.empty(rows, D, dtype=torch.bfloat16, device=dev),
+                        q=torch.empty(rows, D, dtype=torch.uint8, device=dev),
+                        s8=torch.full((1,), 0.02, dtype=torch.float32, device=dev))
         T = rows * D * 2
         M = mrows * D * 2
         ops = {
@@ -445,6 +447,11 @@ def run_suite(args):
             "residual_gate_add": (3 * T + M, lambda s, v: mbx.residual_gate_add(s["x"], s["g"], s["y"], variant=v, out=s["out"])),
             "gated_residual_ln_modulate": (4 * T + 3 * M + D * 2, lambda s, v: mbx.gated_residual_ln_modulate(
                 s["res"], s["g"], s["y"], s["sc"], s["sh"], bias=s["b"], variant=v, out=s["out"], residual_out=s["out2"])),
+            "ln_modulate_fp8": (2 * T + 2 * M + T // 2, lambda s, v: mbx.ln_modulate_fp8(
+                s["x"], s["sc"], s["sh"], s["s8"], variant=v, out=s["out"], out_fp8=s["q"])),
+            "gated_residual_ln_modulate_fp8": (4 * T + 3 * M + D * 2 + T // 2, lambda s, v: mbx.gated_residual_ln_modulate_fp8(
+                s["res"], s["g"], s["y"], s["sc"], s["sh"], s["s8"], bias=s["b"], variant=v, out=s["out"],
+                residual_out=s["out2"], out_fp8=s["q"])),
         }
         for op, (nb, fn) in ops.items():
             for v in ("lossless", "high"):

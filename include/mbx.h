@@ -60,8 +60,9 @@ extern "C" {
 #define MBX_ABI_VERSION 1
 
 /* dtype codes.  Every operation takes bfloat16 operands, except that the
- * modulation-table add also accepts binary32 inputs and writes binary32. */
-enum { MBX_BF16 = 1, MBX_F32 = 2 };
+ * modulation-table add also accepts binary32 inputs and writes binary32, and
+ * the FP8 producers write an extra FP8 E4M3 (one byte per element) output. */
+enum { MBX_BF16 = 1, MBX_F32 = 2, MBX_E4M3 = 3 };
 
 /* variant codes */
 enum { MBX_LOSSLESS = 0, MBX_HIGH = 1 };
@@ -179,6 +180,36 @@ MBX_API int mbx_gated_residual_ln_modulate(const mbx_view* residual_out, const m
                                            float eps, int variant, void* stream);
 
 /*
+ * FP8 producers: the two LayerNorm + AdaLN entry points above with a second,
+ * static E4M3 output.
+ * Defined in: tahou.com SGLang diffusion article, section 将FP8量化融合到前序算子
+ * -- LayerNorm/AdaLN and gated residual + LayerNorm/AdaLN write the BF16
+ * result (kept for the residual branch) and its static-scale E4M3 copy (fed
+ * to the next GEMM) in the same pass, instead of a separate quantisation
+ * kernel re-reading the BF16 tensor:
+ *   out_fp8 = e4m3(float(out) * inv),  inv = 1 / *fp8_scale
+ * inv is the correctly rounded binary32 reciprocal (the pages' quantiser
+ * takes it with div.full.f32, an approximation; see the design notes), the
+ * product is rounded once, and the conversion rounds to nearest even,
+ * saturates finite overflow and infinities to +-448 and maps NaN to 0x7F
+ * (cvt.rn.satfinite; mbx_selftest(5) checks it against the definition).
+ * out_fp8: MBX_E4M3 [rows, D] (row_stride in bytes-as-elements), overlapping
+ * nothing.  fp8_scale: device pointer to one binary32 per-tensor scale
+ * (caller-owned, read on the stream, so it may change between calls without
+ * a sync).  Everything else as in mbx_ln_modulate /
+ * mbx_gated_residual_ln_modulate.
+ */
+MBX_API int mbx_ln_modulate_fp8(const mbx_view* out, const mbx_view* out_fp8, const mbx_cview* x,
+                                const mbx_cview* scale, const mbx_cview* shift,
+                                const float* fp8_scale, float eps, int variant, void* stream);
+MBX_API int mbx_gated_residual_ln_modulate_fp8(const mbx_view* residual_out, const mbx_view* out,
+                                               const mbx_view* out_fp8, const mbx_cview* residual,
+                                               const mbx_cview* gate, const mbx_cview* update,
+                                               const mbx_cview* bias, const mbx_cview* scale,
+                                               const mbx_cview* shift, const float* fp8_scale,
+                                               float eps, int variant, void* stream);
+
+/*
  * Per-token modulation table, written in the (6, rows, D) layout.
  * Defined in: tahou.com SGLang diffusion article, section
  * Wan视频模型的数据搬运优化 -- the eager (table.unsqueeze(0) + temb.float())
@@ -240,6 +271,15 @@ MBX_API int mbx_check_rmsnorm_tanh_residual(const mbx_view* out, const mbx_cview
                                             const mbx_cview* weight, float eps, int variant);
 MBX_API int mbx_check_residual_gate_add(const mbx_view* out, const mbx_cview* x,
                                         const mbx_cview* gate, const mbx_cview* y, int variant);
+MBX_API int mbx_check_ln_modulate_fp8(const mbx_view* out, const mbx_view* out_fp8,
+                                      const mbx_cview* x, const mbx_cview* scale,
+                                      const mbx_cview* shift, const float* fp8_scale, float eps,
+                                      int variant);
+MBX_API int mbx_check_gated_residual_ln_modulate_fp8(
+    const mbx_view* residual_out, const mbx_view* out, const mbx_view* out_fp8,
+    const mbx_cview* residual, const mbx_cview* gate, const mbx_cview* update,
+    const mbx_cview* bias, const mbx_cview* scale, const mbx_cview* shift,
+    const float* fp8_scale, float eps, int variant);
 MBX_API int mbx_check_modulation_table_add(const mbx_view* out, const mbx_cview* table,
                                            const mbx_cview* temb);
 MBX_API int mbx_check_gated_residual_ln_modulate(const mbx_view* residual_out,
@@ -269,7 +309,11 @@ MBX_API int mbx_check_qk_norm_rope_qkv_epilogue(
  *              and +0;
  *   which = 4: the reciprocal-square-root table of the QKV epilogue vs
  *              bf16(div.rn(1, sqrt.rn(v))) for every non-negative bfloat16 v
- *              (finite and +inf).
+ *              (finite and +inf);
+ *   which = 5: the hardware binary32 -> FP8 E4M3 conversion used by the FP8
+ *              producers vs the E4M3 definition (nearest even, saturation
+ *              to +-448, NaN -> 0x7F) for every binary32 pattern; the second
+ *              counter holds NaN inputs whose byte is not 0x7F.
  * counts: device pointer to 2 uint64 counters (caller-owned), overwritten
  * with {mismatches between non-NaN results, mismatches where either is NaN}.
  * Enqueued on `stream`; the caller synchronises before reading counts.

@@ -25,7 +25,8 @@ import torch
 __all__ = [
     "ln_modulate", "rmsnorm_scale", "rmsnorm_tanh_residual", "residual_gate_add",
     "qk_norm_rope_qkv_epilogue", "gated_residual_ln_modulate", "check_gated_residual_ln_modulate",
-    "modulation_table_add", "check_modulation_table_add",
+    "modulation_table_add", "check_modulation_table_add", "ln_modulate_fp8", "check_ln_modulate_fp8",
+    "gated_residual_ln_modulate_fp8", "check_gated_residual_ln_modulate_fp8",
     "check_ln_modulate", "check_rmsnorm_scale",
     "check_rmsnorm_tanh_residual", "check_residual_gate_add",
     "check_qk_norm_rope_qkv_epilogue", "selftest", "status_string", "MbxError",
@@ -33,7 +34,7 @@ __all__ = [
 ]
 
 LOSSLESS, HIGH = 0, 1
-MBX_BF16, MBX_F32 = 1, 2
+MBX_BF16, MBX_F32, MBX_E4M3 = 1, 2, 3
 _VARIANTS = {"lossless": LOSSLESS, "high": HIGH, LOSSLESS: LOSSLESS, HIGH: HIGH}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -85,6 +86,10 @@ def _load() -> ctypes.CDLL:
             "mbx_rmsnorm_scale": [_P, _P, _P, _P, _f32, _int, _vp],
             "mbx_rmsnorm_tanh_residual": [_P, _P, _P, _P, _P, _f32, _int, _vp],
             "mbx_residual_gate_add": [_P, _P, _P, _P, _int, _vp],
+            "mbx_ln_modulate_fp8": [_P, _P, _P, _P, _P, _vp, _f32, _int, _vp],
+            "mbx_check_ln_modulate_fp8": [_P, _P, _P, _P, _P, _vp, _f32, _int],
+            "mbx_gated_residual_ln_modulate_fp8": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _vp, _f32, _int, _vp],
+            "mbx_check_gated_residual_ln_modulate_fp8": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _vp, _f32, _int],
             "mbx_modulation_table_add": [_P, _P, _P, _vp],
             "mbx_check_modulation_table_add": [_P, _P, _P],
             "mbx_gated_residual_ln_modulate": [_P, _P, _P, _P, _P, _P, _P, _P, _f32, _int, _vp],
@@ -159,7 +164,9 @@ def _view(t: torch.Tensor) -> _View:
     return _View(t.data_ptr() if t.numel() else None, rows, cols, stride, dtype)
 
 
-_DTYPES = {torch.bfloat16: MBX_BF16, torch.float32: MBX_F32}
+_DTYPES = {torch.bfloat16: MBX_BF16, torch.float32: MBX_F32, torch.uint8: MBX_E4M3}
+if hasattr(torch, "float8_e4m3fn"):
+    _DTYPES[torch.float8_e4m3fn] = MBX_E4M3
 
 
 def _ref(v: _View):
@@ -237,6 +244,59 @@ def residual_gate_add(x, gate, y, variant="lossless", out=None):
     _raise(L.mbx_residual_gate_add(_ref(o), _ref(xv), _ref(g), _ref(yv), _variant(variant),
                                    _stream(x)))
     return out
+
+
+def _fp8_like(x: torch.Tensor) -> torch.Tensor:
+    dt = getattr(torch, "float8_e4m3fn", torch.uint8)
+    return torch.empty(x.shape, dtype=dt, device=x.device)
+
+
+def ln_modulate_fp8(x, scale, shift, fp8_scale, eps: float = 1e-6, variant="lossless", out=None,
+                    out_fp8=None):
+    """LN + AdaLN modulate writing the bf16 result and its static E4M3 copy
+    e4m3(out / fp8_scale) in one pass (see mbx_ln_modulate_fp8).  fp8_scale is a
+    one-element float32 CUDA tensor.  Returns (out, out_fp8)."""
+    L = _load()
+    out = _empty_like_rows(x) if out is None else out
+    out_fp8 = _fp8_like(x) if out_fp8 is None else out_fp8
+    o, q, xv, sc, sh = _view(out), _view(out_fp8), _view(x), _view(scale), _view(shift)
+    _raise(L.mbx_ln_modulate_fp8(_ref(o), _ref(q), _ref(xv), _ref(sc), _ref(sh), _ptr(fp8_scale), eps,
+                                 _variant(variant), _stream(x)))
+    return out, out_fp8
+
+
+def check_ln_modulate_fp8(out, out_fp8, x, scale, shift, fp8_scale, eps=1e-6, variant="lossless") -> int:
+    return _load().mbx_check_ln_modulate_fp8(_ref(_view(out)), _ref(_view(out_fp8)), _ref(_view(x)),
+                                             _ref(_view(scale)), _ref(_view(shift)), _ptr(fp8_scale), eps,
+                                             _variant(variant))
+
+
+def gated_residual_ln_modulate_fp8(residual, gate, update, scale, shift, fp8_scale, bias=None,
+                                   eps: float = 1e-6, variant="lossless", out=None, residual_out=None,
+                                   out_fp8=None):
+    """Gated residual + LN + AdaLN modulate writing r', the bf16 result and its
+    static E4M3 copy (see mbx_gated_residual_ln_modulate_fp8).  Returns
+    (residual_out, out, out_fp8)."""
+    L = _load()
+    out = _empty_like_rows(residual) if out is None else out
+    residual_out = _empty_like_rows(residual) if residual_out is None else residual_out
+    out_fp8 = _fp8_like(residual) if out_fp8 is None else out_fp8
+    ro, o, q = _view(residual_out), _view(out), _view(out_fp8)
+    r, g, u, sc, sh = _view(residual), _view(gate), _view(update), _view(scale), _view(shift)
+    b = None if bias is None else _view(bias)
+    _raise(L.mbx_gated_residual_ln_modulate_fp8(_ref(ro), _ref(o), _ref(q), _ref(r), _ref(g), _ref(u),
+                                                None if b is None else _ref(b), _ref(sc), _ref(sh),
+                                                _ptr(fp8_scale), eps, _variant(variant), _stream(residual)))
+    return residual_out, out, out_fp8
+
+
+def check_gated_residual_ln_modulate_fp8(residual_out, out, out_fp8, residual, gate, update, scale, shift,
+                                         fp8_scale, bias=None, eps=1e-6, variant="lossless") -> int:
+    b = None if bias is None else _view(bias)
+    return _load().mbx_check_gated_residual_ln_modulate_fp8(
+        _ref(_view(residual_out)), _ref(_view(out)), _ref(_view(out_fp8)), _ref(_view(residual)),
+        _ref(_view(gate)), _ref(_view(update)), None if b is None else _ref(b), _ref(_view(scale)),
+        _ref(_view(shift)), _ptr(fp8_scale), eps, _variant(variant))
 
 
 def modulation_table_add(table, temb, out=None):

@@ -32,7 +32,23 @@ struct LnModParams {
     // -0.0f as a kernel argument: the packed Welford update takes its product
     // as fma(d, t, neg_zero), which the compiler cannot turn into a multiply
     float neg_zero = -0.0f;
+    // static E4M3 copy of out (the FP8 producers): q = e4m3(out * (1/scale))
+    uint8_t* out_fp8 = nullptr;
+    int64_t out_fp8_stride = 0;
+    const float* fp8_scale = nullptr;  // device, one per-tensor scale
 };
+
+// Static E4M3 copy of a bf16 matrix: out[r][e] = e4m3(y[r][e] * (1/scale)).
+struct QuantParams {
+    uint8_t* out;
+    int64_t out_stride;
+    const uint16_t* y;
+    int64_t y_stride;
+    int64_t rows;
+    int D;
+    const float* scale;
+};
+cudaError_t launch_quant_e4m3(const QuantParams& p, cudaStream_t s);
 
 struct RmsScaleParams {
     uint16_t* out;
@@ -152,6 +168,8 @@ cudaError_t launch_rmsnorm_scale(const RmsScaleParams& p, bool vec, bool high, c
 cudaError_t launch_rmsnorm_tanh_residual(const RmsTanhParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_residual_gate_add(const GateAddParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_gated_residual_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s);
+cudaError_t launch_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cudaStream_t s);
+cudaError_t launch_gated_residual_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_qkv_epilogue(const QkvParams& p, bool high, cudaStream_t s);
 cudaError_t launch_selftest(int which, unsigned long long* counts, cudaStream_t s);
 

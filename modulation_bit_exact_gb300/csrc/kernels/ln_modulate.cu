@@ -384,6 +384,8 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
     const int64_t split = (m0 + 1) * p.seq;  // staged: rows from here use slot 1
     const int64_t first = r0 + g;
     RowDiv next(first, groups, p.seq);  // modulation row of the next row to issue
+    // FP8 producer: 1/scale correctly rounded, once per thread
+    const float inv8 = p.out_fp8 != nullptr ? __fdiv_rn(1.0f, __ldg(p.fp8_scale)) : 0.0f;
 
     auto issue = [&](int s, int64_t row) {
         ring.issue(s, 0, p.x + row * p.x_stride, t, nch);
@@ -553,6 +555,9 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                     w_set(o, i, ow);
                 }
                 st_v4(out_row + (int64_t)c * kChunk, o);
+                if (p.out_fp8 != nullptr)
+                    st_v2(p.out_fp8 + row * p.out_fp8_stride + (int64_t)c * kChunk, e4m3x4_of_bf16(o.x, o.y, inv8),
+                          e4m3x4_of_bf16(o.z, o.w, inv8));
             }
         cur = cur + 1 == NS ? 0 : cur + 1;
     }
@@ -619,10 +624,28 @@ static cudaError_t launch_pipe_d(const LnModParams& p, bool high, cudaStream_t s
     }
 }
 
+// Whether the fused ring kernel keeps at least two row groups per SM: its
+// stages carry the residual and the update (and the modulation per token),
+// and per-sample modulation, gate and bias are staged.  At the widest rows
+// one group would remain, and two launches (gated add, then LN) move more
+// bytes but run faster.  Same arithmetic as launch_pipe.
+static bool fused_fits(const LnModParams& p) {
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    const int J = chunks_per_lane(p.D), nch = p.D / kChunk;
+    const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
+    const int nops = staged ? LnOps<true, kModStaged>::N : LnOps<true, kModRing>::N;
+    const int per_group = (int)sizeof(TreeSmem) + 2 * nops * kLanes * J * 16;
+    const int fixed = (staged ? 2 * LnOps<true, kModStaged>::SLOT * nch * 16 : 0) + (p.bias ? nch * 16 : 0);
+    return (optin - 8 * 1024 - fixed) / per_group >= 2;
+}
+
 cudaError_t launch_gated_residual_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
-    if (vec) return launch_pipe_d<true>(p, high, s);
-    // unaligned or ragged rows: the same definition as two steps, the gated
-    // residual into res_out, then LayerNorm + modulate of res_out
+    if (vec && fused_fits(p)) return launch_pipe_d<true>(p, high, s);
+    // unaligned or ragged rows, or rows too wide for the fused ring: the same
+    // definition as two steps, the gated residual into res_out, then
+    // LayerNorm + modulate of res_out
     GateAddParams g;
     g.out = p.res_out;
     g.out_stride = p.res_out_stride;
@@ -636,12 +659,47 @@ cudaError_t launch_gated_residual_ln_modulate(const LnModParams& p, bool vec, bo
     g.D = p.D;
     g.seq = p.seq;
     g.bias = p.bias;
-    cudaError_t e = launch_residual_gate_add(g, false, false, s);
+    cudaError_t e = launch_residual_gate_add(g, vec, false, s);
     if (e != cudaSuccess) return e;
     LnModParams q = p;
     q.x = p.res_out;
     q.x_stride = p.res_out_stride;
-    return launch_ln_modulate(q, false, high, s);
+    q.update = nullptr;
+    q.gate = nullptr;
+    q.bias = nullptr;
+    q.res_out = nullptr;
+    return vec ? launch_pipe_d<false>(q, high, s) : launch_ln_modulate(q, false, high, s);
+}
+
+// The FP8 copy outside the pipelined kernel: quantise the bf16 output after it
+// is written (the same definition: the copy is of the bf16 value).
+static cudaError_t quantise_out(const LnModParams& p, cudaStream_t s) {
+    QuantParams q;
+    q.out = p.out_fp8;
+    q.out_stride = p.out_fp8_stride;
+    q.y = p.out;
+    q.y_stride = p.out_stride;
+    q.rows = p.rows;
+    q.D = p.D;
+    q.scale = p.fp8_scale;
+    return launch_quant_e4m3(q, s);
+}
+
+cudaError_t launch_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
+    if (vec) return launch_pipe_d<false>(p, high, s);
+    LnModParams q = p;
+    q.out_fp8 = nullptr;
+    cudaError_t e = launch_ln_modulate(q, false, high, s);
+    return e != cudaSuccess ? e : quantise_out(p, s);
+}
+
+cudaError_t launch_gated_residual_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
+    if (vec && fused_fits(p)) return launch_pipe_d<true>(p, high, s);
+    if (vec) return launch_gated_residual_ln_modulate(p, true, high, s);  // composed; the LN pass writes the FP8 copy
+    LnModParams q = p;
+    q.out_fp8 = nullptr;
+    cudaError_t e = launch_gated_residual_ln_modulate(q, false, high, s);
+    return e != cudaSuccess ? e : quantise_out(p, s);
 }
 
 cudaError_t launch_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s) {

@@ -274,6 +274,26 @@ __device__ __forceinline__ void st_v4(void* p, uint4 v) {
                  "r"(v.w)
                  : "memory");
 }
+// Two binary32 values to FP8 E4M3 (round to nearest even, finite overflow
+// and infinities saturate to +-448, NaN to 0x7F): `lo` in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float hi, float lo) {
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Four bf16 values (two packed words) times `inv`, each product rounded once,
+// to four E4M3 bytes in element order.
+__device__ __forceinline__ uint32_t e4m3x4_of_bf16(uint32_t w0, uint32_t w1, float inv) {
+    const uint32_t a = e4m3x2(__fmul_rn(hi_f(w0), inv), __fmul_rn(lo_f(w0), inv));
+    const uint32_t b = e4m3x2(__fmul_rn(hi_f(w1), inv), __fmul_rn(lo_f(w1), inv));
+    return a | (b << 16);
+}
+
+__device__ __forceinline__ void st_v2(void* p, uint32_t a, uint32_t b) {
+    asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
 __device__ __forceinline__ uint16_t ld_u16(const void* p) {
     uint16_t v;
     asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));

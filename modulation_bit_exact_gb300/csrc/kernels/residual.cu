@@ -91,4 +91,25 @@ cudaError_t launch_residual_gate_add(const GateAddParams& p, bool vec, bool high
     }
 }
 
+// Static E4M3 copy of a bf16 matrix (the FP8 producers' fallback for rows
+// the pipelined kernel does not take): one element per step, any alignment.
+__global__ void __launch_bounds__(kBlock) quant_e4m3_kernel(QuantParams p) {
+    const float inv = __fdiv_rn(1.0f, __ldg(p.scale));
+    for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
+        const uint16_t* y = p.y + r * p.y_stride;
+        uint8_t* o = p.out + r * p.out_stride;
+        for (int e = threadIdx.x; e < p.D; e += blockDim.x) {
+            const float v = __uint_as_float((uint32_t)ld_u16(y + e) << 16);
+            o[e] = (uint8_t)(e4m3x2(0.0f, __fmul_rn(v, inv)) & 0xffu);
+        }
+    }
+}
+
+cudaError_t launch_quant_e4m3(const QuantParams& p, cudaStream_t s) {
+    const int grid = grid_for_rows(reinterpret_cast<const void*>(quant_e4m3_kernel), p.rows, 1, kBlock);
+    if (grid < 0) return cudaErrorUnknown;
+    quant_e4m3_kernel<<<grid, kBlock, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace mbx

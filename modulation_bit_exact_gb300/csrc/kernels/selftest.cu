@@ -8,7 +8,11 @@
 //   3: div_k_fast<K>(d) (no guard) == div.rn(d, K) for K = 1..64, every
 //      binary32 d with |d| >= 2^-100, and d = +0;
 //   4: the QKV epilogue's rstd table == bf16(div.rn(1, sqrt.rn(v))) for every
-//      non-negative bfloat16 v (finite and +inf).
+//      non-negative bfloat16 v (finite and +inf);
+//   5: the hardware binary32 -> E4M3 conversion of the FP8 producers
+//      (cvt.rn.satfinite.e4m3x2.f32) == the E4M3 definition (nearest even on
+//      the exact value, saturation to +-448, NaN -> 0x7F) for every binary32
+//      pattern; NaN inputs whose byte is not 0x7F are counted apart.
 // A mismatch where either result is a NaN is counted apart from the others:
 // NaN payloads never reach a bfloat16 output except as the canonical NaN.
 #include "launch.h"
@@ -83,6 +87,42 @@ __global__ void selftest_rstd_kernel(unsigned long long* counts) {
     if (bad) atomicAdd(&counts[0], bad);
 }
 
+// E4M3 from its definition: 1 sign, 4 exponent bits (bias 7), 3 mantissa
+// bits, largest finite 1.75 * 2^8; multiples of 2^-9 below 2^-6.
+__device__ uint32_t e4m3_by_definition(float v) {
+    const uint32_t u = __float_as_uint(v);
+    if (is_nan32(u)) return 0x7fu;
+    const uint32_t sign = (u >> 24) & 0x80u;
+    const float a = fabsf(v);
+    if (a >= 448.0f) return sign | 0x7eu;  // 464 ties to 448 (even); beyond saturates
+    if (a < 0x1p-6f) return sign | (uint32_t)rintf(a * 512.0f);
+    const int e = (int)((__float_as_uint(a) >> 23) & 0xffu) - 127;  // a is normal here
+    float q = rintf(a * __uint_as_float((uint32_t)(127 + 3 - e) << 23));  // a / 2^(e-3), exact
+    int ee = e;
+    if (q == 16.0f) {
+        q = 8.0f;
+        ++ee;
+    }
+    return sign | ((uint32_t)(ee + 7) << 3) | ((uint32_t)q - 8u);
+}
+
+__global__ void selftest_e4m3_kernel(unsigned long long* counts) {
+    unsigned long long bad = 0, bad_nan = 0;
+    const uint64_t total = 1ull << 32;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (uint64_t)gridDim.x * blockDim.x) {
+        const float v = __uint_as_float((uint32_t)i);
+        const uint32_t got = e4m3x2(0.0f, v) & 0xffu;
+        if (is_nan32((uint32_t)i)) {
+            if (got != 0x7fu) ++bad_nan;
+        } else if (got != e4m3_by_definition(v)) {
+            ++bad;
+        }
+    }
+    if (bad) atomicAdd(&counts[0], bad);
+    if (bad_nan) atomicAdd(&counts[1], bad_nan);
+}
+
 cudaError_t launch_selftest(int which, unsigned long long* counts, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(counts, 0, 2 * sizeof(unsigned long long), s);
     if (e != cudaSuccess) return e;
@@ -94,6 +134,7 @@ cudaError_t launch_selftest(int which, unsigned long long* counts, cudaStream_t 
         case 0: selftest_div_kernel<false><<<grid, block, 0, s>>>(counts); break;
         case 3: selftest_div_kernel<true><<<grid, block, 0, s>>>(counts); break;
         case 4: selftest_rstd_kernel<<<grid, block, 0, s>>>(counts); break;
+        case 5: selftest_e4m3_kernel<<<grid, block, 0, s>>>(counts); break;
         case 1: selftest_bf16x2_kernel<true><<<grid, block, 0, s>>>(counts); break;
         case 2: selftest_bf16x2_kernel<false><<<grid, block, 0, s>>>(counts); break;
         default: return cudaErrorInvalidValue;

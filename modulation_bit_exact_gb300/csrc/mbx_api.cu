@@ -33,7 +33,7 @@ struct V {  // a view in one form, for the checks
 V of(const mbx_cview* v) { return V{v->data, v->rows, v->cols, v->row_stride, v->dtype}; }
 V of(const mbx_view* v) { return V{v->data, v->rows, v->cols, v->row_stride, v->dtype}; }
 
-int64_t esize(int32_t dtype) { return dtype == MBX_F32 ? 4 : 2; }
+int64_t esize(int32_t dtype) { return dtype == MBX_F32 ? 4 : dtype == MBX_E4M3 ? 1 : 2; }
 
 int64_t extent_bytes(const V& v) { return ((v.rows - 1) * v.stride + v.cols) * esize(v.dtype); }
 
@@ -290,6 +290,64 @@ int check_gated(const mbx_view* res_out, const mbx_view* out, const mbx_cview* r
     return MBX_OK;
 }
 
+// The FP8 producers' extra output and scale: E4M3 [rows, D] like `out`,
+// overlapping none of the other views; the scale one device binary32.
+int check_fp8(const mbx_view* out_fp8, const float* fp8_scale, const V* others, int n, bool dev) {
+    if (!out_fp8 || !out_fp8->data || !fp8_scale) return MBX_E_NULL;
+    V q = of(out_fp8);
+    if (q.dtype != MBX_E4M3) return MBX_E_DTYPE;
+    if (q.rows <= 0 || q.cols <= 0) return MBX_E_EMPTY;
+    if (q.rows > 1 && q.stride < q.cols) return MBX_E_STRIDE;
+    if (reinterpret_cast<uintptr_t>(fp8_scale) % 4) return MBX_E_ALIGN;
+    if (q.rows != others[0].rows || q.cols != others[0].cols) return MBX_E_SHAPE;  // others[0] = out
+    for (int i = 0; i < n; ++i)
+        if (overlaps(q, others[i])) return MBX_E_ALIAS;
+    if (dev) {
+        MBX_TRY(views_on_device(&q, 1));
+        MBX_TRY(raw_on_device(fp8_scale, 4));
+    }
+    return MBX_OK;
+}
+
+bool aligned8_fp8(const mbx_view* q) {
+    return reinterpret_cast<uintptr_t>(q->data) % 8 == 0 && (q->rows == 1 || q->row_stride % 8 == 0);
+}
+
+mbx::LnModParams gated_params(const mbx_view* residual_out, const mbx_view* out, const mbx_cview* residual,
+                              const mbx_cview* gate, const mbx_cview* update, const mbx_cview* bias,
+                              const mbx_cview* scale, const mbx_cview* shift, float eps) {
+    mbx::LnModParams p;
+    p.out = static_cast<uint16_t*>(out->data);
+    p.out_stride = out->row_stride;
+    p.x = static_cast<const uint16_t*>(residual->data);
+    p.x_stride = residual->row_stride;
+    p.scale = static_cast<const uint16_t*>(scale->data);
+    p.scale_stride = scale->row_stride;
+    p.shift = static_cast<const uint16_t*>(shift->data);
+    p.shift_stride = shift->row_stride;
+    p.rows = residual->rows;
+    p.D = (int)residual->cols;
+    p.seq = residual->rows / scale->rows;
+    p.eps = eps;
+    p.update = static_cast<const uint16_t*>(update->data);
+    p.update_stride = update->row_stride;
+    p.gate = static_cast<const uint16_t*>(gate->data);
+    p.gate_stride = gate->row_stride;
+    p.bias = bias ? static_cast<const uint16_t*>(bias->data) : nullptr;
+    p.res_out = static_cast<uint16_t*>(residual_out->data);
+    p.res_out_stride = residual_out->row_stride;
+    return p;
+}
+
+bool gated_vec(const mbx::LnModParams& p, const mbx_view* residual_out, const mbx_view* out,
+               const mbx_cview* residual, const mbx_cview* gate, const mbx_cview* update,
+               const mbx_cview* bias, const mbx_cview* scale, const mbx_cview* shift) {
+    bool vec = p.D % 8 == 0 && aligned16(of(residual_out)) && aligned16(of(out)) && aligned16(of(residual)) &&
+               aligned16(of(gate)) && aligned16(of(update)) && aligned16(of(scale)) && aligned16(of(shift));
+    if (bias) vec = vec && aligned16(of(bias));
+    return vec;
+}
+
 int check_modtable(const mbx_view* out, const mbx_cview* table, const mbx_cview* temb, bool dev) {
     if (!out || !table || !temb) return MBX_E_NULL;
     V o = of(out), t = of(table), e = of(temb);
@@ -507,6 +565,44 @@ MBX_API int mbx_ln_modulate(const mbx_view* out, const mbx_cview* x, const mbx_c
     return cuda_status(mbx::launch_ln_modulate(p, vec, variant == MBX_HIGH, (cudaStream_t)stream));
 }
 
+MBX_API int mbx_check_ln_modulate_fp8(const mbx_view* out, const mbx_view* out_fp8,
+                                      const mbx_cview* x, const mbx_cview* scale,
+                                      const mbx_cview* shift, const float* fp8_scale, float eps,
+                                      int variant) {
+    // every host check of both parts before any device check
+    for (bool dev : {false, true}) {
+        MBX_TRY(check_ln_modulate(out, x, scale, shift, eps, variant, dev));
+        V vs[4] = {of(out), of(x), of(scale), of(shift)};
+        MBX_TRY(check_fp8(out_fp8, fp8_scale, vs, 4, dev));
+    }
+    return MBX_OK;
+}
+
+MBX_API int mbx_ln_modulate_fp8(const mbx_view* out, const mbx_view* out_fp8, const mbx_cview* x,
+                                const mbx_cview* scale, const mbx_cview* shift,
+                                const float* fp8_scale, float eps, int variant, void* stream) {
+    MBX_TRY(mbx_check_ln_modulate_fp8(out, out_fp8, x, scale, shift, fp8_scale, eps, variant));
+    mbx::LnModParams p;
+    p.out = static_cast<uint16_t*>(out->data);
+    p.out_stride = out->row_stride;
+    p.x = static_cast<const uint16_t*>(x->data);
+    p.x_stride = x->row_stride;
+    p.scale = static_cast<const uint16_t*>(scale->data);
+    p.scale_stride = scale->row_stride;
+    p.shift = static_cast<const uint16_t*>(shift->data);
+    p.shift_stride = shift->row_stride;
+    p.rows = x->rows;
+    p.D = (int)x->cols;
+    p.seq = x->rows / scale->rows;
+    p.eps = eps;
+    p.out_fp8 = static_cast<uint8_t*>(out_fp8->data);
+    p.out_fp8_stride = out_fp8->row_stride;
+    p.fp8_scale = fp8_scale;
+    const bool vec = p.D % 8 == 0 && aligned16(of(out)) && aligned16(of(x)) && aligned16(of(scale)) &&
+                     aligned16(of(shift)) && aligned8_fp8(out_fp8);
+    return cuda_status(mbx::launch_ln_modulate_fp8(p, vec, variant == MBX_HIGH, (cudaStream_t)stream));
+}
+
 MBX_API int mbx_check_rmsnorm_scale(const mbx_view* out, const mbx_cview* x,
                                     const mbx_cview* weight, const mbx_cview* scale, float eps,
                                     int variant) {
@@ -590,6 +686,37 @@ MBX_API int mbx_residual_gate_add(const mbx_view* out, const mbx_cview* x, const
         mbx::launch_residual_gate_add(p, vec, variant == MBX_HIGH, (cudaStream_t)stream));
 }
 
+MBX_API int mbx_check_gated_residual_ln_modulate_fp8(
+    const mbx_view* residual_out, const mbx_view* out, const mbx_view* out_fp8,
+    const mbx_cview* residual, const mbx_cview* gate, const mbx_cview* update,
+    const mbx_cview* bias, const mbx_cview* scale, const mbx_cview* shift,
+    const float* fp8_scale, float eps, int variant) {
+    for (bool dev : {false, true}) {
+        MBX_TRY(check_gated(residual_out, out, residual, gate, update, bias, scale, shift, eps, variant, dev));
+        V vs[8] = {of(out), of(residual_out), of(residual), of(gate), of(update), of(scale), of(shift),
+                   bias ? of(bias) : of(gate)};
+        MBX_TRY(check_fp8(out_fp8, fp8_scale, vs, 8, dev));
+    }
+    return MBX_OK;
+}
+
+MBX_API int mbx_gated_residual_ln_modulate_fp8(const mbx_view* residual_out, const mbx_view* out,
+                                               const mbx_view* out_fp8, const mbx_cview* residual,
+                                               const mbx_cview* gate, const mbx_cview* update,
+                                               const mbx_cview* bias, const mbx_cview* scale,
+                                               const mbx_cview* shift, const float* fp8_scale,
+                                               float eps, int variant, void* stream) {
+    MBX_TRY(mbx_check_gated_residual_ln_modulate_fp8(residual_out, out, out_fp8, residual, gate, update,
+                                                     bias, scale, shift, fp8_scale, eps, variant));
+    mbx::LnModParams p = gated_params(residual_out, out, residual, gate, update, bias, scale, shift, eps);
+    p.out_fp8 = static_cast<uint8_t*>(out_fp8->data);
+    p.out_fp8_stride = out_fp8->row_stride;
+    p.fp8_scale = fp8_scale;
+    const bool vec = gated_vec(p, residual_out, out, residual, gate, update, bias, scale, shift) &&
+                     aligned8_fp8(out_fp8);
+    return cuda_status(mbx::launch_gated_residual_ln_modulate_fp8(p, vec, variant == MBX_HIGH, (cudaStream_t)stream));
+}
+
 MBX_API int mbx_check_modulation_table_add(const mbx_view* out, const mbx_cview* table,
                                            const mbx_cview* temb) {
     return check_modtable(out, table, temb, true);
@@ -627,29 +754,8 @@ MBX_API int mbx_gated_residual_ln_modulate(const mbx_view* residual_out, const m
                                            const mbx_cview* scale, const mbx_cview* shift,
                                            float eps, int variant, void* stream) {
     MBX_TRY(check_gated(residual_out, out, residual, gate, update, bias, scale, shift, eps, variant, true));
-    mbx::LnModParams p;
-    p.out = static_cast<uint16_t*>(out->data);
-    p.out_stride = out->row_stride;
-    p.x = static_cast<const uint16_t*>(residual->data);
-    p.x_stride = residual->row_stride;
-    p.scale = static_cast<const uint16_t*>(scale->data);
-    p.scale_stride = scale->row_stride;
-    p.shift = static_cast<const uint16_t*>(shift->data);
-    p.shift_stride = shift->row_stride;
-    p.rows = residual->rows;
-    p.D = (int)residual->cols;
-    p.seq = residual->rows / scale->rows;
-    p.eps = eps;
-    p.update = static_cast<const uint16_t*>(update->data);
-    p.update_stride = update->row_stride;
-    p.gate = static_cast<const uint16_t*>(gate->data);
-    p.gate_stride = gate->row_stride;
-    p.bias = bias ? static_cast<const uint16_t*>(bias->data) : nullptr;
-    p.res_out = static_cast<uint16_t*>(residual_out->data);
-    p.res_out_stride = residual_out->row_stride;
-    bool vec = p.D % 8 == 0 && aligned16(of(residual_out)) && aligned16(of(out)) && aligned16(of(residual)) &&
-               aligned16(of(gate)) && aligned16(of(update)) && aligned16(of(scale)) && aligned16(of(shift));
-    if (bias) vec = vec && aligned16(of(bias));
+    const mbx::LnModParams p = gated_params(residual_out, out, residual, gate, update, bias, scale, shift, eps);
+    const bool vec = gated_vec(p, residual_out, out, residual, gate, update, bias, scale, shift);
     return cuda_status(mbx::launch_gated_residual_ln_modulate(p, vec, variant == MBX_HIGH, (cudaStream_t)stream));
 }
 
@@ -697,7 +803,7 @@ MBX_API int mbx_qk_norm_rope_qkv_epilogue(const mbx_view* joint, const mbx_cview
 
 MBX_API int mbx_selftest(int which, unsigned long long* counts, void* stream) {
     if (!counts) return MBX_E_NULL;
-    if (which < 0 || which > 4) return MBX_E_ARG;
+    if (which < 0 || which > 5) return MBX_E_ARG;
     if (reinterpret_cast<uintptr_t>(counts) % 8) return MBX_E_ALIGN;
     MBX_TRY(raw_on_device(counts, 16));
     return cuda_status(mbx::launch_selftest(which, counts, (cudaStream_t)stream));

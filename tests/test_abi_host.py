@@ -199,7 +199,8 @@ def test_selftest_rejections(mbx):
     L = mbx.lib()
     assert L.mbx_selftest(0, None, None) == -1
     assert L.mbx_selftest(7, BASE, None) == -12
-    assert L.mbx_selftest(5, BASE, None) == -12
+    assert L.mbx_selftest(6, BASE, None) == -12
+    assert L.mbx_selftest(5, BASE, None) == -9  # a valid mode: only the device check refuses
     assert L.mbx_selftest(-1, BASE, None) == -12
     assert L.mbx_selftest(0, BASE + 4, None) == -7
 
@@ -291,3 +292,34 @@ def test_modulation_table_add_rejections(mbx):
     assert st(V(BASE + 2, 6 * rows, D, dtype=2), t, e) == -7         # f32 misaligned
     assert st(o, t, V(BASE + 0x800000, rows, 6 * D, 6 * D - 1)) == -6
     assert st(o, V(0, 6, D), e) == -1
+
+
+def test_fp8_producer_rejections(mbx):
+    L = mbx.lib()
+    rows, D = 8, 64
+    o, x = V(BASE, rows, D), V(BASE + 0x100000, rows, D)
+    sc, sh = V(BASE + 0x200000, 2, D), V(BASE + 0x300000, 2, D)
+    q = V(BASE + 0x400000, rows, D, dtype=3)
+    fs = ctypes.c_void_p(BASE + 0x500000)
+
+    def st(o, q, x, sc, sh, fs, eps=1e-6, variant=0):
+        a = L.mbx_check_ln_modulate_fp8(ref(o), ref(q), ref(x), ref(sc), ref(sh), fs, ctypes.c_float(eps), variant)
+        b = L.mbx_ln_modulate_fp8(ref(o), ref(q), ref(x), ref(sc), ref(sh), fs, ctypes.c_float(eps), variant, None)
+        assert a == b
+        return a
+
+    assert st(o, q, x, sc, sh, fs) == -9                                   # host checks pass
+    assert st(o, V(BASE + 0x400000, rows, D, dtype=1), x, sc, sh, fs) == -2  # fp8 output must be E4M3
+    assert st(o, V(BASE + 0x400000, rows, D - 8, dtype=3), x, sc, sh, fs) == -5
+    assert st(o, V(BASE + 0x100000 + 64, rows, D, dtype=3), x, sc, sh, fs) == -8  # over x
+    assert st(o, V(BASE + 0x40, rows, D, dtype=3), x, sc, sh, fs) == -8     # over out
+    assert st(o, q, x, sc, sh, None) == -1
+    assert st(o, q, x, sc, sh, ctypes.c_void_p(BASE + 0x500002)) == -7      # scale misaligned
+    assert st(o, q, x, sc, sh, fs, variant=5) == -11                         # the LN checks still apply
+    # the gated form runs both sets of checks
+    ro, u, g = V(BASE + 0x600000, rows, D), V(BASE + 0x700000, rows, D), V(BASE + 0x800000, 2, D)
+    args = [ref(ro), ref(o), ref(q), ref(x), ref(g), ref(u), None, ref(sc), ref(sh), fs, ctypes.c_float(1e-6), 0]
+    assert L.mbx_check_gated_residual_ln_modulate_fp8(*args) == -9
+    assert L.mbx_gated_residual_ln_modulate_fp8(*args, None) == -9
+    args[2] = ref(V(BASE + 0x700000, rows, D, dtype=3))                      # fp8 over the update
+    assert L.mbx_check_gated_residual_ln_modulate_fp8(*args) == -8
