@@ -510,6 +510,56 @@ def run_suite(args):
     return 0
 
 
+# ---------------------------------------------------------------- profiler drivers
+
+
+def run_profile_calls(args):
+    """Launch a fixed set of calls `--steps` times, untimed, for a profiler to
+    capture (the commands in profiles/ run these)."""
+    import torch
+
+    import modulation_bit_exact_gb300 as mbx
+    import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device=dev).manual_seed(0)
+    r = lambda *sh, std=1.0: (torch.randn(*sh, generator=g, device=dev) * std).to(torch.bfloat16)
+    calls = []
+    if args.profile_calls == "ln":  # ln_modulate on x [4,4352,3072]: 107 MB in, 107 MB out
+        d = synth.image_dit_block(batch=4, device=dev)
+        calls.append(lambda: mbx.ln_modulate(d["x"], d["scale"], d["shift"]))
+    elif args.profile_calls == "image":  # the bench kernels plus the fused gated LN, [8704, 3072]
+        x, y, res = r(8704, 3072), r(8704, 3072), r(8704, 3072)
+        sc, sh, gt, b = (r(2, 3072, std=0.1) for _ in range(4))
+        out, out2 = torch.empty_like(x), torch.empty_like(x)
+        calls += [lambda: mbx.ln_modulate(x, sc, sh, out=out),
+                  lambda: mbx.residual_gate_add(x, gt, y, out=out),
+                  lambda: mbx.gated_residual_ln_modulate(res, gt, y, sc, sh, bias=b, out=out, residual_out=out2)]
+    elif args.profile_calls == "next":  # QKV epilogue, gated LN, FP8 LN, modulation table
+        q = synth.qkv_epilogue_case(device=dev)
+        res, upd = r(8704, 3072), r(8704, 3072)
+        gt, sc, sh, b = (r(2, 3072, std=0.1) for _ in range(4))
+        out, out2 = torch.empty_like(res), torch.empty_like(res)
+        q8 = torch.empty(8704, 3072, dtype=torch.uint8, device=dev)
+        s8 = torch.tensor([0.02], device=dev)
+        table = torch.randn(6, 3072, generator=g, device=dev)
+        temb = r(4096, 6 * 3072)
+        tout = torch.empty(6, 4096, 3072, device=dev)
+        calls += [lambda: mbx.qk_norm_rope_qkv_epilogue(q["txt"], q["img"], 2, 24, 128, q["wq_txt"], q["wk_txt"],
+                                                        q["wq_img"], q["wk_img"], q["cos_txt"], q["sin_txt"],
+                                                        q["cos_img"], q["sin_img"]),
+                  lambda: mbx.gated_residual_ln_modulate(res, gt, upd, sc, sh, bias=b, out=out, residual_out=out2),
+                  lambda: mbx.ln_modulate_fp8(res, sc, sh, s8, out=out, out_fp8=q8),
+                  lambda: mbx.modulation_table_add(table, temb, out=tout)]
+    for _ in range(args.steps):
+        for c in calls:
+            c()
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"profile_calls": args.profile_calls, "rounds": args.steps, "calls_per_round": len(calls)}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -521,7 +571,11 @@ def main():
     ap.add_argument("--suite", action="store_true",
                     help="time every operation and variant on the configurations' shapes "
                          "(one JSON line per case) instead of the benchmark step")
+    ap.add_argument("--profile-calls", default=None, choices=["ln", "image", "next"],
+                    help="launch a fixed set of calls --steps times, untimed, for a profiler")
     args = ap.parse_args()
+    if args.profile_calls:
+        return run_profile_calls(args)
     if args.suite:
         return run_suite(args)
     if args.warmup < 3:
