@@ -122,6 +122,10 @@ struct QkvParams {
     const uint16_t *wq_txt, *wk_txt, *wq_img, *wk_img;
     const float *cos_txt, *sin_txt, *cos_img, *sin_img;
     float eps;
+    // -0.0f passed at run time: RoPE products are taken as fma(a, b, neg_zero),
+    // the correctly rounded product, which the compiler cannot contract with
+    // the sum that follows
+    float neg_zero = -0.0f;
     // filled by the launcher
     int hpasses;       // head passes per token
     FastDiv by_stot;   // token -> batch index

@@ -113,10 +113,9 @@ __global__ void __launch_bounds__(512) qkv_epilogue_kernel(QkvParams p) {
         const QkvUnit u = qkv_unit<HD>(p, tok);
         const int h = hp * slots + slot;
         const bool active = h < H;
-        auto dst = [&](int part) {
-            return p.joint + ((((u.b * 3 + part) * H + h) * s_tot + u.s) * HD) + l * kChunk;
-        };
-        if (active) st_v4(dst(2), xv);  // V: bit copy
+        uint16_t* const dst_q = p.joint + ((((u.b * 3) * H + h) * s_tot + u.s) * HD) + l * kChunk;
+        const int64_t part_out = (int64_t)H * s_tot * HD;  // between the Q, K and V planes
+        if (active) st_v4(dst_q + 2 * part_out, xv);  // V: bit copy
 
         const uint4 wq = ld_shared_row((u.txt ? p.wq_txt : p.wq_img) + l * kChunk);
         const uint4 wk = ld_shared_row((u.txt ? p.wk_txt : p.wk_img) + l * kChunk);
@@ -152,17 +151,21 @@ __global__ void __launch_bounds__(512) qkv_epilogue_kernel(QkvParams p) {
                 const float ms = lo_f(pack_rn(__fmul_rn(S, 1.0f / HD), 0.0f));
                 const float inner = lo_f(pack_rn(__fadd_rn(ms, p.eps), 0.0f));
                 const uint32_t r2 = bf16_bits(rstd_bf16(inner));
+                // pairs i and i+1 side by side in f32x2: each product is one
+                // correctly rounded fma(a, b, -0) (nz, a run-time -0), each
+                // sum or difference one rounded add
+                const u64 nz = f2(p.neg_zero, p.neg_zero);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t n = bmul(bmul(w_of(x, i), r2), w_of(w, i));
-                    const float c = i == 0 ? c4.x : i == 1 ? c4.y : i == 2 ? c4.z : c4.w;
-                    const float sn = i == 0 ? s4.x : i == 1 ? s4.y : i == 2 ? s4.z : s4.w;
-                    // two roundings per product, one per sum: scalar
-                    // intrinsics, never merged into a fused multiply-add
-                    const float n0 = lo_f(n), n1 = hi_f(n);
-                    const float o0 = __fsub_rn(__fmul_rn(n0, c), __fmul_rn(n1, sn));
-                    const float o1 = __fadd_rn(__fmul_rn(n0, sn), __fmul_rn(n1, c));
-                    w_set(o, i, pack_rn(o0, o1));
+                for (int i = 0; i < 4; i += 2) {
+                    const uint32_t na = bmul(bmul(w_of(x, i), r2), w_of(w, i));
+                    const uint32_t nb = bmul(bmul(w_of(x, i + 1), r2), w_of(w, i + 1));
+                    const u64 n0 = f2(lo_f(na), lo_f(nb)), n1 = f2(hi_f(na), hi_f(nb));
+                    const u64 c = i == 0 ? f2(c4.x, c4.y) : f2(c4.z, c4.w);
+                    const u64 sn = i == 0 ? f2(s4.x, s4.y) : f2(s4.z, s4.w);
+                    const u64 o0 = sub2(fma2(n0, c, nz), fma2(n1, sn, nz));
+                    const u64 o1 = add2(fma2(n0, sn, nz), fma2(n1, c, nz));
+                    w_set(o, i, pack_rn(f2lo(o0), f2lo(o1)));
+                    w_set(o, i + 1, pack_rn(f2hi(o0), f2hi(o1)));
                 }
             } else {
                 const float rstd = rsqrtf(S / (float)HD + p.eps);
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(512) qkv_epilogue_kernel(QkvParams p) {
                     w_set(o, i, pack_rn(fmaf(n0, c, -n1 * sn), fmaf(n0, sn, n1 * c)));
                 }
             }
-            if (active) st_v4(dst(part), o);
+            if (active) st_v4(dst_q + part * part_out, o);
         }
     }
 }
