@@ -243,7 +243,10 @@ __device__ __noinline__ WPair welford_chunk_exact(uint4 a, uint4 b, int k0, int 
 // once, between the fast division (every element plain) and the exact one,
 // so the lane pairs' dependency chains interleave.  `full` (every lane has
 // all J chunks) removes the per-step selects of the last chunk.
-template <class C, class RingT>
+// ROWCHECK: for full rows, decide fast-or-exact once for all of the thread's
+// chunks (measured faster for the unfused kernel at J = 1 and 3; slower at
+// even J and in the fused kernel, where the extra live chunks cost more).
+template <class C, bool ROWCHECK, class RingT>
 __device__ __forceinline__ void welford_stage(const RingT& ring, int s, int t, int nch, bool full,
                                               Wf (&L)[C::M], u64 nz) {
     if constexpr (C::M >= 2) {
@@ -251,6 +254,50 @@ __device__ __forceinline__ void welford_stage(const RingT& ring, int s, int t, i
         u64 mean[P], m2[P];
 #pragma unroll
         for (int p = 0; p < P; ++p) mean[p] = m2[p] = f2(0.0f, 0.0f);
+        if (ROWCHECK && full) {
+            // Common case: every lane has all J chunks.  One check for all of
+            // this thread's elements (the smallest exponent field over every
+            // chunk), then the fast division throughout, both lane pairs'
+            // chains interleaved.
+            uint4 A[C::J][P], B[C::J][P];
+            uint32_t lowest = 0xffffffffu;
+#pragma unroll
+            for (int j = 0; j < C::J; ++j)
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    const int ca = t + C::TPR * p + kLanes * j;
+                    A[j][p] = lds16(ring.at(s, 0, ca));
+                    B[j][p] = lds16(ring.at(s, 0, ca + C::TPR * P));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        lowest = min_u16x2(lowest, w_of(A[j][p], i) & 0x7f807f80u);
+                        lowest = min_u16x2(lowest, w_of(B[j][p], i) & 0x7f807f80u);
+                    }
+                }
+            const uint32_t lo = lowest & 0xffffu, hi = lowest >> 16;
+            if ((lo < hi ? lo : hi) >= 0x2180u) {
+                static_for<0, C::J>([&](auto jc) {
+                    constexpr int j = decltype(jc)::value;
+                    static_for<0, kChunk>([&](auto ec) {
+                        constexpr int e = decltype(ec)::value;
+                        constexpr int K = kChunk * j + e + 1;
+#pragma unroll
+                        for (int p = 0; p < P; ++p)
+                            welford_step2<K, false>(pair_elem(w_of(A[j][p], e / 2), w_of(B[j][p], e / 2), e & 1),
+                                                    mean[p], m2[p], nz);
+                    });
+                });
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    L[p].mean = f2lo(mean[p]);
+                    L[p].m2 = f2lo(m2[p]);
+                    L[p + P].mean = f2hi(mean[p]);
+                    L[p + P].m2 = f2hi(m2[p]);
+                    L[p].n = L[p + P].n = (float)(kChunk * C::J);
+                }
+                return;
+            }
+        }
         static_for<0, C::J>([&](auto jc) {
             constexpr int j = decltype(jc)::value;
             uint4 A[P], B[P];
@@ -474,7 +521,7 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
         if constexpr (!HIGH) {
             Wf L[C::M];
             const bool full = nch == kLanes * C::J;
-            welford_stage<C>(ring, cur, t, nch, full, L, f2(p.neg_zero, p.neg_zero));
+            welford_stage<C, !FUSED && (J == 1 || J == 3)>(ring, cur, t, nch, full, L, f2(p.neg_zero, p.neg_zero));
             const Wf s = full ? tree_reduce<C>(L, t, sm, bar_id, wf_combine_eq)
                               : tree_reduce<C>(L, t, sm, bar_id, wf_combine);
             mean = s.mean;
