@@ -274,6 +274,15 @@ __device__ __forceinline__ void st_v4(void* p, uint4 v) {
                  "r"(v.w)
                  : "memory");
 }
+// The hardware tanh (one MUFU operation; relative error about 2^-11, a small
+// fraction of a bfloat16 ulp): used only by the single-pass "high" variants,
+// whose contract is a bound on the error, not a rounding order.
+__device__ __forceinline__ float tanh_hw(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Two binary32 values to FP8 E4M3 (round to nearest even, finite overflow
 // and infinities saturate to +-448, NaN to 0x7F): `lo` in the low byte.
 __device__ __forceinline__ uint32_t e4m3x2(float hi, float lo) {

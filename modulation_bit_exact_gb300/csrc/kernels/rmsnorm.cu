@@ -12,7 +12,7 @@
 //                          tanh(g); out = bf16(r + bf16(tg * n))
 // (same digest, 实现拆解 item 2; "AI Agent 驱动的 SGLang Kernel 一等公民",
 // 163.com, 3.2: rmsnorm + tanh(gate)·x + residual).
-// High path: binary32 throughout (unrounded squares, rsqrt, tanhf, fused
+// High path: binary32 throughout (unrounded squares, rsqrt, the hardware tanh, fused
 // multiply-add) with one rounding at the output.
 #include "launch.h"
 #include "rowops.cuh"
@@ -200,8 +200,8 @@ __global__ void __launch_bounds__(kBlock) rmsnorm_tanh_residual_kernel(RmsTanhPa
                         uint32_t n = bmul(bmul(xw, r2), ww);
                         ow = badd(rw, bmul(tanh2(gw, tab), n));
                     } else {
-                        float y0 = fmaf(tanhf(lo_f(gw)), lo_f(xw) * rstd * lo_f(ww), lo_f(rw));
-                        float y1 = fmaf(tanhf(hi_f(gw)), hi_f(xw) * rstd * hi_f(ww), hi_f(rw));
+                        float y0 = fmaf(tanh_hw(lo_f(gw)), lo_f(xw) * rstd * lo_f(ww), lo_f(rw));
+                        float y1 = fmaf(tanh_hw(hi_f(gw)), hi_f(xw) * rstd * hi_f(ww), hi_f(rw));
                         ow = pack_rn(y0, y1);
                     }
                     w_set(o, i, ow);
@@ -426,8 +426,8 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeAr
                             const uint32_t tg = MODE == kRmsModStaged ? mw : tanh2(mw, tab);
                             ow = badd(rw, bmul(tg, n));
                         } else {
-                            ow = pack_rn(fmaf(tanhf(lo_f(mw)), lo_f(xw) * rstd * lo_f(ww), lo_f(rw)),
-                                         fmaf(tanhf(hi_f(mw)), hi_f(xw) * rstd * hi_f(ww), hi_f(rw)));
+                            ow = pack_rn(fmaf(tanh_hw(lo_f(mw)), lo_f(xw) * rstd * lo_f(ww), lo_f(rw)),
+                                         fmaf(tanh_hw(hi_f(mw)), hi_f(xw) * rstd * hi_f(ww), hi_f(rw)));
                         }
                     }
                     w_set(o, i, ow);
