@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
                                                    _i64, _p, _i64, _p, _i64, _i64, _f32],
                 "orc_f32_to_e4m3": [_p, _p, _i64],
                 "orc_quant_e4m3": [_p, _i64, _p, _i64, _i64, _i64, _f32],
+                "orc_f32_to_e2m1": [_p, _p, _i64],
+                "orc_quant_nvfp4": [_p, _i64, _p, _p, _i64, _i64, _i64, _f32],
                 "orc_modulation_table_add": [_p, _i64, _p, _i64, ctypes.c_int, _p, _i64,
                                              ctypes.c_int, _i64, _i64],
                 "orc_qkv_epilogue": [_p, _p, _i64, _i64, _p, _i64, _i64, _i64, _i64, _i64,
@@ -266,6 +268,36 @@ def quant_e4m3(y: np.ndarray, scale: float) -> np.ndarray:
     out = np.empty((rows, D), dtype=np.uint8)
     lib().orc_quant_e4m3(_ptr(out), D, _ptr(y2), ys, rows, D, float(scale))
     return out.reshape(y.shape)
+
+
+def f32_to_e2m1(v: np.ndarray) -> np.ndarray:
+    """binary32 -> FP4 E2M1 codes (one per byte): nearest, ties to even,
+    saturating to +-6, NaN -> +6."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    lib().orc_f32_to_e2m1(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def nvfp4_sf_shape(rows: int, D: int) -> tuple[int, int]:
+    """Bytes of the 128x4-swizzled scale buffer: rows padded to 128, blocks to 4."""
+    return ((rows + 127) // 128) * 128, ((D // 16 + 3) // 4) * 4
+
+
+def quant_nvfp4(y: np.ndarray, gs: float, sf_fill: int = 0) -> tuple[np.ndarray, np.ndarray]:
+    """NVFP4 copy of a bfloat16 output (tahou.com article, section
+    将FP8量化融合到前序算子, NVFP4 path; readings at orc_quant_nvfp4): returns
+    (packed E2M1 [rows, D/2] uint8, swizzled E4M3 scales, flat, padding =
+    sf_fill)."""
+    y2, ys = _rows(y)
+    rows, D = y2.shape
+    if D % 16:
+        raise ValueError("D must be a multiple of 16")
+    out = np.empty((rows, D // 2), dtype=np.uint8)
+    mp, kp = nvfp4_sf_shape(rows, D)
+    sf = np.full(mp * kp, sf_fill, dtype=np.uint8)
+    lib().orc_quant_nvfp4(_ptr(out), D // 2, _ptr(sf), _ptr(y2), ys, rows, D, float(gs))
+    return out, sf
 
 
 def modulation_table_add(table: np.ndarray, temb: np.ndarray) -> np.ndarray:

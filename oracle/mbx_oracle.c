@@ -24,6 +24,11 @@
  *             quantisation into the producer): LayerNorm/AdaLN and gated
  *             residual + LayerNorm/AdaLN write a BF16 output and its static
  *             (per-tensor scale) E4M3 copy.
+ *   [FP4]     tahou.com article, section 将FP8量化融合到前序算子, last part (the
+ *             NVFP4 path): the gated residual + LN + modulate chain ending in
+ *             fp4_quantize, writing packed E2M1 values and 128x4-swizzled E4M3
+ *             block scales.  The block-scale rule and the swizzle are not on
+ *             the pages; the readings are stated at orc_quant_nvfp4.
  *   [WAN]     tahou.com article, section Wan视频模型的数据搬运优化 (Wan data
  *             movement): the per-token modulation table
  *             (table.unsqueeze(0) + temb.float()).chunk(6, dim=2), written as six
@@ -370,6 +375,16 @@ static uint8_t e4m3_of(float v) {
     return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | (uint8_t)((int)q - 8));
 }
 
+/* The value of an E4M3 code (NaN for 0x7F/0xFF). */
+static float e4m3_value(uint8_t c) {
+    const int e = (c >> 3) & 0xf, m = c & 7;
+    float v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexpf((float)m, -9);
+    else v = ldexpf((float)(8 + m), e - 10);
+    return (c & 0x80) ? -v : v;
+}
+
 void orc_f32_to_e4m3(const float* in, uint8_t* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = e4m3_of(in[i]);
 }
@@ -383,6 +398,89 @@ void orc_quant_e4m3(uint8_t* out, int64_t out_stride, const uint16_t* y, int64_t
     const float inv = 1.0f / scale;
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t e = 0; e < D; ++e) out[r * out_stride + e] = e4m3_of(f_of(y[r * y_stride + e]) * inv);
+}
+
+/* ------------------------------------------------------------------------ */
+/* NVFP4 quantisation [FP4]                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* binary32 -> FP4 E2M1 code (1 sign bit, 2 exponent bits with bias 1, 1
+ * mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; no infinity or NaN).
+ * Nearest on the exact value, ties to the even code (mantissa 0); beyond 6
+ * (and +-inf) saturates to +-6; NaN gives +6 (0x7).  Signed zero kept. */
+static uint8_t e2m1_of(float v) {
+    uint32_t u;
+    memcpy(&u, &v, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7;
+    const uint8_t sign = (uint8_t)((u >> 28) & 0x8u);
+    const float a = fabsf(v);
+    /* the eight magnitudes and the midpoints between neighbours; at a midpoint
+     * the code with mantissa bit 0 (even) wins */
+    static const float mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+    uint8_t code = 7;
+    for (uint8_t c = 0; c < 7; ++c) {
+        const float mid = (mag[c] + mag[c + 1]) * 0.5f; /* exact: few significant bits */
+        if (a < mid || (a == mid && (c & 1u) == 0)) {
+            code = c;
+            break;
+        }
+    }
+    return (uint8_t)(sign | code);
+}
+
+void orc_f32_to_e2m1(const float* in, uint8_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e2m1_of(in[i]);
+}
+
+/* Byte offset of the scale of (row r, block b) in the 128x4-swizzled layout:
+ * the [rows, D/16] scale matrix is cut into tiles of 128 rows x 4 blocks (512
+ * bytes, tiles in row-major order over the padded matrix); inside a tile, row
+ * r sits in one of four 32-row bands, and (r mod 32, band, b mod 4) are laid
+ * out in that order (16 bytes per r mod 32). */
+int64_t orc_nvfp4_sf_offset(int64_t r, int64_t b, int64_t blocks_per_row) {
+    const int64_t col_tiles = (blocks_per_row + 3) / 4;
+    const int64_t tile = (r / 128) * col_tiles + b / 4;
+    return tile * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (b % 4);
+}
+
+/* NVFP4 copy of a bfloat16 output y [rows, D] (D a multiple of 16), with the
+ * per-tensor global scale gs (the factor that maps the tensor's range onto
+ * E2M1 x E4M3, e.g. 448*6/amax).  Readings (the pages name the output only):
+ *   block      16 consecutive elements of a row; amax = max |y| over them
+ *   scale      s = e4m3(RN(RN(amax * gs) / 6))           (one E4M3 byte)
+ *   elements   q = e2m1(RN(y * RN(gs / float(s))))      (s > 0)
+ *              q = 0 for every element of a block whose s is zero
+ *   packing    out_fp4[r][i] = q[2i] | q[2i+1] << 4
+ *   scales     at orc_nvfp4_sf_offset(r, block); padding bytes untouched
+ * Every division and product is one correctly rounded binary32 operation. */
+void orc_quant_nvfp4(uint8_t* out_fp4, int64_t fp4_stride, uint8_t* out_sf, const uint16_t* y,
+                     int64_t y_stride, int64_t rows, int64_t D, float gs) {
+    const int64_t blocks = D / 16;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < blocks; ++b) {
+            const uint16_t* blk = y + r * y_stride + b * 16;
+            float amax = 0.0f; /* a NaN anywhere makes amax NaN */
+            for (int i = 0; i < 16; ++i) {
+                const float a = fabsf(f_of(blk[i]));
+                if (a != a || amax != amax) amax = NAN;
+                else if (a > amax) amax = a;
+            }
+            const float sf = (amax * gs) / 6.0f;
+            const uint8_t s = e4m3_of(sf);
+            out_sf[orc_nvfp4_sf_offset(r, b, blocks)] = s;
+            const float sv = e4m3_value(s);
+            uint8_t* dst = out_fp4 + r * fp4_stride + b * 8;
+            for (int i = 0; i < 8; ++i) {
+                uint8_t lo = 0, hi = 0;
+                if (sv != 0.0f) {
+                    const float esc = gs / sv;
+                    lo = e2m1_of(f_of(blk[2 * i]) * esc);
+                    hi = e2m1_of(f_of(blk[2 * i + 1]) * esc);
+                }
+                dst[i] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    }
 }
 
 /* ------------------------------------------------------------------------ */

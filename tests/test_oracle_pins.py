@@ -697,3 +697,97 @@ def test_quant_e4m3_of_a_bf16_output(orc):
         inr = np.abs(prod) < 448
         assert np.array_equal(got[inr], _torch_e4m3(prod[inr]))
         assert np.all(got[~inr] == np.where(prod[~inr] > 0, 0x7E, 0xFE))  # saturated
+
+
+# ------------------------------------------------------------ NVFP4
+
+_E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _e2m1_brute(v: float) -> int:
+    """Nearest of the 16 codes in binary64, ties to the code with mantissa 0."""
+    if v != v:
+        return 0x7
+    a = min(abs(v), 6.0)
+    best = min(range(8), key=lambda c: (abs(_E2M1[c] - a), c & 1))
+    return (0x8 if math.copysign(1.0, v) < 0 else 0) | best
+
+
+def test_e2m1_brute_force(orc):
+    rng = np.random.default_rng(11)
+    v = np.concatenate([rng.uniform(-8, 8, 20000), rng.standard_normal(5000) * 0.3,
+                        (_E2M1[:-1] + _E2M1[1:]) / 2, -(_E2M1[:-1] + _E2M1[1:]) / 2, _E2M1, -_E2M1,
+                        [1e30, -1e30, np.inf, -np.inf, 6.0001, 1e-40]]).astype(np.float32)
+    got = orc.f32_to_e2m1(v)
+    want = np.array([_e2m1_brute(float(x)) for x in v], np.uint8)
+    assert np.array_equal(got, want)
+    assert orc.f32_to_e2m1(np.array([-0.0], np.float32))[0] == 0x8
+
+
+def _swizzle_by_reshape(S: np.ndarray) -> np.ndarray:
+    """The 128x4 tile layout by array reshaping (independent of the scalar
+    index formula): rows -> (tile, band of 32, row in band), blocks -> (tile,
+    column), ordered (row tile, column tile, row in band, band, column)."""
+    mp, kp = S.shape
+    return S.reshape(mp // 128, 4, 32, kp // 4, 4).transpose(0, 3, 2, 1, 4).reshape(-1)
+
+
+def _unswizzle_by_reshape(sf: np.ndarray, mp: int, kp: int) -> np.ndarray:
+    return sf.reshape(mp // 128, kp // 4, 32, 4, 4).transpose(0, 3, 2, 1, 4).reshape(mp, kp)
+
+
+def _nvfp4_reference_scales(y: np.ndarray, gs: float, orc) -> np.ndarray:
+    f = (y.astype(np.uint32) << 16).view(np.float32)
+    rows, D = f.shape
+    amax = np.abs(f.reshape(rows, D // 16, 16)).max(axis=2)
+    sf = ((amax.astype(np.float32) * np.float32(gs)).astype(np.float32) / np.float32(6)).astype(np.float32)
+    return orc.f32_to_e4m3(sf)
+
+
+def test_nvfp4_scales_and_swizzle(orc):
+    g = torch.Generator().manual_seed(91)
+    for rows, D in ((130, 256), (5, 64), (256, 1024)):
+        y = u16((torch.randn(rows, D, generator=g) * 2).to(torch.bfloat16))
+        gs = 448.0 * 6.0 / 9.0
+        q, sf = orc.quant_nvfp4(y, gs, sf_fill=0xAB)
+        mp, kp = orc.nvfp4_sf_shape(rows, D)
+        S = np.full((mp, kp), 0xAB, np.uint8)
+        S[:rows, :D // 16] = _nvfp4_reference_scales(y, gs, orc)
+        assert np.array_equal(sf, _swizzle_by_reshape(S))
+
+
+def test_nvfp4_elements_decode_close_and_block_max_is_six(orc):
+    g = torch.Generator().manual_seed(92)
+    rows, D = 64, 512
+    y = u16((torch.randn(rows, D, generator=g) * 3).to(torch.bfloat16))
+    gs = 448.0 * 6.0 / 12.0
+    q, sf = orc.quant_nvfp4(y, gs)
+    codes = np.stack([q & 0xF, q >> 4], axis=-1).reshape(rows, D)
+    mag = _E2M1[codes & 7] * np.where(codes & 8, -1.0, 1.0)
+    Sm = _unswizzle_by_reshape(sf, *orc.nvfp4_sf_shape(rows, D))[:rows, :D // 16]
+    sval = torch.from_numpy(Sm.copy()).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    scale = np.repeat(sval, 16, axis=1) / gs
+    f = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    deq = mag * scale
+    step = np.repeat(sval, 16, axis=1) / gs  # 1 E2M1 unit at the top binade is 2 * scale
+    assert np.all(np.abs(deq - f) <= 1.0 * step + 1e-30)
+    fb = np.abs(f).reshape(rows, D // 16, 16)
+    cb = (codes & 7).reshape(rows, D // 16, 16)
+    top = cb[np.arange(rows)[:, None], np.arange(D // 16)[None, :], fb.argmax(axis=2)]
+    assert np.all(top == 7)  # the block's largest magnitude maps to +-6
+
+
+def test_nvfp4_zero_block_and_exact_values(orc):
+    rows, D = 2, 32
+    vals = np.array([6, 4, 3, 2, 1.5, 1, 0.5, 0, -6, -4, -3, -2, -1.5, -1, -0.5, -0.0], np.float32)
+    y = np.zeros((rows, D), np.float32)
+    y[0, :16] = vals * 2.0  # block amax 12: scale 12 * gs / 6 = 2 * gs; gs = 0.5 -> s = 1.0 exactly
+    y[1, 16:] = vals
+    yb = orc.f32_to_bf16(y)
+    q, sf = orc.quant_nvfp4(yb, 0.5)
+    codes = np.stack([q & 0xF, q >> 4], axis=-1).reshape(rows, D)
+    want = orc.f32_to_e2m1(vals)
+    assert np.array_equal(codes[0, :16], want)
+    assert np.all(codes[0, 16:] == 0) and np.all(codes[1, :16] == 0)  # zero blocks
+    S = _unswizzle_by_reshape(sf, *orc.nvfp4_sf_shape(rows, D))
+    assert S[0, 0] == 0x38 and S[0, 1] == 0 and S[1, 0] == 0  # 1.0 in E4M3; zero blocks: scale 0
