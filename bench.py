@@ -437,7 +437,10 @@ def run_suite(args):
                         b=r(1, D, std=0.5), out=torch.empty(rows, D, dtype=torch.bfloat16, device=dev),
                         out2=torch.empty(rows, D, dtype=torch.bfloat16, device=dev),
                         q=torch.empty(rows, D, dtype=torch.uint8, device=dev),
-                        s8=torch.full((1,), 0.02, dtype=torch.float32, device=dev))
+                        s8=torch.full((1,), 0.02, dtype=torch.float32, device=dev),
+                        q4=torch.empty(rows, D // 2, dtype=torch.uint8, device=dev),
+                        sf4=torch.zeros(mbx.nvfp4_sf_shape(rows, D), dtype=torch.uint8, device=dev),
+                        g4=torch.full((1,), 60.0, dtype=torch.float32, device=dev))
         T = rows * D * 2
         M = mrows * D * 2
         ops = {
@@ -452,6 +455,12 @@ def run_suite(args):
             "gated_residual_ln_modulate_fp8": (4 * T + 3 * M + D * 2 + T // 2, lambda s, v: mbx.gated_residual_ln_modulate_fp8(
                 s["res"], s["g"], s["y"], s["sc"], s["sh"], s["s8"], bias=s["b"], variant=v, out=s["out"],
                 residual_out=s["out2"], out_fp8=s["q"])),
+            "ln_modulate_nvfp4": (2 * T + 2 * M + T // 4 + T // 32, lambda s, v: mbx.ln_modulate_nvfp4(
+                s["x"], s["sc"], s["sh"], s["g4"], variant=v, out=s["out"], out_fp4=s["q4"], out_sf=s["sf4"])),
+            "gated_residual_ln_modulate_nvfp4": (4 * T + 3 * M + D * 2 + T // 4 + T // 32,
+                                                 lambda s, v: mbx.gated_residual_ln_modulate_nvfp4(
+                s["res"], s["g"], s["y"], s["sc"], s["sh"], s["g4"], bias=s["b"], variant=v, out=s["out"],
+                residual_out=s["out2"], out_fp4=s["q4"], out_sf=s["sf4"])),
         }
         for op, (nb, fn) in ops.items():
             for v in ("lossless", "high"):

@@ -61,8 +61,10 @@ extern "C" {
 
 /* dtype codes.  Every operation takes bfloat16 operands, except that the
  * modulation-table add also accepts binary32 inputs and writes binary32, and
- * the FP8 producers write an extra FP8 E4M3 (one byte per element) output. */
-enum { MBX_BF16 = 1, MBX_F32 = 2, MBX_E4M3 = 3 };
+ * the FP8 producers write an extra FP8 E4M3 (one byte per element) output and
+ * the NVFP4 producers packed FP4 E2M1 pairs (MBX_E2M1X2, one byte per two
+ * elements) with E4M3 block scales. */
+enum { MBX_BF16 = 1, MBX_F32 = 2, MBX_E4M3 = 3, MBX_E2M1X2 = 4 };
 
 /* variant codes */
 enum { MBX_LOSSLESS = 0, MBX_HIGH = 1 };
@@ -210,6 +212,37 @@ MBX_API int mbx_gated_residual_ln_modulate_fp8(const mbx_view* residual_out, con
                                                float eps, int variant, void* stream);
 
 /*
+ * NVFP4 producers: the two LayerNorm + AdaLN entry points with an NVFP4 copy of
+ * the bf16 output -- packed E2M1 values and E4M3 block scales.
+ * Defined in: tahou.com SGLang diffusion article, section 将FP8量化融合到前序算子,
+ * NVFP4 part -- the gated residual + layer_norm + (1 + scale)/shift chain
+ * ending in fp4_quantize, writing E2M1 packed values and 128x4-swizzled E4M3
+ * scales in one kernel.  The pages name the output, not the rule; this
+ * library's rule (every operation a correctly rounded binary32 operation):
+ *   blocks  16 consecutive elements of a row of out; amax = max |out| (NaN
+ *           propagates)
+ *   scale   s = e4m3(RN(RN(amax * gs) / 6)), gs = *fp4_scale, the per-tensor
+ *           global scale (e.g. 448*6 / tensor amax), read on the stream
+ *   values  q = e2m1(RN(out * RN(gs / value(s)))), nearest, ties to the code
+ *           with mantissa 0, saturating to +-6 (cvt.rn.satfinite; checked by
+ *           mbx_selftest(6)); every q of a block whose s is 0 is 0
+ *   out_fp4 MBX_E2M1X2 [rows, D/2]: byte i of a row = q[2i] | q[2i+1] << 4
+ *   out_sf  MBX_E4M3 [pad128(rows), pad4(D/16)], contiguous: the block scale of
+ *           (row r, block b) at byte ((r/128)*(cols/4) + b/4)*512 + (r%32)*16 +
+ *           ((r%128)/32)*4 + b%4 (tiles of 128 rows x 4 blocks); padding bytes
+ *           are not written
+ * D must be a multiple of 16.  No output overlaps another output or an input.
+ */
+MBX_API int mbx_ln_modulate_nvfp4(const mbx_view* out, const mbx_view* out_fp4, const mbx_view* out_sf,
+                                  const mbx_cview* x, const mbx_cview* scale, const mbx_cview* shift,
+                                  const float* fp4_scale, float eps, int variant, void* stream);
+MBX_API int mbx_gated_residual_ln_modulate_nvfp4(
+    const mbx_view* residual_out, const mbx_view* out, const mbx_view* out_fp4, const mbx_view* out_sf,
+    const mbx_cview* residual, const mbx_cview* gate, const mbx_cview* update, const mbx_cview* bias,
+    const mbx_cview* scale, const mbx_cview* shift, const float* fp4_scale, float eps, int variant,
+    void* stream);
+
+/*
  * Per-token modulation table, written in the (6, rows, D) layout.
  * Defined in: tahou.com SGLang diffusion article, section
  * Wan视频模型的数据搬运优化 -- the eager (table.unsqueeze(0) + temb.float())
@@ -280,6 +313,14 @@ MBX_API int mbx_check_gated_residual_ln_modulate_fp8(
     const mbx_cview* residual, const mbx_cview* gate, const mbx_cview* update,
     const mbx_cview* bias, const mbx_cview* scale, const mbx_cview* shift,
     const float* fp8_scale, float eps, int variant);
+MBX_API int mbx_check_ln_modulate_nvfp4(const mbx_view* out, const mbx_view* out_fp4,
+                                        const mbx_view* out_sf, const mbx_cview* x,
+                                        const mbx_cview* scale, const mbx_cview* shift,
+                                        const float* fp4_scale, float eps, int variant);
+MBX_API int mbx_check_gated_residual_ln_modulate_nvfp4(
+    const mbx_view* residual_out, const mbx_view* out, const mbx_view* out_fp4, const mbx_view* out_sf,
+    const mbx_cview* residual, const mbx_cview* gate, const mbx_cview* update, const mbx_cview* bias,
+    const mbx_cview* scale, const mbx_cview* shift, const float* fp4_scale, float eps, int variant);
 MBX_API int mbx_check_modulation_table_add(const mbx_view* out, const mbx_cview* table,
                                            const mbx_cview* temb);
 MBX_API int mbx_check_gated_residual_ln_modulate(const mbx_view* residual_out,
@@ -313,7 +354,12 @@ MBX_API int mbx_check_qk_norm_rope_qkv_epilogue(
  *   which = 5: the hardware binary32 -> FP8 E4M3 conversion used by the FP8
  *              producers vs the E4M3 definition (nearest even, saturation
  *              to +-448, NaN -> 0x7F) for every binary32 pattern; the second
- *              counter holds NaN inputs whose byte is not 0x7F.
+ *              counter holds NaN inputs whose byte is not 0x7F;
+ *   which = 6: the hardware binary32 -> FP4 E2M1 conversion used by the
+ *              NVFP4 producers vs the E2M1 definition (nearest, ties to the
+ *              code with mantissa 0, saturation to +-6) for every binary32
+ *              pattern; the second counter holds NaN inputs whose code is
+ *              not 0x7.
  * counts: device pointer to 2 uint64 counters (caller-owned), overwritten
  * with {mismatches between non-NaN results, mismatches where either is NaN}.
  * Enqueued on `stream`; the caller synchronises before reading counts.

@@ -26,7 +26,9 @@ __all__ = [
     "ln_modulate", "rmsnorm_scale", "rmsnorm_tanh_residual", "residual_gate_add",
     "qk_norm_rope_qkv_epilogue", "gated_residual_ln_modulate", "check_gated_residual_ln_modulate",
     "modulation_table_add", "check_modulation_table_add", "ln_modulate_fp8", "check_ln_modulate_fp8",
-    "gated_residual_ln_modulate_fp8", "check_gated_residual_ln_modulate_fp8",
+    "gated_residual_ln_modulate_fp8", "check_gated_residual_ln_modulate_fp8", "ln_modulate_nvfp4",
+    "check_ln_modulate_nvfp4", "gated_residual_ln_modulate_nvfp4", "check_gated_residual_ln_modulate_nvfp4",
+    "nvfp4_sf_shape",
     "check_ln_modulate", "check_rmsnorm_scale",
     "check_rmsnorm_tanh_residual", "check_residual_gate_add",
     "check_qk_norm_rope_qkv_epilogue", "selftest", "status_string", "MbxError",
@@ -34,7 +36,7 @@ __all__ = [
 ]
 
 LOSSLESS, HIGH = 0, 1
-MBX_BF16, MBX_F32, MBX_E4M3 = 1, 2, 3
+MBX_BF16, MBX_F32, MBX_E4M3, MBX_E2M1X2 = 1, 2, 3, 4
 _VARIANTS = {"lossless": LOSSLESS, "high": HIGH, LOSSLESS: LOSSLESS, HIGH: HIGH}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -90,6 +92,10 @@ def _load() -> ctypes.CDLL:
             "mbx_check_ln_modulate_fp8": [_P, _P, _P, _P, _P, _vp, _f32, _int],
             "mbx_gated_residual_ln_modulate_fp8": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _vp, _f32, _int, _vp],
             "mbx_check_gated_residual_ln_modulate_fp8": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _vp, _f32, _int],
+            "mbx_ln_modulate_nvfp4": [_P, _P, _P, _P, _P, _P, _vp, _f32, _int, _vp],
+            "mbx_check_ln_modulate_nvfp4": [_P, _P, _P, _P, _P, _P, _vp, _f32, _int],
+            "mbx_gated_residual_ln_modulate_nvfp4": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _vp, _f32, _int, _vp],
+            "mbx_check_gated_residual_ln_modulate_nvfp4": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _vp, _f32, _int],
             "mbx_modulation_table_add": [_P, _P, _P, _vp],
             "mbx_check_modulation_table_add": [_P, _P, _P],
             "mbx_gated_residual_ln_modulate": [_P, _P, _P, _P, _P, _P, _P, _P, _f32, _int, _vp],
@@ -297,6 +303,76 @@ def check_gated_residual_ln_modulate_fp8(residual_out, out, out_fp8, residual, g
         _ref(_view(residual_out)), _ref(_view(out)), _ref(_view(out_fp8)), _ref(_view(residual)),
         _ref(_view(gate)), _ref(_view(update)), None if b is None else _ref(b), _ref(_view(scale)),
         _ref(_view(shift)), _ptr(fp8_scale), eps, _variant(variant))
+
+
+def nvfp4_sf_shape(rows: int, D: int) -> tuple[int, int]:
+    """Shape of the NVFP4 block-scale buffer: rows padded to 128, blocks of 16
+    padded to 4 (the 128x4 tile layout)."""
+    return (rows + 127) // 128 * 128, (D // 16 + 3) // 4 * 4
+
+
+def _fp4_views(x: torch.Tensor, out_fp4, out_sf):
+    D = x.shape[-1]
+    rows = x.numel() // D
+    if out_fp4 is None:
+        out_fp4 = torch.empty((rows, D // 2), dtype=torch.uint8, device=x.device)
+    if out_sf is None:
+        out_sf = torch.zeros(nvfp4_sf_shape(rows, D), dtype=torch.uint8, device=x.device)
+    q, f = _view(out_fp4), _view(out_sf)
+    q.dtype, f.dtype = MBX_E2M1X2, MBX_E4M3
+    return out_fp4, out_sf, q, f
+
+
+def ln_modulate_nvfp4(x, scale, shift, fp4_scale, eps: float = 1e-6, variant="lossless", out=None,
+                      out_fp4=None, out_sf=None):
+    """LN + AdaLN modulate writing the bf16 result and its NVFP4 copy (packed
+    E2M1 [rows, D/2] uint8, E4M3 block scales in the 128x4 tile layout; see
+    mbx_ln_modulate_nvfp4).  fp4_scale: one-element float32 CUDA tensor (the
+    global scale).  Returns (out, out_fp4, out_sf)."""
+    L = _load()
+    out = _empty_like_rows(x) if out is None else out
+    out_fp4, out_sf, q, f = _fp4_views(x, out_fp4, out_sf)
+    o, xv, sc, sh = _view(out), _view(x), _view(scale), _view(shift)
+    _raise(L.mbx_ln_modulate_nvfp4(_ref(o), _ref(q), _ref(f), _ref(xv), _ref(sc), _ref(sh), _ptr(fp4_scale), eps,
+                                   _variant(variant), _stream(x)))
+    return out, out_fp4, out_sf
+
+
+def check_ln_modulate_nvfp4(out, out_fp4, out_sf, x, scale, shift, fp4_scale, eps=1e-6, variant="lossless") -> int:
+    q, f = _view(out_fp4), _view(out_sf)
+    q.dtype, f.dtype = MBX_E2M1X2, MBX_E4M3
+    return _load().mbx_check_ln_modulate_nvfp4(_ref(_view(out)), _ref(q), _ref(f), _ref(_view(x)),
+                                               _ref(_view(scale)), _ref(_view(shift)), _ptr(fp4_scale), eps,
+                                               _variant(variant))
+
+
+def gated_residual_ln_modulate_nvfp4(residual, gate, update, scale, shift, fp4_scale, bias=None,
+                                     eps: float = 1e-6, variant="lossless", out=None, residual_out=None,
+                                     out_fp4=None, out_sf=None):
+    """Gated residual + LN + AdaLN modulate writing r', the bf16 result and its
+    NVFP4 copy.  Returns (residual_out, out, out_fp4, out_sf)."""
+    L = _load()
+    out = _empty_like_rows(residual) if out is None else out
+    residual_out = _empty_like_rows(residual) if residual_out is None else residual_out
+    out_fp4, out_sf, q, f = _fp4_views(residual, out_fp4, out_sf)
+    ro, o = _view(residual_out), _view(out)
+    r, g, u, sc, sh = _view(residual), _view(gate), _view(update), _view(scale), _view(shift)
+    b = None if bias is None else _view(bias)
+    _raise(L.mbx_gated_residual_ln_modulate_nvfp4(_ref(ro), _ref(o), _ref(q), _ref(f), _ref(r), _ref(g), _ref(u),
+                                                  None if b is None else _ref(b), _ref(sc), _ref(sh),
+                                                  _ptr(fp4_scale), eps, _variant(variant), _stream(residual)))
+    return residual_out, out, out_fp4, out_sf
+
+
+def check_gated_residual_ln_modulate_nvfp4(residual_out, out, out_fp4, out_sf, residual, gate, update, scale,
+                                           shift, fp4_scale, bias=None, eps=1e-6, variant="lossless") -> int:
+    q, f = _view(out_fp4), _view(out_sf)
+    q.dtype, f.dtype = MBX_E2M1X2, MBX_E4M3
+    b = None if bias is None else _view(bias)
+    return _load().mbx_check_gated_residual_ln_modulate_nvfp4(
+        _ref(_view(residual_out)), _ref(_view(out)), _ref(q), _ref(f), _ref(_view(residual)), _ref(_view(gate)),
+        _ref(_view(update)), None if b is None else _ref(b), _ref(_view(scale)), _ref(_view(shift)),
+        _ptr(fp4_scale), eps, _variant(variant))
 
 
 def modulation_table_add(table, temb, out=None):

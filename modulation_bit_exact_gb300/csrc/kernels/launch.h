@@ -36,7 +36,28 @@ struct LnModParams {
     uint8_t* out_fp8 = nullptr;
     int64_t out_fp8_stride = 0;
     const float* fp8_scale = nullptr;  // device, one per-tensor scale
+    // NVFP4 copy of out (16-element blocks): packed E2M1 [rows, D/2] bytes and
+    // E4M3 block scales in the 128x4 tile layout (sf_col_tiles tiles per row band)
+    uint8_t* out_fp4 = nullptr;
+    int64_t out_fp4_stride = 0;
+    uint8_t* out_sf = nullptr;
+    int sf_col_tiles = 0;
+    const float* fp4_scale = nullptr;  // device, the per-tensor global scale
 };
+
+// NVFP4 copy of a bf16 matrix (the same definition as the LN kernel's store).
+struct QuantFp4Params {
+    uint8_t* out;
+    int64_t out_stride;
+    uint8_t* sf;
+    int sf_col_tiles;
+    const uint16_t* y;
+    int64_t y_stride;
+    int64_t rows;
+    int D;
+    const float* gs;
+};
+cudaError_t launch_quant_nvfp4(const QuantFp4Params& p, cudaStream_t s);
 
 // Static E4M3 copy of a bf16 matrix: out[r][e] = e4m3(y[r][e] * (1/scale)).
 struct QuantParams {
@@ -174,6 +195,8 @@ cudaError_t launch_residual_gate_add(const GateAddParams& p, bool vec, bool high
 cudaError_t launch_gated_residual_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_gated_residual_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cudaStream_t s);
+cudaError_t launch_ln_modulate_nvfp4(const LnModParams& p, bool vec, bool high, cudaStream_t s);
+cudaError_t launch_gated_residual_ln_modulate_nvfp4(const LnModParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_qkv_epilogue(const QkvParams& p, bool high, cudaStream_t s);
 cudaError_t launch_selftest(int which, unsigned long long* counts, cudaStream_t s);
 

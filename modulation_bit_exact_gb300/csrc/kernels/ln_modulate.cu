@@ -433,6 +433,7 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
     RowDiv next(first, groups, p.seq);  // modulation row of the next row to issue
     // FP8 producer: 1/scale correctly rounded, once per thread
     const float inv8 = p.out_fp8 != nullptr ? __fdiv_rn(1.0f, __ldg(p.fp8_scale)) : 0.0f;
+    const float gs4 = p.out_fp4 != nullptr ? __ldg(p.fp4_scale) : 0.0f;  // NVFP4 global scale
 
     auto issue = [&](int s, int64_t row) {
         ring.issue(s, 0, p.x + row * p.x_stride, t, nch);
@@ -575,7 +576,9 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
 #pragma unroll
             for (int m = 0; m < C::M; ++m) {
                 const int c = t + C::TPR * m + kLanes * j;
-                if (c >= nch) continue;
+                const bool valid = c < nch;
+                uint4 o = make_uint4(0, 0, 0, 0);
+                if (valid) {
                 const uint4 X = lds16(ring.at(cur, 0, c));
                 uint4 T, SH;
                 if constexpr (MODE == kModStaged) {
@@ -585,7 +588,6 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                     T = lds16(ring.at(cur, O::SC > 0 ? O::SC : 0, c));
                     SH = lds16(ring.at(cur, O::SH > 0 ? O::SH : 0, c));
                 }
-                uint4 o;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint32_t xw = w_of(X, i), tw = w_of(T, i), hw = w_of(SH, i);
@@ -605,6 +607,19 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                 if (p.out_fp8 != nullptr)
                     st_v2(p.out_fp8 + row * p.out_fp8_stride + (int64_t)c * kChunk, e4m3x4_of_bf16(o.x, o.y, inv8),
                           e4m3x4_of_bf16(o.z, o.w, inv8));
+                }
+                if (p.out_fp4 != nullptr) {
+                    // a 16-element block is chunks 2b and 2b+1, held by lanes
+                    // t and t^1 of the same warp (every lane takes part)
+                    const float a8 = valid ? amax8_bf16(o) : 0.0f;
+                    const float a16 = max_nan(a8, __shfl_xor_sync(0xffffffffu, a8, 1));
+                    float sv;
+                    const uint32_t sc = nvfp4_block_scale(a16, gs4, sv);
+                    if (valid) {
+                        st_u32(p.out_fp4 + row * p.out_fp4_stride + (int64_t)c * 4, nvfp4_codes(o, gs4, sv));
+                        if ((c & 1) == 0) p.out_sf[nvfp4_sf_offset(row, c >> 1, p.sf_col_tiles)] = (uint8_t)sc;
+                    }
+                }
             }
         cur = cur + 1 == NS ? 0 : cur + 1;
     }
@@ -738,6 +753,37 @@ cudaError_t launch_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cu
     q.out_fp8 = nullptr;
     cudaError_t e = launch_ln_modulate(q, false, high, s);
     return e != cudaSuccess ? e : quantise_out(p, s);
+}
+
+static cudaError_t quantise_out_fp4(const LnModParams& p, cudaStream_t s) {
+    QuantFp4Params q;
+    q.out = p.out_fp4;
+    q.out_stride = p.out_fp4_stride;
+    q.sf = p.out_sf;
+    q.sf_col_tiles = p.sf_col_tiles;
+    q.y = p.out;
+    q.y_stride = p.out_stride;
+    q.rows = p.rows;
+    q.D = p.D;
+    q.gs = p.fp4_scale;
+    return launch_quant_nvfp4(q, s);
+}
+
+cudaError_t launch_ln_modulate_nvfp4(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
+    if (vec) return launch_pipe_d<false>(p, high, s);
+    LnModParams q = p;
+    q.out_fp4 = nullptr;
+    cudaError_t e = launch_ln_modulate(q, false, high, s);
+    return e != cudaSuccess ? e : quantise_out_fp4(p, s);
+}
+
+cudaError_t launch_gated_residual_ln_modulate_nvfp4(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
+    if (vec && fused_fits(p)) return launch_pipe_d<true>(p, high, s);
+    if (vec) return launch_gated_residual_ln_modulate(p, true, high, s);  // composed; the LN pass writes the copy
+    LnModParams q = p;
+    q.out_fp4 = nullptr;
+    cudaError_t e = launch_gated_residual_ln_modulate(q, false, high, s);
+    return e != cudaSuccess ? e : quantise_out_fp4(p, s);
 }
 
 cudaError_t launch_gated_residual_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cudaStream_t s) {

@@ -21,6 +21,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <type_traits>
 
 namespace mbx {
@@ -299,6 +300,48 @@ __device__ __forceinline__ uint32_t e4m3x4_of_bf16(uint32_t w0, uint32_t w1, flo
     return a | (b << 16);
 }
 
+// Eight binary32 values to eight FP4 E2M1 codes (nearest, ties to even,
+// saturating; cvt.rn.satfinite.e2m1x2.f32), element 2i in the low nibble of
+// byte i.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
+    uint32_t d;
+    asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+        "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+        : "=r"(d)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return d;
+}
+
+// The value of an E4M3 code (exact, through the hardware conversion to f16).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+    uint32_t h2;
+    const uint16_t c = (uint16_t)(code & 0xffu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+}
+
+// max with NaN propagation (max.NaN.f32)
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+// Byte offset of the scale of (row r, block b) in the 128x4 tile layout of
+// NVFP4 block scales: tiles of 128 rows x 4 blocks (512 bytes) in row-major
+// order; inside a tile (r mod 32, (r mod 128) / 32, b mod 4) in that order.
+__device__ __forceinline__ int64_t nvfp4_sf_offset(int64_t r, int b, int col_tiles) {
+    return ((r >> 7) * col_tiles + (b >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (b & 3);
+}
+
+__device__ __forceinline__ void st_u32(void* p, uint32_t a) {
+    asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
+}
+
 __device__ __forceinline__ void st_v2(void* p, uint32_t a, uint32_t b) {
     asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }
@@ -320,6 +363,39 @@ __device__ __forceinline__ void w_set(uint4& v, int i, uint32_t w) {
     else if (i == 1) v.y = w;
     else if (i == 2) v.z = w;
     else v.w = w;
+}
+
+// |largest| of the eight bf16 values of a chunk, NaN propagating.
+__device__ __forceinline__ float amax8_bf16(const uint4& o) {
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t w = w_of(o, i);
+        a = max_nan(a, fabsf(lo_f(w)));
+        a = max_nan(a, fabsf(hi_f(w)));
+    }
+    return a;
+}
+
+// NVFP4 block step: from the block's amax and the global scale gs, the E4M3
+// block scale s = e4m3(RN(RN(amax * gs) / 6)) and its value.
+__device__ __forceinline__ uint32_t nvfp4_block_scale(float amax16, float gs, float& sv) {
+    const uint32_t s = e4m3x2(0.0f, __fdiv_rn(__fmul_rn(amax16, gs), 6.0f)) & 0xffu;
+    sv = e4m3_value(s);
+    return s;
+}
+
+// The eight E2M1 codes of a chunk, e2m1(RN(y * RN(gs / sv))); 0 when sv is 0.
+__device__ __forceinline__ uint32_t nvfp4_codes(const uint4& o, float gs, float sv) {
+    if (sv == 0.0f) return 0u;
+    const float esc = __fdiv_rn(gs, sv);
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __fmul_rn(lo_f(w_of(o, i)), esc);
+        v[2 * i + 1] = __fmul_rn(hi_f(w_of(o, i)), esc);
+    }
+    return e2m1x8(v);
 }
 
 }  // namespace mbx

@@ -112,4 +112,42 @@ cudaError_t launch_quant_e4m3(const QuantParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// NVFP4 copy of a bf16 matrix, one 16-element block per thread, any
+// alignment (the fallback of the NVFP4 producers).
+__global__ void __launch_bounds__(kBlock) quant_nvfp4_kernel(QuantFp4Params p) {
+    const float gs = __ldg(p.gs);
+    const int blocks = p.D / 16;
+    const int64_t total = p.rows * blocks;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / blocks;
+        const int b = (int)(i - r * blocks);
+        const uint16_t* y = p.y + r * p.y_stride + b * 16;
+        uint4 lo, hi;
+        uint32_t wv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) wv[k] = (uint32_t)ld_u16(y + 2 * k) | ((uint32_t)ld_u16(y + 2 * k + 1) << 16);
+        lo = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        hi = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+        float sv;
+        const uint32_t sc = nvfp4_block_scale(max_nan(amax8_bf16(lo), amax8_bf16(hi)), gs, sv);
+        const uint32_t q0 = nvfp4_codes(lo, gs, sv), q1 = nvfp4_codes(hi, gs, sv);
+        uint8_t* o = p.out + r * p.out_stride + b * 8;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            o[k] = (uint8_t)(q0 >> (8 * k));
+            o[4 + k] = (uint8_t)(q1 >> (8 * k));
+        }
+        p.sf[nvfp4_sf_offset(r, b, p.sf_col_tiles)] = (uint8_t)sc;
+    }
+}
+
+cudaError_t launch_quant_nvfp4(const QuantFp4Params& p, cudaStream_t s) {
+    const int64_t total = p.rows * (p.D / 16);
+    const int grid = grid_for_rows(reinterpret_cast<const void*>(quant_nvfp4_kernel), (total + kBlock - 1) / kBlock, 1, kBlock);
+    if (grid < 0) return cudaErrorUnknown;
+    quant_nvfp4_kernel<<<grid, kBlock, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace mbx

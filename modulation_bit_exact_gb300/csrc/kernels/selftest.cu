@@ -12,7 +12,11 @@
 //   5: the hardware binary32 -> E4M3 conversion of the FP8 producers
 //      (cvt.rn.satfinite.e4m3x2.f32) == the E4M3 definition (nearest even on
 //      the exact value, saturation to +-448, NaN -> 0x7F) for every binary32
-//      pattern; NaN inputs whose byte is not 0x7F are counted apart.
+//      pattern; NaN inputs whose byte is not 0x7F are counted apart;
+//   6: the hardware binary32 -> FP4 E2M1 conversion of the NVFP4 producers
+//      (cvt.rn.satfinite.e2m1x2.f32) == the E2M1 definition (nearest, ties to
+//      the code with mantissa 0, saturation to +-6) for every binary32
+//      pattern; NaN inputs whose code is not 0x7 are counted apart.
 // A mismatch where either result is a NaN is counted apart from the others:
 // NaN payloads never reach a bfloat16 output except as the canonical NaN.
 #include "launch.h"
@@ -123,6 +127,44 @@ __global__ void selftest_e4m3_kernel(unsigned long long* counts) {
     if (bad_nan) atomicAdd(&counts[1], bad_nan);
 }
 
+// E2M1 from its definition: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 (codes
+// 0..7); the decision points are the midpoints, each tie going to the code
+// whose mantissa bit is 0.
+__device__ uint32_t e2m1_by_definition(float v) {
+    const uint32_t u = __float_as_uint(v);
+    if (is_nan32(u)) return 0x7u;
+    const uint32_t sign = (u >> 28) & 0x8u;
+    const float a = fabsf(v);
+    uint32_t c;
+    if (a <= 0.25f) c = 0;
+    else if (a < 0.75f) c = 1;
+    else if (a <= 1.25f) c = 2;
+    else if (a < 1.75f) c = 3;
+    else if (a <= 2.5f) c = 4;
+    else if (a < 3.5f) c = 5;
+    else if (a <= 5.0f) c = 6;
+    else c = 7;
+    return sign | c;
+}
+
+__global__ void selftest_e2m1_kernel(unsigned long long* counts) {
+    unsigned long long bad = 0, bad_nan = 0;
+    const uint64_t total = 1ull << 32;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (uint64_t)gridDim.x * blockDim.x) {
+        const float v = __uint_as_float((uint32_t)i);
+        const float v8[8] = {v, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        const uint32_t got = e2m1x8(v8) & 0xfu;
+        if (is_nan32((uint32_t)i)) {
+            if (got != 0x7u) ++bad_nan;
+        } else if (got != e2m1_by_definition(v)) {
+            ++bad;
+        }
+    }
+    if (bad) atomicAdd(&counts[0], bad);
+    if (bad_nan) atomicAdd(&counts[1], bad_nan);
+}
+
 cudaError_t launch_selftest(int which, unsigned long long* counts, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(counts, 0, 2 * sizeof(unsigned long long), s);
     if (e != cudaSuccess) return e;
@@ -135,6 +177,7 @@ cudaError_t launch_selftest(int which, unsigned long long* counts, cudaStream_t 
         case 3: selftest_div_kernel<true><<<grid, block, 0, s>>>(counts); break;
         case 4: selftest_rstd_kernel<<<grid, block, 0, s>>>(counts); break;
         case 5: selftest_e4m3_kernel<<<grid, block, 0, s>>>(counts); break;
+        case 6: selftest_e2m1_kernel<<<grid, block, 0, s>>>(counts); break;
         case 1: selftest_bf16x2_kernel<true><<<grid, block, 0, s>>>(counts); break;
         case 2: selftest_bf16x2_kernel<false><<<grid, block, 0, s>>>(counts); break;
         default: return cudaErrorInvalidValue;

@@ -33,7 +33,7 @@ struct V {  // a view in one form, for the checks
 V of(const mbx_cview* v) { return V{v->data, v->rows, v->cols, v->row_stride, v->dtype}; }
 V of(const mbx_view* v) { return V{v->data, v->rows, v->cols, v->row_stride, v->dtype}; }
 
-int64_t esize(int32_t dtype) { return dtype == MBX_F32 ? 4 : dtype == MBX_E4M3 ? 1 : 2; }
+int64_t esize(int32_t dtype) { return dtype == MBX_F32 ? 4 : (dtype == MBX_E4M3 || dtype == MBX_E2M1X2) ? 1 : 2; }
 
 int64_t extent_bytes(const V& v) { return ((v.rows - 1) * v.stride + v.cols) * esize(v.dtype); }
 
@@ -307,6 +307,43 @@ int check_fp8(const mbx_view* out_fp8, const float* fp8_scale, const V* others, 
         MBX_TRY(raw_on_device(fp8_scale, 4));
     }
     return MBX_OK;
+}
+
+// The NVFP4 producers' outputs: packed values [rows, D/2] (MBX_E2M1X2) and the
+// swizzled block scales [pad128(rows), pad4(D/16)] (MBX_E4M3, contiguous).
+int check_fp4(const mbx_view* out_fp4, const mbx_view* out_sf, const float* fp4_scale, const V* others,
+              int n, bool dev) {
+    if (!out_fp4 || !out_fp4->data || !out_sf || !out_sf->data || !fp4_scale) return MBX_E_NULL;
+    V q = of(out_fp4), f = of(out_sf);
+    if (q.dtype != MBX_E2M1X2 || f.dtype != MBX_E4M3) return MBX_E_DTYPE;
+    if (q.rows <= 0 || q.cols <= 0 || f.rows <= 0 || f.cols <= 0) return MBX_E_EMPTY;
+    if ((q.rows > 1 && q.stride < q.cols) || (f.rows > 1 && f.stride != f.cols)) return MBX_E_STRIDE;
+    if (reinterpret_cast<uintptr_t>(fp4_scale) % 4) return MBX_E_ALIGN;
+    const int64_t rows = others[0].rows, D = others[0].cols;  // others[0] = out
+    if (D % 16) return MBX_E_SHAPE;
+    if (q.rows != rows || q.cols != D / 2) return MBX_E_SHAPE;
+    if (f.rows != (rows + 127) / 128 * 128 || f.cols != (D / 16 + 3) / 4 * 4) return MBX_E_SHAPE;
+    if (overlaps(q, f)) return MBX_E_ALIAS;
+    for (int i = 0; i < n; ++i)
+        if (overlaps(q, others[i]) || overlaps(f, others[i])) return MBX_E_ALIAS;
+    if (dev) {
+        V all[2] = {q, f};
+        MBX_TRY(views_on_device(all, 2));
+        MBX_TRY(raw_on_device(fp4_scale, 4));
+    }
+    return MBX_OK;
+}
+
+void set_fp4(mbx::LnModParams& p, const mbx_view* out_fp4, const mbx_view* out_sf, const float* fp4_scale) {
+    p.out_fp4 = static_cast<uint8_t*>(out_fp4->data);
+    p.out_fp4_stride = out_fp4->row_stride;
+    p.out_sf = static_cast<uint8_t*>(out_sf->data);
+    p.sf_col_tiles = (int)(out_sf->cols / 4);
+    p.fp4_scale = fp4_scale;
+}
+
+bool aligned4_fp4(const mbx_view* q) {
+    return reinterpret_cast<uintptr_t>(q->data) % 4 == 0 && (q->rows == 1 || q->row_stride % 4 == 0);
 }
 
 bool aligned8_fp8(const mbx_view* q) {
@@ -603,6 +640,41 @@ MBX_API int mbx_ln_modulate_fp8(const mbx_view* out, const mbx_view* out_fp8, co
     return cuda_status(mbx::launch_ln_modulate_fp8(p, vec, variant == MBX_HIGH, (cudaStream_t)stream));
 }
 
+MBX_API int mbx_check_ln_modulate_nvfp4(const mbx_view* out, const mbx_view* out_fp4,
+                                        const mbx_view* out_sf, const mbx_cview* x,
+                                        const mbx_cview* scale, const mbx_cview* shift,
+                                        const float* fp4_scale, float eps, int variant) {
+    for (bool dev : {false, true}) {
+        MBX_TRY(check_ln_modulate(out, x, scale, shift, eps, variant, dev));
+        V vs[4] = {of(out), of(x), of(scale), of(shift)};
+        MBX_TRY(check_fp4(out_fp4, out_sf, fp4_scale, vs, 4, dev));
+    }
+    return MBX_OK;
+}
+
+MBX_API int mbx_ln_modulate_nvfp4(const mbx_view* out, const mbx_view* out_fp4, const mbx_view* out_sf,
+                                  const mbx_cview* x, const mbx_cview* scale, const mbx_cview* shift,
+                                  const float* fp4_scale, float eps, int variant, void* stream) {
+    MBX_TRY(mbx_check_ln_modulate_nvfp4(out, out_fp4, out_sf, x, scale, shift, fp4_scale, eps, variant));
+    mbx::LnModParams p;
+    p.out = static_cast<uint16_t*>(out->data);
+    p.out_stride = out->row_stride;
+    p.x = static_cast<const uint16_t*>(x->data);
+    p.x_stride = x->row_stride;
+    p.scale = static_cast<const uint16_t*>(scale->data);
+    p.scale_stride = scale->row_stride;
+    p.shift = static_cast<const uint16_t*>(shift->data);
+    p.shift_stride = shift->row_stride;
+    p.rows = x->rows;
+    p.D = (int)x->cols;
+    p.seq = x->rows / scale->rows;
+    p.eps = eps;
+    set_fp4(p, out_fp4, out_sf, fp4_scale);
+    const bool vec = p.D % 8 == 0 && aligned16(of(out)) && aligned16(of(x)) && aligned16(of(scale)) &&
+                     aligned16(of(shift)) && aligned4_fp4(out_fp4);
+    return cuda_status(mbx::launch_ln_modulate_nvfp4(p, vec, variant == MBX_HIGH, (cudaStream_t)stream));
+}
+
 MBX_API int mbx_check_rmsnorm_scale(const mbx_view* out, const mbx_cview* x,
                                     const mbx_cview* weight, const mbx_cview* scale, float eps,
                                     int variant) {
@@ -717,6 +789,34 @@ MBX_API int mbx_gated_residual_ln_modulate_fp8(const mbx_view* residual_out, con
     return cuda_status(mbx::launch_gated_residual_ln_modulate_fp8(p, vec, variant == MBX_HIGH, (cudaStream_t)stream));
 }
 
+MBX_API int mbx_check_gated_residual_ln_modulate_nvfp4(
+    const mbx_view* residual_out, const mbx_view* out, const mbx_view* out_fp4, const mbx_view* out_sf,
+    const mbx_cview* residual, const mbx_cview* gate, const mbx_cview* update, const mbx_cview* bias,
+    const mbx_cview* scale, const mbx_cview* shift, const float* fp4_scale, float eps, int variant) {
+    for (bool dev : {false, true}) {
+        MBX_TRY(check_gated(residual_out, out, residual, gate, update, bias, scale, shift, eps, variant, dev));
+        V vs[8] = {of(out), of(residual_out), of(residual), of(gate), of(update), of(scale), of(shift),
+                   bias ? of(bias) : of(gate)};
+        MBX_TRY(check_fp4(out_fp4, out_sf, fp4_scale, vs, 8, dev));
+    }
+    return MBX_OK;
+}
+
+MBX_API int mbx_gated_residual_ln_modulate_nvfp4(
+    const mbx_view* residual_out, const mbx_view* out, const mbx_view* out_fp4, const mbx_view* out_sf,
+    const mbx_cview* residual, const mbx_cview* gate, const mbx_cview* update, const mbx_cview* bias,
+    const mbx_cview* scale, const mbx_cview* shift, const float* fp4_scale, float eps, int variant,
+    void* stream) {
+    MBX_TRY(mbx_check_gated_residual_ln_modulate_nvfp4(residual_out, out, out_fp4, out_sf, residual, gate,
+                                                       update, bias, scale, shift, fp4_scale, eps, variant));
+    mbx::LnModParams p = gated_params(residual_out, out, residual, gate, update, bias, scale, shift, eps);
+    set_fp4(p, out_fp4, out_sf, fp4_scale);
+    const bool vec = gated_vec(p, residual_out, out, residual, gate, update, bias, scale, shift) &&
+                     aligned4_fp4(out_fp4);
+    return cuda_status(
+        mbx::launch_gated_residual_ln_modulate_nvfp4(p, vec, variant == MBX_HIGH, (cudaStream_t)stream));
+}
+
 MBX_API int mbx_check_modulation_table_add(const mbx_view* out, const mbx_cview* table,
                                            const mbx_cview* temb) {
     return check_modtable(out, table, temb, true);
@@ -803,7 +903,7 @@ MBX_API int mbx_qk_norm_rope_qkv_epilogue(const mbx_view* joint, const mbx_cview
 
 MBX_API int mbx_selftest(int which, unsigned long long* counts, void* stream) {
     if (!counts) return MBX_E_NULL;
-    if (which < 0 || which > 5) return MBX_E_ARG;
+    if (which < 0 || which > 6) return MBX_E_ARG;
     if (reinterpret_cast<uintptr_t>(counts) % 8) return MBX_E_ALIGN;
     MBX_TRY(raw_on_device(counts, 16));
     return cuda_status(mbx::launch_selftest(which, counts, (cudaStream_t)stream));

@@ -199,8 +199,8 @@ def test_selftest_rejections(mbx):
     L = mbx.lib()
     assert L.mbx_selftest(0, None, None) == -1
     assert L.mbx_selftest(7, BASE, None) == -12
-    assert L.mbx_selftest(6, BASE, None) == -12
-    assert L.mbx_selftest(5, BASE, None) == -9  # a valid mode: only the device check refuses
+    assert L.mbx_selftest(8, BASE, None) == -12
+    assert L.mbx_selftest(6, BASE, None) == -9  # a valid mode: only the device check refuses
     assert L.mbx_selftest(-1, BASE, None) == -12
     assert L.mbx_selftest(0, BASE + 4, None) == -7
 
@@ -323,3 +323,34 @@ def test_fp8_producer_rejections(mbx):
     assert L.mbx_gated_residual_ln_modulate_fp8(*args, None) == -9
     args[2] = ref(V(BASE + 0x700000, rows, D, dtype=3))                      # fp8 over the update
     assert L.mbx_check_gated_residual_ln_modulate_fp8(*args) == -8
+
+
+def test_nvfp4_producer_rejections(mbx):
+    L = mbx.lib()
+    rows, D = 130, 64
+    o, x = V(BASE, rows, D), V(BASE + 0x100000, rows, D)
+    sc, sh = V(BASE + 0x200000, 2, D), V(BASE + 0x300000, 2, D)
+    q = V(BASE + 0x400000, rows, D // 2, dtype=4)
+    f = V(BASE + 0x500000, 256, 4, dtype=3)
+    gs = ctypes.c_void_p(BASE + 0x600000)
+
+    def st(o, q, f, x, sc, sh, gs):
+        a = L.mbx_check_ln_modulate_nvfp4(ref(o), ref(q), ref(f), ref(x), ref(sc), ref(sh), gs, ctypes.c_float(1e-6), 0)
+        b = L.mbx_ln_modulate_nvfp4(ref(o), ref(q), ref(f), ref(x), ref(sc), ref(sh), gs, ctypes.c_float(1e-6), 0, None)
+        assert a == b
+        return a
+
+    assert st(o, q, f, x, sc, sh, gs) == -9                                     # host checks pass
+    assert st(o, V(BASE + 0x400000, rows, D // 2, dtype=3), f, x, sc, sh, gs) == -2  # values must be E2M1X2
+    assert st(o, q, V(BASE + 0x500000, 256, 4, dtype=4), x, sc, sh, gs) == -2      # scales must be E4M3
+    assert st(o, q, V(BASE + 0x500000, 130, 4, dtype=3), x, sc, sh, gs) == -5      # rows padded to 128
+    assert st(o, q, V(BASE + 0x500000, 256, 8, dtype=3), x, sc, sh, gs) == -5      # blocks padded to 4
+    assert st(o, q, V(BASE + 0x500000, 256, 4, 8, dtype=3), x, sc, sh, gs) == -6   # scales contiguous
+    assert st(o, V(BASE + 0x400000, rows, D, dtype=4), f, x, sc, sh, gs) == -5     # D/2 bytes a row
+    assert st(o, q, V(BASE + 0x400000 + 64, 256, 4, dtype=3), x, sc, sh, gs) == -8  # scales over values
+    assert st(o, q, f, x, sc, sh, None) == -1
+    d2 = 72  # not a multiple of 16
+    o2, x2 = V(BASE, rows, d2), V(BASE + 0x100000, rows, d2)
+    sc2, sh2 = V(BASE + 0x200000, 2, d2), V(BASE + 0x300000, 2, d2)
+    assert st(o2, V(BASE + 0x400000, rows, d2 // 2, dtype=4), V(BASE + 0x500000, 256, 8, dtype=3),
+              x2, sc2, sh2, gs) == -5
