@@ -60,8 +60,8 @@ def peaks():
 
 def kernel_sha(op: str) -> str:
     k = os.path.join(ROOT, "modulation_bit_exact_gb300", "csrc", "kernels")
-    files = ["numerics.cuh", "rowops.cuh", {"ln_modulate": "ln_modulate.cu",
-                                             "residual_gate_add": "residual.cu"}[op]]
+    files = ["numerics.cuh", "rowops.cuh"] + {"ln_modulate": ["ln_pipe.cuh", "ln_modulate.cu"],
+                                               "residual_gate_add": ["residual.cu"]}[op]
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(k, f), "rb") as fh:
@@ -506,6 +506,10 @@ def run_suite(args):
             table_case("Wan2.2-TI2V table [1,109120,6,3072] bf16 temb", 31 * 44 * 80, 3072)
             table_case("video table [1,32760,6,5120] bf16 temb", 32760, 5120)
             table_case("video table [1,32760,6,5120] f32 temb", 32760, 5120, emb_dt=torch.float32)
+        if "image" in only:
+            row_case("image-DiT [2,4352,3072]", 2, 4352, 3072, False)
+        if "video" in only:
+            row_case("video-DiT [1,32760,5120] per-token", 1, 32760, 5120, True)
         return 0
     row_case("tiny [2,256,512]", 2, 256, 512, False)
     row_case("image-DiT [2,4352,3072]", 2, 4352, 3072, False)
@@ -576,7 +580,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", default="mbx", choices=["mbx", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", default=None, help="with --suite: run only the named group (table)")
+    ap.add_argument("--only", default=None, help="with --suite: run only the named groups (table, image, video)")
     ap.add_argument("--suite", action="store_true",
                     help="time every operation and variant on the configurations' shapes "
                          "(one JSON line per case) instead of the benchmark step")

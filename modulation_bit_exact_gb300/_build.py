@@ -17,6 +17,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = [
     os.path.join(CSRC, "mbx_api.cu"),
     os.path.join(KERN, "ln_modulate.cu"),
+    os.path.join(KERN, "ln_nvfp4.cu"),
     os.path.join(KERN, "rmsnorm.cu"),
     os.path.join(KERN, "residual.cu"),
     os.path.join(KERN, "qkv.cu"),

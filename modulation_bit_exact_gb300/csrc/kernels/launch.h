@@ -195,6 +195,7 @@ cudaError_t launch_residual_gate_add(const GateAddParams& p, bool vec, bool high
 cudaError_t launch_gated_residual_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_gated_residual_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cudaStream_t s);
+cudaError_t launch_gated_add_part(const LnModParams& p, bool vec, cudaStream_t s, LnModParams* ln);
 cudaError_t launch_ln_modulate_nvfp4(const LnModParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_gated_residual_ln_modulate_nvfp4(const LnModParams& p, bool vec, bool high, cudaStream_t s);
 cudaError_t launch_qkv_epilogue(const QkvParams& p, bool high, cudaStream_t s);

@@ -13,14 +13,9 @@
 //   out = bf16(bf16(nrm * bf16(1 + scale)) + shift)
 // High path: the same formula in one binary32 pass (two-pass mean/variance
 // over registers, fused multiply-add allowed) with one rounding at the output.
-#include "launch.h"
-#include "rowops.cuh"
+#include "ln_pipe.cuh"
 
 namespace mbx {
-
-__device__ __forceinline__ u64 sel2(bool a, bool b, u64 n, u64 o) {
-    return f2(a ? f2lo(n) : f2lo(o), b ? f2hi(n) : f2hi(o));
-}
 
 // Welford statistics of every lane this thread owns (GUARD: division safe for
 // any d; otherwise the fast division, for lanes that pass lanes_plain).
@@ -194,438 +189,6 @@ __global__ void __launch_bounds__(kBlock) ln_modulate_kernel(LnModParams p) {
     }
 }
 
-// ------------------------------------------------------------------ pipelined path
-//
-// For 16-byte-aligned rows (D % 8 == 0): one CTA per SM holds several row
-// groups; each group streams its next rows into a ring of shared-memory
-// stages with cp.async (each thread copies exactly the chunks it will read),
-// so loads stay in flight while the group computes.  Same lanes, same order,
-// same tree as above: the results are the same bits.
-
-// Every element of the chunk has |x| >= 2^-60 (bf16 exponent field >= 67).
-__device__ __forceinline__ bool chunk_plain(const uint4& v) {
-    uint32_t a = min_u16x2(min_u16x2(v.x & 0x7f807f80u, v.y & 0x7f807f80u),
-                           min_u16x2(v.z & 0x7f807f80u, v.w & 0x7f807f80u));
-    uint32_t lo = a & 0xffffu, hi = a >> 16;
-    return (lo < hi ? lo : hi) >= 0x2180u;
-}
-
-struct WPair {
-    u64 mean, m2;
-};
-
-// Welford over one chunk of lane A (low halves) and one of lane B (high
-// halves), counts k0+1..k0+8, with plain correctly rounded division: the rare
-// path for chunks holding zeros or values below 2^-60.  na / nb: elements of
-// each chunk that exist (0 or 8).
-__device__ __noinline__ WPair welford_chunk_exact(uint4 a, uint4 b, int k0, int na, int nb, WPair st) {
-    float ma = f2lo(st.mean), qa = f2lo(st.m2), mb = f2hi(st.mean), qb = f2hi(st.m2);
-    for (int e = 0; e < kChunk; ++e) {
-        const float k = (float)(k0 + e + 1);
-        const uint32_t wa = w_of(a, e >> 1), wb = w_of(b, e >> 1);
-        const float xa = (e & 1) ? hi_f(wa) : lo_f(wa), xb = (e & 1) ? hi_f(wb) : lo_f(wb);
-        if (e < na) {
-            float d = __fsub_rn(xa, ma);
-            ma = __fadd_rn(ma, __fdiv_rn(d, k));
-            qa = __fadd_rn(qa, __fmul_rn(d, __fsub_rn(xa, ma)));
-        }
-        if (e < nb) {
-            float d = __fsub_rn(xb, mb);
-            mb = __fadd_rn(mb, __fdiv_rn(d, k));
-            qb = __fadd_rn(qb, __fmul_rn(d, __fsub_rn(xb, mb)));
-        }
-    }
-    return WPair{f2(ma, mb), f2(qa, qb)};
-}
-
-// Welford of every lane this thread owns, reading its chunks from ring stage
-// s.  For each chunk index j one branch decides, for all the thread's lanes at
-// once, between the fast division (every element plain) and the exact one,
-// so the lane pairs' dependency chains interleave.  `full` (every lane has
-// all J chunks) removes the per-step selects of the last chunk.
-// ROWCHECK: for full rows, decide fast-or-exact once for all of the thread's
-// chunks (measured faster for the unfused kernel at J = 1 and 3; slower at
-// even J and in the fused kernel, where the extra live chunks cost more).
-template <class C, bool ROWCHECK, class RingT>
-__device__ __forceinline__ void welford_stage(const RingT& ring, int s, int t, int nch, bool full,
-                                              Wf (&L)[C::M], u64 nz) {
-    if constexpr (C::M >= 2) {
-        constexpr int P = C::M / 2;
-        u64 mean[P], m2[P];
-#pragma unroll
-        for (int p = 0; p < P; ++p) mean[p] = m2[p] = f2(0.0f, 0.0f);
-        if (ROWCHECK && full) {
-            // Common case: every lane has all J chunks.  One check for all of
-            // this thread's elements (the smallest exponent field over every
-            // chunk), then the fast division throughout, both lane pairs'
-            // chains interleaved.
-            uint4 A[C::J][P], B[C::J][P];
-            uint32_t lowest = 0xffffffffu;
-#pragma unroll
-            for (int j = 0; j < C::J; ++j)
-#pragma unroll
-                for (int p = 0; p < P; ++p) {
-                    const int ca = t + C::TPR * p + kLanes * j;
-                    A[j][p] = lds16(ring.at(s, 0, ca));
-                    B[j][p] = lds16(ring.at(s, 0, ca + C::TPR * P));
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        lowest = min_u16x2(lowest, w_of(A[j][p], i) & 0x7f807f80u);
-                        lowest = min_u16x2(lowest, w_of(B[j][p], i) & 0x7f807f80u);
-                    }
-                }
-            const uint32_t lo = lowest & 0xffffu, hi = lowest >> 16;
-            if ((lo < hi ? lo : hi) >= 0x2180u) {
-                static_for<0, C::J>([&](auto jc) {
-                    constexpr int j = decltype(jc)::value;
-                    static_for<0, kChunk>([&](auto ec) {
-                        constexpr int e = decltype(ec)::value;
-                        constexpr int K = kChunk * j + e + 1;
-#pragma unroll
-                        for (int p = 0; p < P; ++p)
-                            welford_step2<K, false>(pair_elem(w_of(A[j][p], e / 2), w_of(B[j][p], e / 2), e & 1),
-                                                    mean[p], m2[p], nz);
-                    });
-                });
-#pragma unroll
-                for (int p = 0; p < P; ++p) {
-                    L[p].mean = f2lo(mean[p]);
-                    L[p].m2 = f2lo(m2[p]);
-                    L[p + P].mean = f2hi(mean[p]);
-                    L[p + P].m2 = f2hi(m2[p]);
-                    L[p].n = L[p + P].n = (float)(kChunk * C::J);
-                }
-                return;
-            }
-        }
-        static_for<0, C::J>([&](auto jc) {
-            constexpr int j = decltype(jc)::value;
-            uint4 A[P], B[P];
-            bool va[P], vb[P];
-            bool plain = true;
-#pragma unroll
-            for (int p = 0; p < P; ++p) {
-                const int ca = t + C::TPR * p + kLanes * j, cb = ca + C::TPR * P;
-                va[p] = ca < nch;
-                vb[p] = cb < nch;
-                A[p] = va[p] ? lds16(ring.at(s, 0, ca)) : make_uint4(0, 0, 0, 0);
-                B[p] = vb[p] ? lds16(ring.at(s, 0, cb)) : make_uint4(0, 0, 0, 0);
-                plain = plain && (!va[p] || chunk_plain(A[p])) && (!vb[p] || chunk_plain(B[p]));
-            }
-            if (plain && (j < C::J - 1 || full)) {
-                static_for<0, kChunk>([&](auto ec) {
-                    constexpr int e = decltype(ec)::value;
-                    constexpr int K = kChunk * j + e + 1;
-#pragma unroll
-                    for (int p = 0; p < P; ++p)
-                        welford_step2<K, false>(pair_elem(w_of(A[p], e / 2), w_of(B[p], e / 2), e & 1), mean[p], m2[p], nz);
-                });
-            } else if (plain) {  // last chunk, some lanes without it
-                static_for<0, kChunk>([&](auto ec) {
-                    constexpr int e = decltype(ec)::value;
-                    constexpr int K = kChunk * j + e + 1;
-#pragma unroll
-                    for (int p = 0; p < P; ++p) {
-                        u64 mn = mean[p], q = m2[p];
-                        welford_step2<K, false>(pair_elem(w_of(A[p], e / 2), w_of(B[p], e / 2), e & 1), mn, q, nz);
-                        mean[p] = sel2(va[p], vb[p], mn, mean[p]);
-                        m2[p] = sel2(va[p], vb[p], q, m2[p]);
-                    }
-                });
-            } else {
-#pragma unroll
-                for (int p = 0; p < P; ++p) {
-                    WPair r = welford_chunk_exact(A[p], B[p], kChunk * j, va[p] ? kChunk : 0, vb[p] ? kChunk : 0,
-                                                  WPair{mean[p], m2[p]});
-                    mean[p] = r.mean;
-                    m2[p] = r.m2;
-                }
-            }
-        });
-#pragma unroll
-        for (int p = 0; p < P; ++p) {
-            L[p].mean = f2lo(mean[p]);
-            L[p].m2 = f2lo(m2[p]);
-            L[p + P].mean = f2hi(mean[p]);
-            L[p + P].m2 = f2hi(m2[p]);
-        }
-    } else {
-        u64 st = f2(0.0f, 0.0f), sq = f2(0.0f, 0.0f);  // lane in the low halves
-        static_for<0, C::J>([&](auto jc) {
-            constexpr int j = decltype(jc)::value;
-            const int c = t + kLanes * j;
-            if (c >= nch) return;
-            const uint4 A = lds16(ring.at(s, 0, c));
-            if (chunk_plain(A)) {
-                float mean = f2lo(st), m2 = f2lo(sq);
-                static_for<0, kChunk>([&](auto ec) {
-                    constexpr int e = decltype(ec)::value;
-                    constexpr int K = kChunk * j + e + 1;
-                    const uint32_t w = w_of(A, e / 2);
-                    welford_step<K, false>((e & 1) ? hi_f(w) : lo_f(w), mean, m2);
-                });
-                st = f2(mean, 0.0f);
-                sq = f2(m2, 0.0f);
-            } else {
-                WPair r = welford_chunk_exact(A, make_uint4(0, 0, 0, 0), kChunk * j, kChunk, 0, WPair{st, sq});
-                st = r.mean;
-                sq = r.m2;
-            }
-        });
-        L[0].mean = f2lo(st);
-        L[0].m2 = f2lo(sq);
-    }
-#pragma unroll
-    for (int m = 0; m < C::M; ++m) {
-        const int c_last = t + C::TPR * m + kLanes * (C::J - 1);
-        L[m].n = (float)(kChunk * (C::J - 1) + (c_last < nch ? kChunk : 0));
-    }
-}
-
-// Modulation modes of the pipelined kernel:
-//   kModRing:   the modulation rows travel in the ring with x (per-token
-//               modulation, or samples that change within a CTA's rows);
-//   kModStaged: a CTA's rows span at most two samples; their bf16(1+scale)
-//               (lossless) or scale (high) and shift are staged in shared
-//               memory once.
-enum { kModRing = 0, kModStaged = 1 };
-
-// Ring operands of the pipelined kernel: x (the residual when FUSED), then
-// the update (FUSED), then, in ring mode, scale, shift and the gate (FUSED).
-template <bool FUSED, int MODE>
-struct LnOps {
-    static constexpr int U = FUSED ? 1 : -1;
-    static constexpr int SC = MODE == kModRing ? (FUSED ? 2 : 1) : -1;
-    static constexpr int SH = MODE == kModRing ? SC + 1 : -1;
-    static constexpr int G = MODE == kModRing && FUSED ? SH + 1 : -1;
-    static constexpr int N = 1 + (FUSED ? 1 : 0) + (MODE == kModRing ? (FUSED ? 3 : 2) : 0);
-    static constexpr int SLOT = FUSED ? 3 : 2;  // staged arrays per sample: t, shift[, gate]
-};
-
-__device__ __forceinline__ void sts16(uint4* p, uint4 v) {
-    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
-}
-
-template <int TPR, int J, int NS, bool HIGH, int MODE, bool FUSED>
-__global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p, int64_t rows_per_cta) {
-    using C = RowCfg<TPR, J, true>;
-    using O = LnOps<FUSED, MODE>;
-    constexpr int NOPS = O::N;
-    using R = Ring<C, NS, NOPS>;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    const int groups = blockDim.x / TPR;
-    const int g = threadIdx.x / TPR, t = threadIdx.x % TPR;
-    const int D = p.D;
-    const int nch = D / kChunk;
-    TreeSmem& sm = reinterpret_cast<TreeSmem*>(smem_raw)[g];
-    uint4* mod = reinterpret_cast<uint4*>(smem_raw + groups * sizeof(TreeSmem));  // [2 slots][t|shift[|gate]][nch]
-    const int mod_chunks = MODE == kModStaged ? 2 * O::SLOT * nch : 0;
-    uint4* bias_sm = mod + mod_chunks;  // [nch] when FUSED with a bias
-    const int bias_chunks = FUSED && p.bias != nullptr ? nch : 0;
-    const R ring{bias_sm + bias_chunks + (size_t)g * (R::kBytes / 16)};
-    const int bar_id = 1 + g;
-    const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
-    const int64_t r1 = r0 + rows_per_cta < p.rows ? r0 + rows_per_cta : p.rows;
-    const int64_t m0 = r0 / p.seq;
-    const int64_t split = (m0 + 1) * p.seq;  // staged: rows from here use slot 1
-    const int64_t first = r0 + g;
-    RowDiv next(first, groups, p.seq);  // modulation row of the next row to issue
-    // FP8 producer: 1/scale correctly rounded, once per thread
-    const float inv8 = p.out_fp8 != nullptr ? __fdiv_rn(1.0f, __ldg(p.fp8_scale)) : 0.0f;
-    const float gs4 = p.out_fp4 != nullptr ? __ldg(p.fp4_scale) : 0.0f;  // NVFP4 global scale
-
-    auto issue = [&](int s, int64_t row) {
-        ring.issue(s, 0, p.x + row * p.x_stride, t, nch);
-        if constexpr (FUSED) ring.issue(s, O::U, p.update + row * p.update_stride, t, nch);
-        if constexpr (MODE == kModRing) {
-            const int64_t mrow = next.q;
-            ring.issue(s, O::SC, p.scale + mrow * p.scale_stride, t, nch);
-            ring.issue(s, O::SH, p.shift + mrow * p.shift_stride, t, nch);
-            if constexpr (FUSED) ring.issue(s, O::G, p.gate + mrow * p.gate_stride, t, nch);
-        }
-    };
-#pragma unroll
-    for (int s = 0; s < NS - 1; ++s) {
-        const int64_t r = first + s * groups;
-        if (r < r1) issue(s, r);
-        if constexpr (MODE == kModRing) next.advance();
-        cp_async_commit();
-    }
-    // the first rows are on their way; stage the modulation meanwhile
-    if constexpr (MODE == kModStaged) {
-        const int64_t m_last = (r1 - 1) / p.seq;
-        const int slots = (int)(m_last - m0 + 1);  // 1 or 2 (host guarantees)
-        for (int i = threadIdx.x; i < slots * nch; i += blockDim.x) {
-            const int slot = i / nch, c = i - slot * nch;
-            const uint4 sc = ld_shared_row(p.scale + (m0 + slot) * p.scale_stride + (int64_t)c * kChunk);
-            const uint4 sh = ld_shared_row(p.shift + (m0 + slot) * p.shift_stride + (int64_t)c * kChunk);
-            uint4 tv;
-            if constexpr (!HIGH) {
-                tv.x = badd(0x3f803f80u, sc.x);  // bf16(1 + scale), as the eager chain rounds it
-                tv.y = badd(0x3f803f80u, sc.y);
-                tv.z = badd(0x3f803f80u, sc.z);
-                tv.w = badd(0x3f803f80u, sc.w);
-            } else {
-                tv = sc;
-            }
-            mod[(slot * O::SLOT + 0) * nch + c] = tv;
-            mod[(slot * O::SLOT + 1) * nch + c] = sh;
-            if constexpr (FUSED)
-                mod[(slot * O::SLOT + 2) * nch + c] = ld_shared_row(p.gate + (m0 + slot) * p.gate_stride + (int64_t)c * kChunk);
-        }
-    }
-    if constexpr (FUSED) {
-        for (int c = threadIdx.x; c < bias_chunks; c += blockDim.x)
-            bias_sm[c] = ld_shared_row(p.bias + (int64_t)c * kChunk);
-    }
-    if constexpr (MODE == kModStaged || FUSED) __syncthreads();
-
-    int cur = 0;
-    for (int64_t row = first; row < r1; row += groups) {
-        const int64_t rn = row + (NS - 1) * groups;
-        const int sn = cur == 0 ? NS - 1 : cur - 1;
-        if (rn < r1) issue(sn, rn);
-        if constexpr (MODE == kModRing) next.advance();
-        cp_async_commit();
-        cp_async_wait<NS - 1>();
-        const int slot = row >= split ? 1 : 0;
-
-        if constexpr (FUSED) {
-            // front pass: the new residual r' = bf16(x + bf16(gate * a)), written
-            // out and back over x in this thread's own ring chunks
-            const uint4* gm = MODE == kModStaged ? mod + (slot * O::SLOT + 2) * nch : nullptr;
-            uint16_t* res_row = p.res_out + row * p.res_out_stride;
-#pragma unroll
-            for (int j = 0; j < C::J; ++j)
-#pragma unroll
-                for (int m = 0; m < C::M; ++m) {
-                    const int c = t + C::TPR * m + kLanes * j;
-                    if (c >= nch) continue;
-                    const uint4 X = lds16(ring.at(cur, 0, c));
-                    uint4 U = lds16(ring.at(cur, O::U, c));
-                    if (bias_chunks) {
-                        const uint4 B = lds16(bias_sm + c);
-                        U = make_uint4(badd(U.x, B.x), badd(U.y, B.y), badd(U.z, B.z), badd(U.w, B.w));
-                    }
-                    uint4 G;
-                    if constexpr (MODE == kModStaged) G = lds16(gm + c);
-                    else G = lds16(ring.at(cur, O::G > 0 ? O::G : 0, c));
-                    const uint4 Y = make_uint4(badd(X.x, bmul(G.x, U.x)), badd(X.y, bmul(G.y, U.y)),
-                                               badd(X.z, bmul(G.z, U.z)), badd(X.w, bmul(G.w, U.w)));
-                    st_v4(res_row + (int64_t)c * kChunk, Y);
-                    sts16(ring.at(cur, 0, c), Y);
-                }
-        }
-
-        float mean = 0.0f, rstd = 0.0f;
-        if constexpr (!HIGH) {
-            Wf L[C::M];
-            const bool full = nch == kLanes * C::J;
-            welford_stage<C, !FUSED && (J == 1 || J == 3)>(ring, cur, t, nch, full, L, f2(p.neg_zero, p.neg_zero));
-            const Wf s = full ? tree_reduce<C>(L, t, sm, bar_id, wf_combine_eq)
-                              : tree_reduce<C>(L, t, sm, bar_id, wf_combine);
-            mean = s.mean;
-            if (t == 0) {
-                const float var = __fdiv_rn(s.m2, (float)D);
-                rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, p.eps)));
-            }
-        } else {
-            float acc[C::M];
-#pragma unroll
-            for (int m = 0; m < C::M; ++m) {
-                acc[m] = 0.0f;
-#pragma unroll
-                for (int j = 0; j < C::J; ++j) {
-                    const int c = t + C::TPR * m + kLanes * j;
-                    if (c >= nch) continue;
-                    const uint4 v = lds16(ring.at(cur, 0, c));
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[m] += lo_f(w_of(v, i)) + hi_f(w_of(v, i));
-                }
-            }
-            float dummy = 0.0f;
-            mean = tree_reduce<C>(acc, t, sm, bar_id, sum_combine) / (float)D;
-            group_bcast<C>(mean, dummy, t, sm, bar_id);
-#pragma unroll
-            for (int m = 0; m < C::M; ++m) {
-                acc[m] = 0.0f;
-#pragma unroll
-                for (int j = 0; j < C::J; ++j) {
-                    const int c = t + C::TPR * m + kLanes * j;
-                    if (c >= nch) continue;
-                    const uint4 v = lds16(ring.at(cur, 0, c));
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float d0 = lo_f(w_of(v, i)) - mean, d1 = hi_f(w_of(v, i)) - mean;
-                        acc[m] += d0 * d0 + d1 * d1;
-                    }
-                }
-            }
-            const float q = tree_reduce<C>(acc, t, sm, bar_id, sum_combine);
-            if (t == 0) rstd = rsqrtf(q / (float)D + p.eps);
-        }
-        group_bcast<C>(mean, rstd, t, sm, bar_id);
-
-        const uint4* tm = MODE == kModStaged ? mod + (slot * O::SLOT + 0) * nch : nullptr;
-        const uint4* sh = MODE == kModStaged ? tm + nch : nullptr;
-        uint16_t* out_row = p.out + row * p.out_stride;
-        const u64 mean2 = f2(mean, mean), rstd2 = f2(rstd, rstd);
-#pragma unroll
-        for (int j = 0; j < C::J; ++j)
-#pragma unroll
-            for (int m = 0; m < C::M; ++m) {
-                const int c = t + C::TPR * m + kLanes * j;
-                const bool valid = c < nch;
-                uint4 o = make_uint4(0, 0, 0, 0);
-                if (valid) {
-                const uint4 X = lds16(ring.at(cur, 0, c));
-                uint4 T, SH;
-                if constexpr (MODE == kModStaged) {
-                    T = lds16(tm + c);
-                    SH = lds16(sh + c);
-                } else {
-                    T = lds16(ring.at(cur, O::SC > 0 ? O::SC : 0, c));
-                    SH = lds16(ring.at(cur, O::SH > 0 ? O::SH : 0, c));
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t xw = w_of(X, i), tw = w_of(T, i), hw = w_of(SH, i);
-                    uint32_t ow;
-                    if constexpr (!HIGH) {
-                        const uint32_t nrm = pack2_rn(mul2(sub2(widen2(xw), mean2), rstd2));
-                        // ring mode carries scale itself: round 1 + scale here
-                        const uint32_t tt = MODE == kModStaged ? tw : badd(0x3f803f80u, tw);
-                        ow = badd(bmul(nrm, tt), hw);
-                    } else {
-                        ow = pack_rn(fmaf((lo_f(xw) - mean) * rstd, 1.0f + lo_f(tw), lo_f(hw)),
-                                     fmaf((hi_f(xw) - mean) * rstd, 1.0f + hi_f(tw), hi_f(hw)));
-                    }
-                    w_set(o, i, ow);
-                }
-                st_v4(out_row + (int64_t)c * kChunk, o);
-                if (p.out_fp8 != nullptr)
-                    st_v2(p.out_fp8 + row * p.out_fp8_stride + (int64_t)c * kChunk, e4m3x4_of_bf16(o.x, o.y, inv8),
-                          e4m3x4_of_bf16(o.z, o.w, inv8));
-                }
-                if (p.out_fp4 != nullptr) {
-                    // a 16-element block is chunks 2b and 2b+1, held by lanes
-                    // t and t^1 of the same warp (every lane takes part)
-                    const float a8 = valid ? amax8_bf16(o) : 0.0f;
-                    const float a16 = max_nan(a8, __shfl_xor_sync(0xffffffffu, a8, 1));
-                    float sv;
-                    const uint32_t sc = nvfp4_block_scale(a16, gs4, sv);
-                    if (valid) {
-                        st_u32(p.out_fp4 + row * p.out_fp4_stride + (int64_t)c * 4, nvfp4_codes(o, gs4, sv));
-                        if ((c & 1) == 0) p.out_sf[nvfp4_sf_offset(row, c >> 1, p.sf_col_tiles)] = (uint8_t)sc;
-                    }
-                }
-            }
-        cur = cur + 1 == NS ? 0 : cur + 1;
-    }
-    cp_async_wait<0>();
-}
-
 // ------------------------------------------------------------------ host
 
 template <int TPR, int J, bool VEC, bool HIGH>
@@ -642,72 +205,9 @@ static cudaError_t launch_j(const LnModParams& p, bool, bool high, cudaStream_t 
     return high ? launch_one<TPR, J, false, true>(p, s) : launch_one<TPR, J, false, false>(p, s);
 }
 
-template <int TPR, int J, int NS, bool HIGH, int MODE, bool FUSED>
-static cudaError_t launch_pipe(const LnModParams& p, cudaStream_t s) {
-    auto k = ln_modulate_pipe_kernel<TPR, J, NS, HIGH, MODE, FUSED>;
-    using C = RowCfg<TPR, J, true>;
-    using O = LnOps<FUSED, MODE>;
-    using R = Ring<C, NS, O::N>;
-    const int nch = p.D / kChunk;
-    const int fixed = (MODE == kModStaged ? 2 * O::SLOT * nch * 16 : 0) + (FUSED && p.bias ? nch * 16 : 0);
-    PipeShape sh;
-    if (!pipe_shape(reinterpret_cast<const void*>(k), TPR, (int)sizeof(TreeSmem) + R::kBytes, fixed, p.rows, &sh))
-        return cudaErrorInvalidConfiguration;
-    k<<<sh.grid, sh.groups * TPR, sh.smem, s>>>(p, sh.rows_per_cta);
-    return cudaGetLastError();
-}
-
-template <int TPR, int J, int NS, bool FUSED>
-static cudaError_t launch_pipe_v(const LnModParams& p, bool high, cudaStream_t s) {
-    // stage the modulation when each CTA's block of rows spans at most two
-    // samples (rows per CTA <= seq); otherwise carry it in the ring
-    const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
-    if (high)
-        return staged ? launch_pipe<TPR, J, NS, true, kModStaged, FUSED>(p, s)
-                      : launch_pipe<TPR, J, NS, true, kModRing, FUSED>(p, s);
-    return staged ? launch_pipe<TPR, J, NS, false, kModStaged, FUSED>(p, s)
-                  : launch_pipe<TPR, J, NS, false, kModRing, FUSED>(p, s);
-}
-
-template <bool FUSED>
-static cudaError_t launch_pipe_d(const LnModParams& p, bool high, cudaStream_t s) {
-    // one warp per row up to 2048 elements, two up to 4096 (measured fastest
-    // at 3072: fewer, longer row rounds), four above
-    switch (chunks_per_lane(p.D)) {
-        case 1: return launch_pipe_v<32, 1, 2, FUSED>(p, high, s);
-        case 2: return launch_pipe_v<32, 2, 2, FUSED>(p, high, s);
-        case 3: return launch_pipe_v<64, 3, 2, FUSED>(p, high, s);
-        case 4: return launch_pipe_v<64, 4, 2, FUSED>(p, high, s);
-        case 5: return launch_pipe_v<128, 5, 2, FUSED>(p, high, s);
-        case 6: return launch_pipe_v<128, 6, 2, FUSED>(p, high, s);
-        case 7: return launch_pipe_v<128, 7, 2, FUSED>(p, high, s);
-        case 8: return launch_pipe_v<128, 8, 2, FUSED>(p, high, s);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-// Whether the fused ring kernel keeps at least two row groups per SM: its
-// stages carry the residual and the update (and the modulation per token),
-// and per-sample modulation, gate and bias are staged.  At the widest rows
-// one group would remain, and two launches (gated add, then LN) move more
-// bytes but run faster.  Same arithmetic as launch_pipe.
-static bool fused_fits(const LnModParams& p) {
-    int dev = 0, optin = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    const int J = chunks_per_lane(p.D), nch = p.D / kChunk;
-    const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
-    const int nops = staged ? LnOps<true, kModStaged>::N : LnOps<true, kModRing>::N;
-    const int per_group = (int)sizeof(TreeSmem) + 2 * nops * kLanes * J * 16;
-    const int fixed = (staged ? 2 * LnOps<true, kModStaged>::SLOT * nch * 16 : 0) + (p.bias ? nch * 16 : 0);
-    return (optin - 8 * 1024 - fixed) / per_group >= 2;
-}
-
-cudaError_t launch_gated_residual_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
-    if (vec && fused_fits(p)) return launch_pipe_d<true>(p, high, s);
-    // unaligned or ragged rows, or rows too wide for the fused ring: the same
-    // definition as two steps, the gated residual into res_out, then
-    // LayerNorm + modulate of res_out
+// First half of the composed gated op: r' = bf16(x + bf16(gate * a)) into
+// res_out; returns the parameters of the LN pass over r'.
+cudaError_t launch_gated_add_part(const LnModParams& p, bool vec, cudaStream_t s, LnModParams* ln) {
     GateAddParams g;
     g.out = p.res_out;
     g.out_stride = p.res_out_stride;
@@ -721,16 +221,25 @@ cudaError_t launch_gated_residual_ln_modulate(const LnModParams& p, bool vec, bo
     g.D = p.D;
     g.seq = p.seq;
     g.bias = p.bias;
-    cudaError_t e = launch_residual_gate_add(g, vec, false, s);
+    *ln = p;
+    ln->x = p.res_out;
+    ln->x_stride = p.res_out_stride;
+    ln->update = nullptr;
+    ln->gate = nullptr;
+    ln->bias = nullptr;
+    ln->res_out = nullptr;
+    return launch_residual_gate_add(g, vec, false, s);
+}
+
+cudaError_t launch_gated_residual_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
+    if (vec && fused_fits(p)) return launch_pipe_d<true, false>(p, high, s);
+    // unaligned or ragged rows, or rows too wide for the fused ring: the same
+    // definition as two steps, the gated residual into res_out, then
+    // LayerNorm + modulate of res_out
+    LnModParams q;
+    const cudaError_t e = launch_gated_add_part(p, vec, s, &q);
     if (e != cudaSuccess) return e;
-    LnModParams q = p;
-    q.x = p.res_out;
-    q.x_stride = p.res_out_stride;
-    q.update = nullptr;
-    q.gate = nullptr;
-    q.bias = nullptr;
-    q.res_out = nullptr;
-    return vec ? launch_pipe_d<false>(q, high, s) : launch_ln_modulate(q, false, high, s);
+    return vec ? launch_pipe_d<false, false>(q, high, s) : launch_ln_modulate(q, false, high, s);
 }
 
 // The FP8 copy outside the pipelined kernel: quantise the bf16 output after it
@@ -748,46 +257,15 @@ static cudaError_t quantise_out(const LnModParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
-    if (vec) return launch_pipe_d<false>(p, high, s);
+    if (vec) return launch_pipe_d<false, false>(p, high, s);
     LnModParams q = p;
     q.out_fp8 = nullptr;
     cudaError_t e = launch_ln_modulate(q, false, high, s);
     return e != cudaSuccess ? e : quantise_out(p, s);
 }
 
-static cudaError_t quantise_out_fp4(const LnModParams& p, cudaStream_t s) {
-    QuantFp4Params q;
-    q.out = p.out_fp4;
-    q.out_stride = p.out_fp4_stride;
-    q.sf = p.out_sf;
-    q.sf_col_tiles = p.sf_col_tiles;
-    q.y = p.out;
-    q.y_stride = p.out_stride;
-    q.rows = p.rows;
-    q.D = p.D;
-    q.gs = p.fp4_scale;
-    return launch_quant_nvfp4(q, s);
-}
-
-cudaError_t launch_ln_modulate_nvfp4(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
-    if (vec) return launch_pipe_d<false>(p, high, s);
-    LnModParams q = p;
-    q.out_fp4 = nullptr;
-    cudaError_t e = launch_ln_modulate(q, false, high, s);
-    return e != cudaSuccess ? e : quantise_out_fp4(p, s);
-}
-
-cudaError_t launch_gated_residual_ln_modulate_nvfp4(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
-    if (vec && fused_fits(p)) return launch_pipe_d<true>(p, high, s);
-    if (vec) return launch_gated_residual_ln_modulate(p, true, high, s);  // composed; the LN pass writes the copy
-    LnModParams q = p;
-    q.out_fp4 = nullptr;
-    cudaError_t e = launch_gated_residual_ln_modulate(q, false, high, s);
-    return e != cudaSuccess ? e : quantise_out_fp4(p, s);
-}
-
 cudaError_t launch_gated_residual_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
-    if (vec && fused_fits(p)) return launch_pipe_d<true>(p, high, s);
+    if (vec && fused_fits(p)) return launch_pipe_d<true, false>(p, high, s);
     if (vec) return launch_gated_residual_ln_modulate(p, true, high, s);  // composed; the LN pass writes the FP8 copy
     LnModParams q = p;
     q.out_fp8 = nullptr;
@@ -797,7 +275,7 @@ cudaError_t launch_gated_residual_ln_modulate_fp8(const LnModParams& p, bool vec
 
 cudaError_t launch_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
     const int J = chunks_per_lane(p.D);
-    if (vec) return launch_pipe_d<false>(p, high, s);
+    if (vec) return launch_pipe_d<false, false>(p, high, s);
     switch (J) {
         // threads per row: enough that a thread holds at most ~5 chunks of x
         case 1: return launch_j<32, 1>(p, vec, high, s);

@@ -378,11 +378,45 @@ __device__ __forceinline__ float amax8_bf16(const uint4& o) {
 }
 
 // NVFP4 block step: from the block's amax and the global scale gs, the E4M3
-// block scale s = e4m3(RN(RN(amax * gs) / 6)) and its value.
+// block scale s = e4m3(RN(RN(amax * gs) / 6)) and its value.  The division by
+// 6 is the guarded Markstein form (equal to div.rn for every finite numerator,
+// mbx_selftest(0)); an infinite or NaN numerator takes div.rn itself.
+__device__ __forceinline__ float div6(float d) {
+    return isfinite(d) ? div_k<6>(d) : __fdiv_rn(d, 6.0f);
+}
 __device__ __forceinline__ uint32_t nvfp4_block_scale(float amax16, float gs, float& sv) {
-    const uint32_t s = e4m3x2(0.0f, __fdiv_rn(__fmul_rn(amax16, gs), 6.0f)) & 0xffu;
+    const uint32_t s = e4m3x2(0.0f, div6(__fmul_rn(amax16, gs))) & 0xffu;
     sv = e4m3_value(s);
     return s;
+}
+
+// The same step with the element factor gs / value(s) looked up in a table of
+// all 256 codes (built once per CTA by nvfp4_fill_table): returns s and sets
+// esc.
+__device__ __forceinline__ uint32_t nvfp4_block_scale_tab(float amax16, float gs, const float* tab, float& esc) {
+    const uint32_t s = e4m3x2(0.0f, div6(__fmul_rn(amax16, gs))) & 0xffu;
+    esc = tab[s];
+    return s;
+}
+__device__ __forceinline__ void nvfp4_fill_table(float* tab, float gs) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+        const float sv = e4m3_value((uint32_t)i);
+        tab[i] = __fdiv_rn(gs, sv);  // the entries of the two zero codes are never used
+    }
+}
+
+// The eight E2M1 codes of a chunk given the block scale code s and the
+// element factor esc = gs / value(s); every code is 0 when value(s) is 0 (s is
+// +0 or -0), whatever esc.
+__device__ __forceinline__ uint32_t nvfp4_codes_esc(const uint4& o, uint32_t s, float esc) {
+    if ((s & 0x7fu) == 0u) return 0u;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __fmul_rn(lo_f(w_of(o, i)), esc);
+        v[2 * i + 1] = __fmul_rn(hi_f(w_of(o, i)), esc);
+    }
+    return e2m1x8(v);
 }
 
 // The eight E2M1 codes of a chunk, e2m1(RN(y * RN(gs / sv))); 0 when sv is 0.

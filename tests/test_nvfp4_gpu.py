@@ -116,3 +116,17 @@ def test_gated_nvfp4(mbx, bias, D):
     assert_bits_equal(u16(res), want_r, "residual")
     assert_bits_equal(u16(out), want_o, "bf16")
     _check_lossless(q, sf, want_o, gs)
+
+
+@pytest.mark.parametrize("gs", [0.0, 1e-44, 3e38])
+def test_nvfp4_extreme_global_scales(mbx, gs):
+    """A zero global scale (every block scale 0), one so small that gs / value
+    underflows to zero (codes of +-0 keep their sign), and one that saturates
+    every block scale."""
+    g = torch.Generator().manual_seed(17)
+    x = (torch.randn(256, 1024, generator=g) * 2).to(BF16)
+    sc = (0.1 * torch.randn(2, 1024, generator=g)).to(BF16)
+    out, q, sf = mbx.ln_modulate_nvfp4(x.to(DEV), sc.to(DEV), sc.to(DEV), _gs(gs))
+    want = oracle.ln_modulate(u16(x), u16(sc), u16(sc), 1e-6)
+    assert_bits_equal(u16(out), want, "bf16")
+    _check_lossless(q, sf, want, gs)
