@@ -62,6 +62,54 @@ __global__ void __launch_bounds__(kBlock) residual_gate_add_kernel(GateAddParams
     }
 }
 
+// Aligned rows (D % 8 == 0): the tensor as one list of 16-byte chunks, rows
+// back to back, so every thread gets within one chunk of the same share
+// (rows would leave the last round of row slots partly idle).  Each thread
+// issues the loads of kFlatU chunks before it computes and stores them; the
+// row and modulation row of a chunk come from multiply-shift divisions.
+constexpr int kFlatU = 4;
+
+__device__ __forceinline__ unsigned fdiv_u(unsigned n, const FastDiv& f) {
+    return (unsigned)(((unsigned long long)n * f.m) >> f.shift);
+}
+
+template <bool HIGH>
+__global__ void __launch_bounds__(kBlock) residual_gate_add_flat_kernel(GateAddParams p, FastDiv by_nch,
+                                                                        FastDiv by_seq, unsigned total) {
+    const unsigned nch = (unsigned)p.D / kChunk;
+    const unsigned stride = gridDim.x * kBlock * kFlatU;
+    for (unsigned base = blockIdx.x * kBlock * kFlatU + threadIdx.x; base < total; base += stride) {
+        uint4 xv[kFlatU], yv[kFlatU], gv[kFlatU];
+        unsigned row[kFlatU], col[kFlatU];
+#pragma unroll
+        for (int u = 0; u < kFlatU; ++u) {
+            const unsigned q = base + u * kBlock;
+            if (q >= total) continue;
+            row[u] = fdiv_u(q, by_nch);
+            col[u] = q - row[u] * nch;
+            const unsigned mrow = fdiv_u(row[u], by_seq);
+            xv[u] = ld_stream(p.x + (int64_t)row[u] * p.x_stride + col[u] * kChunk);
+            yv[u] = ld_stream(p.y + (int64_t)row[u] * p.y_stride + col[u] * kChunk);
+            gv[u] = ld_shared_row(p.gate + (int64_t)mrow * p.gate_stride + col[u] * kChunk);
+        }
+#pragma unroll
+        for (int u = 0; u < kFlatU; ++u) {
+            const unsigned q = base + u * kBlock;
+            if (q >= total) continue;
+            uint4 o;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t xw = w_of(xv[u], i), yw = w_of(yv[u], i), gw = w_of(gv[u], i);
+                uint32_t ow;
+                if constexpr (!HIGH) ow = badd(xw, bmul(gw, yw));
+                else ow = pack_rn(fmaf(lo_f(gw), lo_f(yw), lo_f(xw)), fmaf(hi_f(gw), hi_f(yw), hi_f(xw)));
+                w_set(o, i, ow);
+            }
+            st_v4(p.out + (int64_t)row[u] * p.out_stride + col[u] * kChunk, o);
+        }
+    }
+}
+
 template <int J, bool VEC, bool HIGH>
 static cudaError_t launch_one(const GateAddParams& p, cudaStream_t s) {
     auto k = residual_gate_add_kernel<J, VEC, HIGH>;
@@ -77,7 +125,21 @@ static cudaError_t launch_j(const GateAddParams& p, bool vec, bool high, cudaStr
     return high ? launch_one<J, false, true>(p, s) : launch_one<J, false, false>(p, s);
 }
 
+template <bool HIGH>
+static cudaError_t launch_flat(const GateAddParams& p, cudaStream_t s) {
+    auto k = residual_gate_add_flat_kernel<HIGH>;
+    const unsigned total = (unsigned)(p.rows * (p.D / kChunk));
+    const int grid = grid_for_rows(reinterpret_cast<const void*>(k), (total + kBlock * kFlatU - 1) / (kBlock * kFlatU), 1, kBlock);
+    if (grid < 0) return cudaErrorUnknown;
+    k<<<grid, kBlock, 0, s>>>(p, make_fastdiv((unsigned)(p.D / kChunk)), make_fastdiv((unsigned)p.seq), total);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_residual_gate_add(const GateAddParams& p, bool vec, bool high, cudaStream_t s) {
+    // the flat form when its 32-bit chunk index fits (and no bias: the
+    // internal bias form stays on the row kernel)
+    if (vec && p.bias == nullptr && p.rows * (p.D / kChunk) < (1ll << 31))
+        return high ? launch_flat<true>(p, s) : launch_flat<false>(p, s);
     switch (chunks_per_lane(p.D)) {
         case 1: return launch_j<1>(p, vec, high, s);
         case 2: return launch_j<2>(p, vec, high, s);
