@@ -98,6 +98,52 @@ __global__ void __launch_bounds__(kTabThreads) modtable_vec_kernel(ModTableParam
     }
 }
 
+// The same with the whole output as one list of chunks (token rows back to
+// back, 6*D/8 chunks each), so that every thread holds within one chunk of
+// the same share; used while that index fits in 32 bits.
+template <bool TAB_F32, bool EMB_F32>
+__global__ void __launch_bounds__(kTabThreads) modtable_flat_kernel(ModTableParams p, FastDiv by_row,
+                                                                    unsigned total) {
+    const unsigned nch = (unsigned)p.D / kChunk, per_row = 6u * nch;
+    const int64_t esz = EMB_F32 ? 4 : 2, tsz = TAB_F32 ? 4 : 2;
+    const unsigned stride = gridDim.x * kTabThreads * kUnroll;
+    for (unsigned base = blockIdx.x * kTabThreads * kUnroll + threadIdx.x; base < total; base += stride) {
+        float e[kUnroll][8];
+        unsigned row[kUnroll], idx[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const unsigned q = base + u * kTabThreads;
+            if (q >= total) continue;
+            row[u] = div_by(q, by_row);
+            idx[u] = q - row[u] * per_row;
+            load8<EMB_F32, true>(static_cast<const char*>(p.temb) + (int64_t)row[u] * p.temb_stride * esz,
+                                 (int64_t)idx[u] * kChunk, e[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const unsigned q = base + u * kTabThreads;
+            if (q >= total) continue;
+            const unsigned k = div_by(idx[u], p.by_nch);
+            const unsigned c = idx[u] - k * nch;
+            float t[8];
+            load8<TAB_F32, false>(static_cast<const char*>(p.table) + (int64_t)k * p.table_stride * tsz,
+                                  (int64_t)c * kChunk, t);
+            uint4 o0, o1;
+            o0.x = __float_as_uint(__fadd_rn(t[0], e[u][0]));
+            o0.y = __float_as_uint(__fadd_rn(t[1], e[u][1]));
+            o0.z = __float_as_uint(__fadd_rn(t[2], e[u][2]));
+            o0.w = __float_as_uint(__fadd_rn(t[3], e[u][3]));
+            o1.x = __float_as_uint(__fadd_rn(t[4], e[u][4]));
+            o1.y = __float_as_uint(__fadd_rn(t[5], e[u][5]));
+            o1.z = __float_as_uint(__fadd_rn(t[6], e[u][6]));
+            o1.w = __float_as_uint(__fadd_rn(t[7], e[u][7]));
+            float* dst = p.out + ((int64_t)k * p.rows + row[u]) * p.out_stride + (int64_t)c * kChunk;
+            st_v4(dst, o0);
+            st_v4(dst + 4, o1);
+        }
+    }
+}
+
 template <bool F32>
 __device__ __forceinline__ float elem(const void* base, int64_t i) {
     if constexpr (F32) return static_cast<const float*>(base)[i];
@@ -122,7 +168,15 @@ __global__ void __launch_bounds__(kTabThreads) modtable_scalar_kernel(ModTablePa
 template <bool TAB_F32, bool EMB_F32>
 static cudaError_t launch_t(const ModTableParams& p0, bool vec, cudaStream_t s) {
     ModTableParams p = p0;
-    if (vec) {
+    const int64_t total = p.rows * 6 * (p.D / kChunk);
+    if (vec && total < (1ll << 31)) {
+        auto k = modtable_flat_kernel<TAB_F32, EMB_F32>;
+        p.by_nch = make_fastdiv((unsigned)(p.D / kChunk));
+        const int grid = grid_for_rows(reinterpret_cast<const void*>(k),
+                                       (total + kTabThreads * kUnroll - 1) / (kTabThreads * kUnroll), 1, kTabThreads);
+        if (grid < 0) return cudaErrorUnknown;
+        k<<<grid, kTabThreads, 0, s>>>(p, make_fastdiv((unsigned)(6 * (p.D / kChunk))), (unsigned)total);
+    } else if (vec) {
         auto k = modtable_vec_kernel<TAB_F32, EMB_F32>;
         p.by_nch = make_fastdiv((unsigned)(p.D / kChunk));
         const int grid = grid_for_rows(reinterpret_cast<const void*>(k), p.rows, 1, kTabThreads);
