@@ -173,6 +173,17 @@ def oracle_rate(budget_s: float, rows_per_call: int = 64):
     return done * per_row / el / 1e9, done, el
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of every rank's `value` (the job time of a weak-scaling run
+    is the slowest rank's); `value` itself when there is one process."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _oracle_share(job):
     """One host process's share of the all-cores oracle baseline: rows
     [lo, hi) of the sample, both operations, for about `budget` seconds."""
@@ -376,10 +387,7 @@ def run_gpu(args):
     total_ms = ev[0].elapsed_time(ev[2 * K])
     ln_ms = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(K))
     rga_ms = sum(ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(K))
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
 
     # end to end: pinned host inputs -> device, both calls, outputs -> host
     e2e = None
