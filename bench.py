@@ -632,7 +632,8 @@ def run_profile_calls(args):
         calls.append(lambda: mbx.ln_modulate(d["x"], d["scale"], d["shift"]))
     elif args.profile_calls == "image":  # the bench kernels plus the fused gated LN, [8704, 3072]
         x, y, res = r(8704, 3072), r(8704, 3072), r(8704, 3072)
-        sc, sh, gt, b = (r(2, 3072, std=0.1) for _ in range(4))
+        sc, sh, gt = (r(2, 3072, std=0.1) for _ in range(3))
+        b = r(1, 3072, std=0.5)
         out, out2 = torch.empty_like(x), torch.empty_like(x)
         calls += [lambda: mbx.ln_modulate(x, sc, sh, out=out),
                   lambda: mbx.residual_gate_add(x, gt, y, out=out),
@@ -640,7 +641,8 @@ def run_profile_calls(args):
     elif args.profile_calls == "next":  # QKV epilogue, gated LN, FP8 LN, modulation table
         q = synth.qkv_epilogue_case(device=dev)
         res, upd = r(8704, 3072), r(8704, 3072)
-        gt, sc, sh, b = (r(2, 3072, std=0.1) for _ in range(4))
+        gt, sc, sh = (r(2, 3072, std=0.1) for _ in range(3))
+        b = r(1, 3072, std=0.5)
         out, out2 = torch.empty_like(res), torch.empty_like(res)
         q8 = torch.empty(8704, 3072, dtype=torch.uint8, device=dev)
         s8 = torch.tensor([0.02], device=dev)
