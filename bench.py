@@ -481,8 +481,9 @@ def run_gpu(args):
 def run_suite(args):
     """Every operation x variant on the configurations' shapes, one JSON line
     per case: device time per call (CUDA events, median of 5 repeats of a
-    rotating loop over buffer sets whose total exceeds L2), GB/s of the
-    algorithmic bytes and the fraction of the measured HBM peak."""
+    rotating loop over buffer sets whose total exceeds L2, with the fastest
+    and slowest repeat as us_min / us_max), GB/s of the algorithmic bytes
+    and the fraction of the measured HBM peak."""
     import torch
 
     import modulation_bit_exact_gb300 as mbx
@@ -492,6 +493,8 @@ def run_suite(args):
     torch.cuda.set_device(dev)
     peak, _ = peaks()
     L2 = 129 * 2 ** 20
+
+    spread = {}  # min and max of the five repeats of the last case timed
 
     def time_cases(make, nbytes, fn):
         per_set = max(1, nbytes)
@@ -511,6 +514,7 @@ def run_suite(args):
             torch.cuda.synchronize(dev)
             times.append(a.elapsed_time(b) / reps * 1e3)
         times.sort()
+        spread.update(lo=round(times[0], 2), hi=round(times[-1], 2))
         return times[2]
 
     def row_case(name, B, S, D, tok):
@@ -555,7 +559,8 @@ def run_suite(args):
                 us = time_cases(make, nb, lambda st: fn(st, v))
                 gbs = nb / (us * 1e-6) / 1e9
                 print(json.dumps({"case": name, "shape": [rows, D], "modulation": "per-token" if tok else "per-sample",
-                                  "op": op, "variant": v, "us_per_call": round(us, 2), "bytes": nb,
+                                  "op": op, "variant": v, "us_per_call": round(us, 2), "us_min": spread["lo"],
+                                  "us_max": spread["hi"], "bytes": nb,
                                   "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}), flush=True)
 
     def qkv_case(name, B, s_txt, gh, gw, H):
@@ -571,7 +576,8 @@ def run_suite(args):
             us = time_cases(make, nb, fn)
             gbs = nb / (us * 1e-6) / 1e9
             print(json.dumps({"case": name, "shape": [B, s_txt, gh * gw, H, hd], "op": "qk_norm_rope_qkv_epilogue",
-                              "variant": v, "us_per_call": round(us, 2), "bytes": nb, "gbs": round(gbs, 1),
+                              "variant": v, "us_per_call": round(us, 2), "us_min": spread["lo"],
+                              "us_max": spread["hi"], "bytes": nb, "gbs": round(gbs, 1),
                               "frac_of_peak": round(gbs / peak, 4)}), flush=True)
 
     def table_case(name, rows, D, tab_dt=torch.float32, emb_dt=torch.bfloat16):
@@ -585,7 +591,8 @@ def run_suite(args):
         us = time_cases(make, nb, lambda st: mbx.modulation_table_add(st["t"], st["e"], out=st["o"]))
         gbs = nb / (us * 1e-6) / 1e9
         print(json.dumps({"case": name, "shape": [rows, 6, D], "op": "modulation_table_add",
-                          "variant": "exact", "us_per_call": round(us, 2), "bytes": nb, "gbs": round(gbs, 1),
+                          "variant": "exact", "us_per_call": round(us, 2), "us_min": spread["lo"],
+                          "us_max": spread["hi"], "bytes": nb, "gbs": round(gbs, 1),
                           "frac_of_peak": round(gbs / peak, 4)}), flush=True)
 
     only = getattr(args, "only", None)
