@@ -432,6 +432,8 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
         const uint4* tm = MODE == kModStaged ? mod + (slot * O::SLOT + 0) * nch : nullptr;
         const uint4* sh = MODE == kModStaged ? tm + nch : nullptr;
         uint16_t* out_row = p.out + row * p.out_stride;
+        uint8_t* const q_row = FP4 ? p.out_fp4 + row * p.out_fp4_stride : nullptr;
+        uint8_t* const sf_row = FP4 ? p.out_sf + nvfp4_sf_row(row, p.sf_col_tiles) : nullptr;
         const u64 mean2 = f2(mean, mean), rstd2 = f2(rstd, rstd);
 #pragma unroll
         for (int j = 0; j < C::J; ++j)
@@ -481,8 +483,8 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                     float esc;
                     const uint32_t sc = nvfp4_block_scale_tab(a16, gs4, fp4_tab, esc);
                     if (valid) {
-                        st_u32(p.out_fp4 + row * p.out_fp4_stride + (int64_t)c * 4, nvfp4_codes_esc(o, sc, esc));
-                        if ((c & 1) == 0) p.out_sf[nvfp4_sf_offset(row, c >> 1, p.sf_col_tiles)] = (uint8_t)sc;
+                        st_u32(q_row + c * 4, nvfp4_codes_esc(o, sc, esc));
+                        if ((c & 1) == 0) sf_row[nvfp4_sf_block(c >> 1)] = (uint8_t)sc;
                     }
                 }
             }

@@ -337,6 +337,11 @@ __device__ __forceinline__ float max_nan(float a, float b) {
 __device__ __forceinline__ int64_t nvfp4_sf_offset(int64_t r, int b, int col_tiles) {
     return ((r >> 7) * col_tiles + (b >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (b & 3);
 }
+// The same split into its row part (once per row) and its block part.
+__device__ __forceinline__ int64_t nvfp4_sf_row(int64_t r, int col_tiles) {
+    return (r >> 7) * col_tiles * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+}
+__device__ __forceinline__ int nvfp4_sf_block(int b) { return (b >> 2) * 512 + (b & 3); }
 
 __device__ __forceinline__ void st_u32(void* p, uint32_t a) {
     asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
@@ -365,16 +370,19 @@ __device__ __forceinline__ void w_set(uint4& v, int i, uint32_t w) {
     else v.w = w;
 }
 
-// |largest| of the eight bf16 values of a chunk, NaN propagating.
+// max.NaN of two bf16 pairs (a max selects an operand: exact)
+__device__ __forceinline__ uint32_t bmax_nan(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// |largest| of the eight bf16 values of a chunk, NaN propagating: the sign
+// bits cleared, pairwise bf16 maxima, then the larger half.
 __device__ __forceinline__ float amax8_bf16(const uint4& o) {
-    float a = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t w = w_of(o, i);
-        a = max_nan(a, fabsf(lo_f(w)));
-        a = max_nan(a, fabsf(hi_f(w)));
-    }
-    return a;
+    const uint32_t m = 0x7fff7fffu;
+    const uint32_t a = bmax_nan(bmax_nan(o.x & m, o.y & m), bmax_nan(o.z & m, o.w & m));
+    return max_nan(lo_f(a), hi_f(a));
 }
 
 // NVFP4 block step: from the block's amax and the global scale gs, the E4M3
@@ -407,14 +415,17 @@ __device__ __forceinline__ void nvfp4_fill_table(float* tab, float gs) {
 
 // The eight E2M1 codes of a chunk given the block scale code s and the
 // element factor esc = gs / value(s); every code is 0 when value(s) is 0 (s is
-// +0 or -0), whatever esc.
+// +0 or -0), whatever esc.  The products are packed (each one rounding; they
+// feed conversions, not sums).
 __device__ __forceinline__ uint32_t nvfp4_codes_esc(const uint4& o, uint32_t s, float esc) {
     if ((s & 0x7fu) == 0u) return 0u;
+    const u64 e2 = f2(esc, esc);
     float v[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        v[2 * i] = __fmul_rn(lo_f(w_of(o, i)), esc);
-        v[2 * i + 1] = __fmul_rn(hi_f(w_of(o, i)), esc);
+        const u64 pr = mul2(widen2(w_of(o, i)), e2);
+        v[2 * i] = f2lo(pr);
+        v[2 * i + 1] = f2hi(pr);
     }
     return e2m1x8(v);
 }
