@@ -482,8 +482,10 @@ def run_suite(args):
     """Every operation x variant on the configurations' shapes, one JSON line
     per case: device time per call (CUDA events, median of 5 repeats of a
     rotating loop over buffer sets whose total exceeds L2, with the fastest
-    and slowest repeat as us_min / us_max), GB/s of the algorithmic bytes
-    and the fraction of the measured HBM peak."""
+    and slowest repeat as us_min / us_max; for calls under 64 MB also the
+    device time per call through a CUDA graph, us_device, which leaves out
+    host submission), GB/s of the algorithmic bytes and the fraction of the
+    measured HBM peak."""
     import torch
 
     import modulation_bit_exact_gb300 as mbx
@@ -496,10 +498,44 @@ def run_suite(args):
 
     spread = {}  # min and max of the five repeats of the last case timed
 
+    def time_graph(sets, fn, calls=64):
+        """Device time per call without host submission: `calls` launches
+        over the rotating sets captured in one CUDA graph, replayed five
+        times (median).  None if capture is refused."""
+        try:
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                for i in range(len(sets)):
+                    fn(sets[i])
+            torch.cuda.current_stream(dev).wait_stream(side)
+            torch.cuda.synchronize(dev)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="relaxed"):
+                for i in range(calls):
+                    fn(sets[i % len(sets)])
+            g.replay()
+            torch.cuda.synchronize(dev)
+            ts = []
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                b.record()
+                torch.cuda.synchronize(dev)
+                ts.append(a.elapsed_time(b) / calls * 1e3)
+            del g
+            return round(sorted(ts)[2], 2)
+        except Exception:
+            torch.cuda.synchronize(dev)
+            return None
+
     def time_cases(make, nbytes, fn):
         per_set = max(1, nbytes)
         nsets = max(2, min(8, int(3 * L2 // per_set) + 1))
         sets = [make(i) for i in range(nsets)]
+        # small calls: the device time through a CUDA graph as well
+        spread["device"] = time_graph(sets, fn) if nbytes < 64 * 2 ** 20 else None
         for i in range(3 * nsets):
             fn(sets[i % nsets])
         torch.cuda.synchronize(dev)
@@ -560,7 +596,7 @@ def run_suite(args):
                 gbs = nb / (us * 1e-6) / 1e9
                 print(json.dumps({"case": name, "shape": [rows, D], "modulation": "per-token" if tok else "per-sample",
                                   "op": op, "variant": v, "us_per_call": round(us, 2), "us_min": spread["lo"],
-                                  "us_max": spread["hi"], "bytes": nb,
+                                  "us_max": spread["hi"], "us_device": spread["device"], "bytes": nb,
                                   "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}), flush=True)
 
     def qkv_case(name, B, s_txt, gh, gw, H):
@@ -601,12 +637,16 @@ def run_suite(args):
             table_case("Wan2.2-TI2V table [1,109120,6,3072] bf16 temb", 31 * 44 * 80, 3072)
             table_case("video table [1,32760,6,5120] bf16 temb", 32760, 5120)
             table_case("video table [1,32760,6,5120] f32 temb", 32760, 5120, emb_dt=torch.float32)
+        if "tiny" in only:
+            row_case("tiny [2,256,512]", 2, 256, 512, False)
+            row_case("sweep [77,3072]", 1, 77, 3072, False)
         if "image" in only:
             row_case("image-DiT [2,4352,3072]", 2, 4352, 3072, False)
         if "video" in only:
             row_case("video-DiT [1,32760,5120] per-token", 1, 32760, 5120, True)
         return 0
     row_case("tiny [2,256,512]", 2, 256, 512, False)
+    row_case("sweep [77,3072]", 1, 77, 3072, False)
     row_case("image-DiT [2,4352,3072]", 2, 4352, 3072, False)
     qkv_case("QKV epilogue [2,256+64x64,24x128]", 2, 256, 64, 64, 24)
     row_case("video-DiT [1,32760,5120] per-token", 1, 32760, 5120, True)
@@ -677,7 +717,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", default="mbx", choices=["mbx", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", default=None, help="with --suite: run only the named groups (table, image, video)")
+    ap.add_argument("--only", default=None, help="with --suite: run only the named groups (tiny, image, video, table)")
     ap.add_argument("--suite", action="store_true",
                     help="time every operation and variant on the configurations' shapes "
                          "(one JSON line per case) instead of the benchmark step")
