@@ -391,38 +391,38 @@ def run_gpu(args):
 
     # end to end: pinned host inputs -> device, both calls, outputs -> host
     e2e = None
-    if rank == 0 or True:
-        host = {k: torch.empty(sets[0][0][k].shape, dtype=torch.bfloat16, pin_memory=True)
-                for k in ("x", "xb", "y", "scale", "shift", "gate", "out1", "out2")}
+    # every rank measures its own replica end to end; the slowest is reported
+    host = {k: torch.empty(sets[0][0][k].shape, dtype=torch.bfloat16, pin_memory=True)
+            for k in ("x", "xb", "y", "scale", "shift", "gate", "out1", "out2")}
+    for k in ("x", "xb", "y", "scale", "shift", "gate"):
+        host[k].copy_(sets[0][0][k])
+    dsets = sets[0]
+    n_e2e = max(3, min(50, K // 100))
+
+    def e2e_step():
+        s, v = dsets
         for k in ("x", "xb", "y", "scale", "shift", "gate"):
-            host[k].copy_(sets[0][0][k])
-        dsets = sets[0]
-        n_e2e = max(3, min(50, K // 100))
+            s[k].copy_(host[k], non_blocking=True)
+        L.mbx_ln_modulate(ref(v["out1"]), ref(v["x"]), ref(v["scale"]), ref(v["shift"]), eps, 0, sptr)
+        L.mbx_residual_gate_add(ref(v["out2"]), ref(v["xb"]), ref(v["gate"]), ref(v["y"]), 0, sptr)
+        host["out1"].copy_(s["out1"], non_blocking=True)
+        host["out2"].copy_(s["out2"], non_blocking=True)
 
-        def e2e_step():
-            s, v = dsets
-            for k in ("x", "xb", "y", "scale", "shift", "gate"):
-                s[k].copy_(host[k], non_blocking=True)
-            L.mbx_ln_modulate(ref(v["out1"]), ref(v["x"]), ref(v["scale"]), ref(v["shift"]), eps, 0, sptr)
-            L.mbx_residual_gate_add(ref(v["out2"]), ref(v["xb"]), ref(v["gate"]), ref(v["y"]), 0, sptr)
-            host["out1"].copy_(s["out1"], non_blocking=True)
-            host["out2"].copy_(s["out2"], non_blocking=True)
-
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = e0.elapsed_time(e1) / n_e2e
-        h2d = sum(host[k].numel() * 2 for k in ("x", "xb", "y", "scale", "shift", "gate"))
-        d2h = sum(host[k].numel() * 2 for k in ("out1", "out2"))
-        e2e = {"value": round(STEP_BYTES * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(e2e_ms, 4), "steps": n_e2e}
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dist, dev)
+    h2d = sum(host[k].numel() * 2 for k in ("x", "xb", "y", "scale", "shift", "gate"))
+    d2h = sum(host[k].numel() * 2 for k in ("out1", "out2"))
+    e2e = {"value": round(STEP_BYTES * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": round(e2e_ms, 4), "steps": n_e2e}
 
     if rank != 0:
         if dist:
@@ -445,8 +445,15 @@ def run_gpu(args):
             "frac": kern[dom]["frac"], "traffic": dram_traffic(dom), "kernel": dom,
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
             else "fallback 6.8 TB/s"}
-    cpu_gbs, cpu_rows, cpu_s = oracle_rate(args.cpu_seconds)
-    all_gbs, all_rows, all_s, all_n = oracle_rate_all_cores(args.cpu_seconds)
+    cpu = None
+    if world == 1:  # the oracle on this host's cores, timed at N = 1 only
+        cpu_gbs, cpu_rows, cpu_s = oracle_rate(args.cpu_seconds)
+        all_gbs, all_rows, all_s, all_n = oracle_rate_all_cores(args.cpu_seconds)
+        cpu = {"value": round(all_gbs, 4), "unit": "GB/s", "cores": all_n, "kind": "oracle",
+               "sample": f"{all_rows} rows of the workload (both operations) in {all_s:.1f} s, "
+                         f"{all_n} processes, one per host core, each on a static share of the "
+                         f"rows; single thread: {cpu_gbs:.4f} GB/s ({cpu_rows} rows in {cpu_s:.1f} s)",
+               "value_1_thread": round(cpu_gbs, 4)}
     value = STEP_BYTES * K * world / (total_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -460,11 +467,7 @@ def run_gpu(args):
         "frac_of_8tbs_spec": round(value / world / 8000.0, 4),
         "kernels": kern,
         "roofline": roof,
-        "cpu_baseline": {"value": round(all_gbs, 4), "unit": "GB/s", "cores": all_n, "kind": "oracle",
-                         "sample": f"{all_rows} rows of the workload (both operations) in {all_s:.1f} s, "
-                                   f"{all_n} processes, one per host core, each on a static share of the "
-                                   f"rows; single thread: {cpu_gbs:.4f} GB/s ({cpu_rows} rows in {cpu_s:.1f} s)",
-                         "value_1_thread": round(cpu_gbs, 4)},
+        "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 2 * K * world,
         "clocks": clocks.summary(),
