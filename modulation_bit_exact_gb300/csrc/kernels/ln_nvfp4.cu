@@ -3,6 +3,13 @@
 // kernel's store pass (instantiated here with FP4 = true, apart from the
 // plain kernels), or, for rows the ring kernel does not take, from the written
 // bf16 output by the separate quantiser.
+//
+// "Agent-assisted SGLang diffusion kernel optimisation: Qwen-Image, FLUX.2 and
+// video models" (tahou.com), section 将FP8量化融合到前序算子, NVFP4 part: the
+// residual update, layer_norm and (1 + scale)/shift chain ending in
+// fp4_quantize, one kernel writing E2M1 packed values and 128x4-swizzled E4M3
+// block scales.  The block rule and the tile order are stated with
+// mbx_ln_modulate_nvfp4 in the public header.
 #include "ln_pipe.cuh"
 
 namespace mbx {

@@ -2,6 +2,12 @@
 // modulate kernel and its launch helpers, shared by the translation units
 // that instantiate it (ln_modulate.cu: plain, gated and FP8 outputs;
 // ln_nvfp4.cu: the NVFP4 output).
+//
+// The operation and its lossless rounding order are defined at the top of
+// ln_modulate.cu ("Agent-assisted SGLang diffusion kernel optimisation"
+// (tahou.com), section 扩散Kernel对数值精度的敏感性); the gated front pass and
+// the FP8/NVFP4 stores follow the section 将FP8量化融合到前序算子 and the
+// gated-residual chain of section Qwen-Image FP8和NVFP4优化 of the same article.
 #pragma once
 #include "launch.h"
 #include "rowops.cuh"
