@@ -130,3 +130,24 @@ def test_nvfp4_extreme_global_scales(mbx, gs):
     want = oracle.ln_modulate(u16(x), u16(sc), u16(sc), 1e-6)
     assert_bits_equal(u16(out), want, "bf16")
     _check_lossless(q, sf, want, gs)
+
+
+def test_nvfp4_and_fp8_non_finite_rows(mbx):
+    """Rows holding inf or NaN make NaN outputs (0x7FFF); their NVFP4 blocks get
+    the NaN scale code 0x7F and codes 0x7, their FP8 bytes 0x7F, as in the
+    oracle.  Finite rows next to them are unaffected."""
+    g = torch.Generator().manual_seed(23)
+    rows, D = 64, 1024
+    x = torch.randn(rows, D, generator=g)
+    x[3, 5] = float("inf")
+    x[7, 100] = float("nan")
+    x[9, :] = -float("inf")
+    x = x.to(BF16)
+    sc = (0.1 * torch.randn(2, D, generator=g)).to(BF16)
+    out, q, sf = mbx.ln_modulate_nvfp4(x.to(DEV), sc.to(DEV), sc.to(DEV), _gs(100.0))
+    want = oracle.ln_modulate(u16(x), u16(sc), u16(sc), 1e-6)
+    assert_bits_equal(u16(out), want, "bf16")
+    _check_lossless(q, sf, want, 100.0)
+    out8, q8 = mbx.ln_modulate_fp8(x.to(DEV), sc.to(DEV), sc.to(DEV), _gs(0.05))
+    assert_bits_equal(u16(out8), want, "bf16 (fp8 call)")
+    assert_bits_equal(_b(q8.view(torch.uint8)), oracle.quant_e4m3(want, 0.05), "e4m3")
