@@ -218,11 +218,16 @@ enum { kModRing = 0, kModStaged = 1 };
 // the update (FUSED), then, in ring mode, scale, shift and the gate (FUSED).
 template <bool FUSED, int MODE>
 struct LnOps {
+    // unfused, per-row modulation: scale and shift are read from global memory
+    // into registers when the row's data has landed (their latency hides
+    // behind the statistics), so the ring carries x alone and more row
+    // groups fit in shared memory
+    static constexpr bool DIRECT = !FUSED && MODE == kModRing;
     static constexpr int U = FUSED ? 1 : -1;
-    static constexpr int SC = MODE == kModRing ? (FUSED ? 2 : 1) : -1;
-    static constexpr int SH = MODE == kModRing ? SC + 1 : -1;
+    static constexpr int SC = MODE == kModRing && FUSED ? 2 : -1;
+    static constexpr int SH = MODE == kModRing && FUSED ? SC + 1 : -1;
     static constexpr int G = MODE == kModRing && FUSED ? SH + 1 : -1;
-    static constexpr int N = 1 + (FUSED ? 1 : 0) + (MODE == kModRing ? (FUSED ? 3 : 2) : 0);
+    static constexpr int N = 1 + (FUSED ? 1 : 0) + (MODE == kModRing && FUSED ? 3 : 0);
     static constexpr int SLOT = FUSED ? 3 : 2;  // staged arrays per sample: t, shift[, gate]
 };
 
@@ -255,6 +260,7 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
     const int64_t split = (m0 + 1) * p.seq;  // staged: rows from here use slot 1
     const int64_t first = r0 + g;
     RowDiv next(first, groups, p.seq);  // modulation row of the next row to issue
+    RowDiv here(first, groups, p.seq);  // modulation row of the row being processed
     // FP8 producer: 1/scale correctly rounded, once per thread
     const float inv8 = p.out_fp8 != nullptr ? __fdiv_rn(1.0f, __ldg(p.fp8_scale)) : 0.0f;
     // NVFP4 copy: the global scale, and gs / value(s) for every E4M3 code s
@@ -265,11 +271,11 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
     auto issue = [&](int s, int64_t row) {
         ring.issue(s, 0, p.x + row * p.x_stride, t, nch);
         if constexpr (FUSED) ring.issue(s, O::U, p.update + row * p.update_stride, t, nch);
-        if constexpr (MODE == kModRing) {
+        if constexpr (MODE == kModRing && FUSED) {
             const int64_t mrow = next.q;
             ring.issue(s, O::SC, p.scale + mrow * p.scale_stride, t, nch);
             ring.issue(s, O::SH, p.shift + mrow * p.shift_stride, t, nch);
-            if constexpr (FUSED) ring.issue(s, O::G, p.gate + mrow * p.gate_stride, t, nch);
+            ring.issue(s, O::G, p.gate + mrow * p.gate_stride, t, nch);
         }
     };
 #pragma unroll
@@ -317,6 +323,22 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
         cp_async_commit();
         cp_async_wait<NS - 1>();
         const int slot = row >= split ? 1 : 0;
+        // DIRECT: this row's scale and shift chunks, in flight during the statistics
+        uint4 dT[O::DIRECT ? C::J : 1][O::DIRECT ? C::M : 1], dSH[O::DIRECT ? C::J : 1][O::DIRECT ? C::M : 1];
+        if constexpr (O::DIRECT) {
+            const uint16_t* sc_row = p.scale + here.q * p.scale_stride;
+            const uint16_t* sh_row = p.shift + here.q * p.shift_stride;
+#pragma unroll
+            for (int j = 0; j < C::J; ++j)
+#pragma unroll
+                for (int m = 0; m < C::M; ++m) {
+                    const int c = t + C::TPR * m + kLanes * j;
+                    if (c < nch) {
+                        dT[j][m] = ld_stream(sc_row + (int64_t)c * kChunk);
+                        dSH[j][m] = ld_stream(sh_row + (int64_t)c * kChunk);
+                    }
+                }
+        }
 
         if constexpr (FUSED) {
             // front pass: the new residual r' = bf16(x + bf16(gate * a)), written
@@ -457,6 +479,9 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                 if constexpr (MODE == kModStaged) {
                     T = lds16(tm + c);
                     SH = lds16(sh + c);
+                } else if constexpr (O::DIRECT) {
+                    T = dT[O::DIRECT ? j : 0][O::DIRECT ? m : 0];
+                    SH = dSH[O::DIRECT ? j : 0][O::DIRECT ? m : 0];
                 } else {
                     T = lds16(ring.at(cur, O::SC > 0 ? O::SC : 0, c));
                     SH = lds16(ring.at(cur, O::SH > 0 ? O::SH : 0, c));
@@ -495,6 +520,7 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                 }
             }
         cur = cur + 1 == NS ? 0 : cur + 1;
+        if constexpr (O::DIRECT) here.advance();
     }
     cp_async_wait<0>();
 }
