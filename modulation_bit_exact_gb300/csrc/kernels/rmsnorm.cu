@@ -230,12 +230,16 @@ struct RmsPipeArgs<kRmsScale> {
     using P = RmsScaleParams;
     static __device__ const uint16_t* mod(const P& p) { return p.scale; }
     static __device__ int64_t mod_stride(const P& p) { return p.scale_stride; }
+    static __device__ const uint16_t* residual(const P&) { return nullptr; }
+    static __device__ int64_t res_stride(const P&) { return 0; }
 };
 template <>
 struct RmsPipeArgs<kRmsTanh> {
     using P = RmsTanhParams;
     static __device__ const uint16_t* mod(const P& p) { return p.gate; }
     static __device__ int64_t mod_stride(const P& p) { return p.gate_stride; }
+    static __device__ const uint16_t* residual(const P& p) { return p.residual; }
+    static __device__ int64_t res_stride(const P& p) { return p.res_stride; }
 };
 
 // Sum of bf16(x*x) per lane, chunks read from ring stage s (absent chunks
@@ -309,11 +313,12 @@ template <int TPR, int J, int NS, bool HIGH, int OP, int MODE>
 __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeArgs<OP>::P p, int64_t rows_per_cta) {
     using A = RmsPipeArgs<OP>;
     using C = RowCfg<TPR, J, true>;
-    // ring operands: x, [mod when not staged], [residual for the tanh op]
-    constexpr int OP_MOD = MODE == kRmsModRing ? 1 : -1;
-    constexpr int OP_RES = OP == kRmsTanh ? (MODE == kRmsModRing ? 2 : 1) : -1;
-    constexpr int NOPS = 1 + (MODE == kRmsModRing ? 1 : 0) + (OP == kRmsTanh ? 1 : 0);
-    using R = Ring<C, NS, NOPS>;
+    // the ring holds x alone: it is read twice (sum of squares, output), while a
+    // per-row modulation row and the tanh op's residual are read once, by the
+    // output pass, and go straight from global memory into registers
+    constexpr bool DMOD = MODE == kRmsModRing;
+    constexpr bool DRES = OP == kRmsTanh;
+    using R = Ring<C, NS, 1>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int groups = blockDim.x / TPR;
     const int g = threadIdx.x / TPR, t = threadIdx.x % TPR;
@@ -333,18 +338,13 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeAr
     const uint16_t* modp = A::mod(p);
     const int64_t mod_stride = A::mod_stride(p);
     const int64_t first = r0 + g;
-    RowDiv next(first, groups, p.seq);  // modulation row of the next row to issue
+    RowDiv here(first, groups, p.seq);  // modulation row of the row being processed
 
-    auto issue = [&](int s, int64_t row) {
-        ring.issue(s, 0, p.x + row * p.x_stride, t, nch);
-        if constexpr (OP_MOD >= 0) ring.issue(s, OP_MOD, modp + next.q * mod_stride, t, nch);
-        if constexpr (OP_RES >= 0) ring.issue(s, OP_RES, p.residual + row * p.res_stride, t, nch);
-    };
+    auto issue = [&](int s, int64_t row) { ring.issue(s, 0, p.x + row * p.x_stride, t, nch); };
 #pragma unroll
     for (int s = 0; s < NS - 1; ++s) {
         const int64_t r = first + s * groups;
         if (r < r1) issue(s, r);
-        if constexpr (MODE == kRmsModRing) next.advance();
         cp_async_commit();
     }
     // the first rows are on their way; stage the per-CTA data meanwhile
@@ -373,9 +373,25 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeAr
         const int64_t rn = row + (NS - 1) * groups;
         const int sn = cur == 0 ? NS - 1 : cur - 1;
         if (rn < r1) issue(sn, rn);
-        if constexpr (MODE == kRmsModRing) next.advance();
         cp_async_commit();
         cp_async_wait<NS - 1>();
+
+        // this row's modulation and residual chunks, in flight during the reduction
+        uint4 dMD[DMOD ? C::J : 1][DMOD ? C::M : 1], dRS[DRES ? C::J : 1][DRES ? C::M : 1];
+        {
+            const uint16_t* md_row = modp + here.q * mod_stride;
+            const uint16_t* rs_row = nullptr;
+            if constexpr (DRES) rs_row = A::residual(p) + row * A::res_stride(p);
+#pragma unroll
+            for (int j = 0; j < C::J; ++j)
+#pragma unroll
+                for (int m = 0; m < C::M; ++m) {
+                    const int c = t + C::TPR * m + kLanes * j;
+                    if (c >= nch) continue;
+                    if constexpr (DMOD) dMD[DMOD ? j : 0][DMOD ? m : 0] = ld_stream(md_row + (int64_t)c * kChunk);
+                    if constexpr (DRES) dRS[DRES ? j : 0][DRES ? m : 0] = ld_stream(rs_row + (int64_t)c * kChunk);
+                }
+        }
 
         float L[C::M];
         if constexpr (!HIGH) sumsq_stage<C>(ring, cur, t, nch, L);
@@ -405,9 +421,9 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeAr
                 const uint4 W = lds16(wsm + c);
                 uint4 MD;
                 if constexpr (MODE == kRmsModStaged) MD = lds16(mrow + c);
-                else MD = lds16(ring.at(cur, OP_MOD > 0 ? OP_MOD : 0, c));
+                else MD = dMD[DMOD ? j : 0][DMOD ? m : 0];
                 uint4 RS = make_uint4(0, 0, 0, 0);
-                if constexpr (OP_RES >= 0) RS = lds16(ring.at(cur, OP_RES, c));
+                if constexpr (DRES) RS = dRS[DRES ? j : 0][DRES ? m : 0];
                 uint4 o;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -435,6 +451,7 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeAr
                 st_v4(out_row + (int64_t)c * kChunk, o);
             }
         cur = cur + 1 == NS ? 0 : cur + 1;
+        if constexpr (DMOD) here.advance();
     }
     cp_async_wait<0>();
 }
@@ -443,8 +460,7 @@ template <int TPR, int J, int NS, bool HIGH, int OP, int MODE>
 static cudaError_t launch_rms_pipe(const typename RmsPipeArgs<OP>::P& p, cudaStream_t s) {
     auto k = rmsnorm_pipe_kernel<TPR, J, NS, HIGH, OP, MODE>;
     using C = RowCfg<TPR, J, true>;
-    constexpr int NOPS = 1 + (MODE == kRmsModRing ? 1 : 0) + (OP == kRmsTanh ? 1 : 0);
-    using R = Ring<C, NS, NOPS>;
+    using R = Ring<C, NS, 1>;
     const int nch = p.D / kChunk;
     const int tab_bytes = OP == kRmsTanh && MODE == kRmsModRing ? (((MBX_TANH_HI - MBX_TANH_LO) + 7) / 8) * 16 : 0;
     const int fixed = nch * 16 + (MODE == kRmsModStaged ? 2 * nch * 16 : 0) + tab_bytes;
