@@ -153,6 +153,27 @@ struct QkvParams {
     FastDiv by_hpass;  // unit -> token
 };
 
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel in the stream drains, and calls grid_dep_wait() before
+// it touches global memory that kernel may use.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl(void (*k)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k, args...);
+    const cudaError_t last = cudaGetLastError();
+    return e != cudaSuccess ? e : last;
+}
+
 // ceil(ceil(D / 8) / 128): chunks per lane of a row of D elements.
 inline int chunks_per_lane(int D) { return ((D + 7) / 8 + 127) / 128; }
 

@@ -92,6 +92,8 @@ __device__ __forceinline__ void welford_lanes(const uint4 (&v)[C::M][C::J], int 
 
 template <int TPR, int J, bool VEC, bool HIGH>
 __global__ void __launch_bounds__(kBlock) ln_modulate_kernel(LnModParams p) {
+    grid_dep_wait();  // launched programmatically: the previous kernel has finished
+    grid_dep_launch();
     using C = RowCfg<TPR, J, VEC>;
     __shared__ TreeSmem smem[C::RPC];
     const RowLoop rl = row_loop<C>();
@@ -196,8 +198,7 @@ static cudaError_t launch_one(const LnModParams& p, cudaStream_t s) {
     auto k = ln_modulate_kernel<TPR, J, VEC, HIGH>;
     int grid = grid_for_rows(reinterpret_cast<const void*>(k), p.rows, kBlock / TPR, kBlock);
     if (grid < 0) return cudaErrorUnknown;
-    k<<<grid, kBlock, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(k, grid, kBlock, 0, s, p);
 }
 
 template <int TPR, int J>

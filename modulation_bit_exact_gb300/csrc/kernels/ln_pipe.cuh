@@ -236,6 +236,9 @@ __device__ __forceinline__ void sts16(uint4* p, uint4 v) {
     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// rows per group brought into L2 before the wait on the previous kernel
+constexpr int kPrefetchRows = 2;
+
 template <int TPR, int J, int NS, bool HIGH, int MODE, bool FUSED, bool FP4>
 __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p, int64_t rows_per_cta) {
     using C = RowCfg<TPR, J, true>;
@@ -261,6 +264,22 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
     const int64_t first = r0 + g;
     RowDiv next(first, groups, p.seq);  // modulation row of the next row to issue
     RowDiv here(first, groups, p.seq);  // modulation row of the row being processed
+    // while the previous kernel in the stream drains, bring this group's first
+    // rows into L2; then wait for it before reading anything it may write
+    if (t == 0)
+#pragma unroll
+        for (int s = 0; s < kPrefetchRows; ++s) {
+            const int64_t r = first + s * groups;
+            if (r >= r1) break;
+            prefetch_l2_bulk(p.x + r * p.x_stride, (uint32_t)D * 2);
+            if constexpr (FUSED) prefetch_l2_bulk(p.update + r * p.update_stride, (uint32_t)D * 2);
+            if constexpr (O::DIRECT) {
+                prefetch_l2_bulk(p.scale + r / p.seq * p.scale_stride, (uint32_t)D * 2);
+                prefetch_l2_bulk(p.shift + r / p.seq * p.shift_stride, (uint32_t)D * 2);
+            }
+        }
+    grid_dep_wait();
+    grid_dep_launch();
     // FP8 producer: 1/scale correctly rounded, once per thread
     const float inv8 = p.out_fp8 != nullptr ? __fdiv_rn(1.0f, __ldg(p.fp8_scale)) : 0.0f;
     // NVFP4 copy: the global scale, and gs / value(s) for every E4M3 code s
@@ -538,8 +557,7 @@ static cudaError_t launch_pipe(const LnModParams& p, cudaStream_t s) {
     PipeShape sh;
     if (!pipe_shape(reinterpret_cast<const void*>(k), TPR, (int)sizeof(TreeSmem) + R::kBytes, fixed, p.rows, &sh))
         return cudaErrorInvalidConfiguration;
-    k<<<sh.grid, sh.groups * TPR, sh.smem, s>>>(p, sh.rows_per_cta);
-    return cudaGetLastError();
+    return launch_pdl(k, sh.grid, sh.groups * TPR, sh.smem, s, p, sh.rows_per_cta);
 }
 
 template <int TPR, int J, int NS, bool FUSED, bool FP4>

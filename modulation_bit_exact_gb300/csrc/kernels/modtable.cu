@@ -60,6 +60,8 @@ __device__ __forceinline__ void load8(const void* row, int64_t e, float (&v)[8])
 
 template <bool TAB_F32, bool EMB_F32>
 __global__ void __launch_bounds__(kTabThreads) modtable_vec_kernel(ModTableParams p) {
+    grid_dep_wait();  // launched programmatically: the previous kernel has finished
+    grid_dep_launch();
     const int nch = p.D / kChunk;
     const unsigned per_row = 6u * (unsigned)nch;
     const int64_t esz = EMB_F32 ? 4 : 2, tsz = TAB_F32 ? 4 : 2;
@@ -104,6 +106,8 @@ __global__ void __launch_bounds__(kTabThreads) modtable_vec_kernel(ModTableParam
 template <bool TAB_F32, bool EMB_F32>
 __global__ void __launch_bounds__(kTabThreads) modtable_flat_kernel(ModTableParams p, FastDiv by_row,
                                                                     unsigned total) {
+    grid_dep_wait();  // launched programmatically: the previous kernel has finished
+    grid_dep_launch();
     const unsigned nch = (unsigned)p.D / kChunk, per_row = 6u * nch;
     const int64_t esz = EMB_F32 ? 4 : 2, tsz = TAB_F32 ? 4 : 2;
     const unsigned stride = gridDim.x * kTabThreads * kUnroll;
@@ -153,6 +157,8 @@ __device__ __forceinline__ float elem(const void* base, int64_t i) {
 // Any alignment, any D: one element per step, the same addition.
 template <bool TAB_F32, bool EMB_F32>
 __global__ void __launch_bounds__(kTabThreads) modtable_scalar_kernel(ModTableParams p, FastDiv by_d) {
+    grid_dep_wait();  // launched programmatically: the previous kernel has finished
+    grid_dep_launch();
     const unsigned per_row = 6u * (unsigned)p.D;
     for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
         for (unsigned i = threadIdx.x; i < per_row; i += kTabThreads) {
@@ -175,20 +181,19 @@ static cudaError_t launch_t(const ModTableParams& p0, bool vec, cudaStream_t s) 
         const int grid = grid_for_rows(reinterpret_cast<const void*>(k),
                                        (total + kTabThreads * kUnroll - 1) / (kTabThreads * kUnroll), 1, kTabThreads);
         if (grid < 0) return cudaErrorUnknown;
-        k<<<grid, kTabThreads, 0, s>>>(p, make_fastdiv((unsigned)(6 * (p.D / kChunk))), (unsigned)total);
+        return launch_pdl(k, grid, kTabThreads, 0, s, p, make_fastdiv((unsigned)(6 * (p.D / kChunk))), (unsigned)total);
     } else if (vec) {
         auto k = modtable_vec_kernel<TAB_F32, EMB_F32>;
         p.by_nch = make_fastdiv((unsigned)(p.D / kChunk));
         const int grid = grid_for_rows(reinterpret_cast<const void*>(k), p.rows, 1, kTabThreads);
         if (grid < 0) return cudaErrorUnknown;
-        k<<<grid, kTabThreads, 0, s>>>(p);
+        return launch_pdl(k, grid, kTabThreads, 0, s, p);
     } else {
         auto k = modtable_scalar_kernel<TAB_F32, EMB_F32>;
         const int grid = grid_for_rows(reinterpret_cast<const void*>(k), p.rows, 1, kTabThreads);
         if (grid < 0) return cudaErrorUnknown;
-        k<<<grid, kTabThreads, 0, s>>>(p, make_fastdiv((unsigned)p.D));
+        return launch_pdl(k, grid, kTabThreads, 0, s, p, make_fastdiv((unsigned)p.D));
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_modulation_table_add(const ModTableParams& p, bool vec, cudaStream_t s) {

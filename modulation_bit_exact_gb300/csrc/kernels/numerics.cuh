@@ -254,6 +254,24 @@ __device__ __forceinline__ Wf wf_shfl_down(Wf v, int s, unsigned mask = 0xffffff
 
 // ---------------------------------------------------------------- memory
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may begin while the kernel before it in the stream is still
+// running, so it touches no global memory that kernel may read or write until
+// grid_dep_wait() has returned (the earlier grid has completed and its writes
+// are visible).  grid_dep_launch() lets the next kernel in the stream begin
+// launching; that kernel's own wait still covers this whole grid.  Both are
+// no-ops in a kernel launched without the attribute.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Bring [p, p + n) into L2 (p 16-byte aligned, n a multiple of 16), or the
+// line holding p.  L2 is the device's point of coherence: a write the earlier
+// kernel makes after the prefetch lands in the L2 copy, so a prefetch may be
+// issued before grid_dep_wait().
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t n) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
 // 16-byte streaming load (read once: not kept in L1).
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
     uint4 v;

@@ -75,6 +75,8 @@ __device__ __forceinline__ QkvUnit qkv_unit(const QkvParams& p, int64_t tok) {
 
 template <int TPH, bool HIGH>
 __global__ void __launch_bounds__(512) qkv_epilogue_kernel(QkvParams p) {
+    grid_dep_wait();  // launched programmatically: the previous kernel has finished
+    grid_dep_launch();
     constexpr int HD = TPH * kChunk;
     const int l = threadIdx.x % TPH;     // chunk / lane within the head
     const int slot = threadIdx.x / TPH;  // head unit within the CTA
@@ -198,8 +200,7 @@ static cudaError_t launch_one(const QkvParams& p0, cudaStream_t s) {
     p.by_hpass = make_fastdiv((unsigned)p.hpasses);
     int grid = grid_for_rows(reinterpret_cast<const void*>(k), tokens * p.hpasses, 1, block);
     if (grid < 0) return cudaErrorUnknown;
-    k<<<grid, block, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(k, grid, block, 0, s, p);
 }
 
 cudaError_t launch_qkv_epilogue(const QkvParams& p, bool high, cudaStream_t s) {

@@ -13,6 +13,8 @@ namespace mbx {
 
 template <int J, bool VEC, bool HIGH>
 __global__ void __launch_bounds__(kBlock) residual_gate_add_kernel(GateAddParams p) {
+    grid_dep_wait();  // launched programmatically: the previous kernel has finished
+    grid_dep_launch();
     using C = RowCfg<128, J, VEC>;  // one 128-thread group per row, no reduction
     const RowLoop rl = row_loop<C>();
     const int D = p.D;
@@ -78,6 +80,18 @@ __global__ void __launch_bounds__(kBlock) residual_gate_add_flat_kernel(GateAddP
                                                                         FastDiv by_seq, unsigned total) {
     const unsigned nch = (unsigned)p.D / kChunk;
     const unsigned stride = gridDim.x * kBlock * kFlatU;
+    // while the previous kernel in the stream drains, bring this thread's
+    // first chunks of x and y into L2; then wait for it
+#pragma unroll
+    for (int u = 0; u < kFlatU; ++u) {
+        const unsigned q = blockIdx.x * kBlock * kFlatU + threadIdx.x + u * kBlock;
+        if (q >= total) break;
+        const unsigned row = fdiv_u(q, by_nch), col = q - row * nch;
+        prefetch_l2(p.x + (int64_t)row * p.x_stride + col * kChunk);
+        prefetch_l2(p.y + (int64_t)row * p.y_stride + col * kChunk);
+    }
+    grid_dep_wait();
+    grid_dep_launch();
     for (unsigned base = blockIdx.x * kBlock * kFlatU + threadIdx.x; base < total; base += stride) {
         uint4 xv[kFlatU], yv[kFlatU], gv[kFlatU];
         unsigned row[kFlatU], col[kFlatU];
@@ -115,8 +129,7 @@ static cudaError_t launch_one(const GateAddParams& p, cudaStream_t s) {
     auto k = residual_gate_add_kernel<J, VEC, HIGH>;
     int grid = grid_for_rows(reinterpret_cast<const void*>(k), p.rows, kBlock / 128, kBlock);
     if (grid < 0) return cudaErrorUnknown;
-    k<<<grid, kBlock, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(k, grid, kBlock, 0, s, p);
 }
 
 template <int J>
@@ -131,8 +144,8 @@ static cudaError_t launch_flat(const GateAddParams& p, cudaStream_t s) {
     const unsigned total = (unsigned)(p.rows * (p.D / kChunk));
     const int grid = grid_for_rows(reinterpret_cast<const void*>(k), (total + kBlock * kFlatU - 1) / (kBlock * kFlatU), 1, kBlock);
     if (grid < 0) return cudaErrorUnknown;
-    k<<<grid, kBlock, 0, s>>>(p, make_fastdiv((unsigned)(p.D / kChunk)), make_fastdiv((unsigned)p.seq), total);
-    return cudaGetLastError();
+    return launch_pdl(k, grid, kBlock, 0, s, p, make_fastdiv((unsigned)(p.D / kChunk)), make_fastdiv((unsigned)p.seq),
+                      total);
 }
 
 cudaError_t launch_residual_gate_add(const GateAddParams& p, bool vec, bool high, cudaStream_t s) {
@@ -156,6 +169,8 @@ cudaError_t launch_residual_gate_add(const GateAddParams& p, bool vec, bool high
 // Static E4M3 copy of a bf16 matrix (the FP8 producers' fallback for rows
 // the pipelined kernel does not take): one element per step, any alignment.
 __global__ void __launch_bounds__(kBlock) quant_e4m3_kernel(QuantParams p) {
+    grid_dep_wait();  // launched programmatically: the previous kernel has finished
+    grid_dep_launch();
     const float inv = __fdiv_rn(1.0f, __ldg(p.scale));
     for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
         const uint16_t* y = p.y + r * p.y_stride;
@@ -170,13 +185,14 @@ __global__ void __launch_bounds__(kBlock) quant_e4m3_kernel(QuantParams p) {
 cudaError_t launch_quant_e4m3(const QuantParams& p, cudaStream_t s) {
     const int grid = grid_for_rows(reinterpret_cast<const void*>(quant_e4m3_kernel), p.rows, 1, kBlock);
     if (grid < 0) return cudaErrorUnknown;
-    quant_e4m3_kernel<<<grid, kBlock, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(quant_e4m3_kernel, grid, kBlock, 0, s, p);
 }
 
 // NVFP4 copy of a bf16 matrix, one 16-element block per thread, any
 // alignment (the fallback of the NVFP4 producers).
 __global__ void __launch_bounds__(kBlock) quant_nvfp4_kernel(QuantFp4Params p) {
+    grid_dep_wait();  // launched programmatically: the previous kernel has finished
+    grid_dep_launch();
     const float gs = __ldg(p.gs);
     const int blocks = p.D / 16;
     const int64_t total = p.rows * blocks;
@@ -208,8 +224,7 @@ cudaError_t launch_quant_nvfp4(const QuantFp4Params& p, cudaStream_t s) {
     const int64_t total = p.rows * (p.D / 16);
     const int grid = grid_for_rows(reinterpret_cast<const void*>(quant_nvfp4_kernel), (total + kBlock - 1) / kBlock, 1, kBlock);
     if (grid < 0) return cudaErrorUnknown;
-    quant_nvfp4_kernel<<<grid, kBlock, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(quant_nvfp4_kernel, grid, kBlock, 0, s, p);
 }
 
 }  // namespace mbx

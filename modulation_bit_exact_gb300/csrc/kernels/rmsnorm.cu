@@ -114,6 +114,8 @@ __device__ __forceinline__ float row_rstd(const uint4 (&v)[C::M][C::J], const Ro
 
 template <int TPR, int J, bool VEC, bool HIGH>
 __global__ void __launch_bounds__(kBlock) rmsnorm_scale_kernel(RmsScaleParams p) {
+    grid_dep_wait();  // launched programmatically: the previous kernel has finished
+    grid_dep_launch();
     using C = RowCfg<TPR, J, VEC>;
     __shared__ TreeSmem smem[C::RPC];
     const RowLoop rl = row_loop<C>();
@@ -159,6 +161,8 @@ __global__ void __launch_bounds__(kBlock) rmsnorm_scale_kernel(RmsScaleParams p)
 
 template <int TPR, int J, bool VEC, bool HIGH>
 __global__ void __launch_bounds__(kBlock) rmsnorm_tanh_residual_kernel(RmsTanhParams p) {
+    grid_dep_wait();  // launched programmatically: the previous kernel has finished
+    grid_dep_launch();
     using C = RowCfg<TPR, J, VEC>;
     __shared__ TreeSmem smem[C::RPC];
     __shared__ unsigned short tab[MBX_TANH_HI - MBX_TANH_LO];
@@ -309,6 +313,9 @@ __device__ __forceinline__ void sumsq_stage_f32(const RingT& ring, int s, int t,
     }
 }
 
+// rows per group brought into L2 before the wait on the previous kernel
+constexpr int kRmsPrefetchRows = 2;
+
 template <int TPR, int J, int NS, bool HIGH, int OP, int MODE>
 __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeArgs<OP>::P p, int64_t rows_per_cta) {
     using A = RmsPipeArgs<OP>;
@@ -339,6 +346,18 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeAr
     const int64_t mod_stride = A::mod_stride(p);
     const int64_t first = r0 + g;
     RowDiv here(first, groups, p.seq);  // modulation row of the row being processed
+    // while the previous kernel in the stream drains, bring this group's first
+    // rows into L2; then wait for it before reading anything it may write
+    if (t == 0)
+#pragma unroll
+        for (int s = 0; s < kRmsPrefetchRows; ++s) {
+            const int64_t r = first + s * groups;
+            if (r >= r1) break;
+            prefetch_l2_bulk(p.x + r * p.x_stride, (uint32_t)D * 2);
+            if constexpr (DRES) prefetch_l2_bulk(A::residual(p) + r * A::res_stride(p), (uint32_t)D * 2);
+        }
+    grid_dep_wait();
+    grid_dep_launch();
 
     auto issue = [&](int s, int64_t row) { ring.issue(s, 0, p.x + row * p.x_stride, t, nch); };
 #pragma unroll
@@ -467,8 +486,7 @@ static cudaError_t launch_rms_pipe(const typename RmsPipeArgs<OP>::P& p, cudaStr
     PipeShape sh;
     if (!pipe_shape(reinterpret_cast<const void*>(k), TPR, (int)sizeof(TreeSmem) + R::kBytes, fixed, p.rows, &sh))
         return cudaErrorInvalidConfiguration;
-    k<<<sh.grid, sh.groups * TPR, sh.smem, s>>>(p, sh.rows_per_cta);
-    return cudaGetLastError();
+    return launch_pdl(k, sh.grid, sh.groups * TPR, sh.smem, s, p, sh.rows_per_cta);
 }
 
 template <int OP, int TPR, int J, int NS>
@@ -505,8 +523,7 @@ static cudaError_t launch_one(const P& p, cudaStream_t s) {
     else k = rmsnorm_tanh_residual_kernel<TPR, J, VEC, HIGH>;
     int grid = grid_for_rows(reinterpret_cast<const void*>(k), p.rows, kBlock / TPR, kBlock);
     if (grid < 0) return cudaErrorUnknown;
-    k<<<grid, kBlock, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(k, grid, kBlock, 0, s, p);
 }
 
 template <class P, int TPR, int J>
