@@ -60,7 +60,7 @@ def peaks():
 
 def kernel_sha(op: str) -> str:
     k = os.path.join(ROOT, "modulation_bit_exact_gb300", "csrc", "kernels")
-    files = ["numerics.cuh", "rowops.cuh"] + {"ln_modulate": ["ln_pipe.cuh", "ln_modulate.cu"],
+    files = ["numerics.cuh", "rowops.cuh", "launch.h"] + {"ln_modulate": ["ln_pipe.cuh", "ln_modulate.cu"],
                                                "residual_gate_add": ["residual.cu"]}[op]
     h = hashlib.sha256()
     for f in files:

@@ -438,34 +438,39 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                 // longer rows: each lane's mean and sum of squared deviations
                 // from its own elements (two passes over the lane's chunks),
                 // then one tree of Chan combines (measured faster from J = 3)
+                // (element pairs of a word in f32x2, two accumulators per pass:
+                // short dependency chains)
                 Wf L[C::M];
-    #pragma unroll
+#pragma unroll
                 for (int m = 0; m < C::M; ++m) {
-                    float sum = 0.0f;
+                    u64 s2[2] = {f2(0.0f, 0.0f), f2(0.0f, 0.0f)};
                     int n = 0;
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < C::J; ++j) {
                         const int c = t + C::TPR * m + kLanes * j;
                         if (c >= nch) continue;
                         const uint4 v = lds16(ring.at(cur, 0, c));
                         n += kChunk;
-    #pragma unroll
-                        for (int i = 0; i < 4; ++i) sum += lo_f(w_of(v, i)) + hi_f(w_of(v, i));
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) s2[i & 1] = add2(s2[i & 1], widen2(w_of(v, i)));
                     }
-                    const float lm = n ? sum / (float)n : 0.0f;
-                    float q = 0.0f;
-    #pragma unroll
+                    const u64 sum = add2(s2[0], s2[1]);
+                    const float lm = n ? (f2lo(sum) + f2hi(sum)) / (float)n : 0.0f;
+                    const u64 lm2 = f2(lm, lm);
+                    u64 q2[2] = {f2(0.0f, 0.0f), f2(0.0f, 0.0f)};
+#pragma unroll
                     for (int j = 0; j < C::J; ++j) {
                         const int c = t + C::TPR * m + kLanes * j;
                         if (c >= nch) continue;
                         const uint4 v = lds16(ring.at(cur, 0, c));
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const float d0 = lo_f(w_of(v, i)) - lm, d1 = hi_f(w_of(v, i)) - lm;
-                            q = fmaf(d0, d0, fmaf(d1, d1, q));
+                            const u64 d = sub2(widen2(w_of(v, i)), lm2);
+                            q2[i & 1] = fma2(d, d, q2[i & 1]);
                         }
                     }
-                    L[m] = Wf{lm, q, (float)n};
+                    const u64 q = add2(q2[0], q2[1]);
+                    L[m] = Wf{lm, f2lo(q) + f2hi(q), (float)n};
                 }
                 const bool full = nch == kLanes * C::J;
                 const Wf st = full ? tree_reduce<C>(L, t, sm, bar_id, wf_combine_eq)
@@ -515,8 +520,8 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                         const uint32_t tt = MODE == kModStaged ? tw : badd(0x3f803f80u, tw);
                         ow = badd(bmul(nrm, tt), hw);
                     } else {
-                        ow = pack_rn(fmaf((lo_f(xw) - mean) * rstd, 1.0f + lo_f(tw), lo_f(hw)),
-                                     fmaf((hi_f(xw) - mean) * rstd, 1.0f + hi_f(tw), hi_f(hw)));
+                        const u64 nrm = mul2(sub2(widen2(xw), mean2), rstd2);
+                        ow = pack2_rn(fma2(nrm, add2(widen2(tw), f2(1.0f, 1.0f)), widen2(hw)));
                     }
                     w_set(o, i, ow);
                 }

@@ -503,8 +503,9 @@ template <int OP>
 static cudaError_t launch_rms_pipe_d(const typename RmsPipeArgs<OP>::P& p, bool high, cudaStream_t s) {
     switch (chunks_per_lane(p.D)) {
         case 1: return launch_rms_pipe_v<OP, 32, 1, 2>(p, high, s);
-        case 2: return launch_rms_pipe_v<OP, 32, 2, 2>(p, high, s);
-        case 3: return launch_rms_pipe_v<OP, 64, 3, 2>(p, high, s);
+        // three stages measured faster at 2048 and 3072, two elsewhere
+        case 2: return launch_rms_pipe_v<OP, 32, 2, 3>(p, high, s);
+        case 3: return launch_rms_pipe_v<OP, 64, 3, 3>(p, high, s);
         case 4: return launch_rms_pipe_v<OP, 64, 4, 2>(p, high, s);
         case 5: return launch_rms_pipe_v<OP, 128, 5, 2>(p, high, s);
         case 6: return launch_rms_pipe_v<OP, 128, 6, 2>(p, high, s);
