@@ -75,7 +75,8 @@ __device__ __forceinline__ unsigned fdiv_u(unsigned n, const FastDiv& f) {
     return (unsigned)(((unsigned long long)n * f.m) >> f.shift);
 }
 
-template <bool HIGH>
+// BIAS (internal: the composed gated LN): y is replaced by bf16(y + bias).
+template <bool HIGH, bool BIAS>
 __global__ void __launch_bounds__(kBlock) residual_gate_add_flat_kernel(GateAddParams p, FastDiv by_nch,
                                                                         FastDiv by_seq, unsigned total) {
     const unsigned nch = (unsigned)p.D / kChunk;
@@ -105,6 +106,10 @@ __global__ void __launch_bounds__(kBlock) residual_gate_add_flat_kernel(GateAddP
             xv[u] = ld_stream(p.x + (int64_t)row[u] * p.x_stride + col[u] * kChunk);
             yv[u] = ld_stream(p.y + (int64_t)row[u] * p.y_stride + col[u] * kChunk);
             gv[u] = ld_shared_row(p.gate + (int64_t)mrow * p.gate_stride + col[u] * kChunk);
+            if constexpr (BIAS) {
+                const uint4 b = ld_shared_row(p.bias + col[u] * kChunk);
+                yv[u] = make_uint4(badd(yv[u].x, b.x), badd(yv[u].y, b.y), badd(yv[u].z, b.z), badd(yv[u].w, b.w));
+            }
         }
 #pragma unroll
         for (int u = 0; u < kFlatU; ++u) {
@@ -138,9 +143,9 @@ static cudaError_t launch_j(const GateAddParams& p, bool vec, bool high, cudaStr
     return high ? launch_one<J, false, true>(p, s) : launch_one<J, false, false>(p, s);
 }
 
-template <bool HIGH>
+template <bool HIGH, bool BIAS>
 static cudaError_t launch_flat(const GateAddParams& p, cudaStream_t s) {
-    auto k = residual_gate_add_flat_kernel<HIGH>;
+    auto k = residual_gate_add_flat_kernel<HIGH, BIAS>;
     const unsigned total = (unsigned)(p.rows * (p.D / kChunk));
     const int grid = grid_for_rows(reinterpret_cast<const void*>(k), (total + kBlock * kFlatU - 1) / (kBlock * kFlatU), 1, kBlock);
     if (grid < 0) return cudaErrorUnknown;
@@ -149,10 +154,11 @@ static cudaError_t launch_flat(const GateAddParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_residual_gate_add(const GateAddParams& p, bool vec, bool high, cudaStream_t s) {
-    // the flat form when its 32-bit chunk index fits (and no bias: the
-    // internal bias form stays on the row kernel)
-    if (vec && p.bias == nullptr && p.rows * (p.D / kChunk) < (1ll << 31))
-        return high ? launch_flat<true>(p, s) : launch_flat<false>(p, s);
+    // the flat form when its 32-bit chunk index fits
+    if (vec && p.rows * (p.D / kChunk) < (1ll << 31)) {
+        if (p.bias != nullptr) return high ? launch_flat<true, true>(p, s) : launch_flat<false, true>(p, s);
+        return high ? launch_flat<true, false>(p, s) : launch_flat<false, false>(p, s);
+    }
     switch (chunks_per_lane(p.D)) {
         case 1: return launch_j<1>(p, vec, high, s);
         case 2: return launch_j<2>(p, vec, high, s);
