@@ -37,7 +37,7 @@ cudaError_t launch_ln_modulate_nvfp4(const LnModParams& p, bool vec, bool high, 
 }
 
 cudaError_t launch_gated_residual_ln_modulate_nvfp4(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
-    if (vec && fused_fits(p)) return launch_pipe_d<true, true>(p, high, s);
+    if (vec && fused_fits(p, high)) return launch_pipe_d<true, true>(p, high, s);
     if (vec) {  // rows too wide for the fused ring: gated add, then the NVFP4 LN pass
         LnModParams q;
         const cudaError_t e = launch_gated_add_part(p, true, s, &q);

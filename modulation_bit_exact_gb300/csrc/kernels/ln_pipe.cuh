@@ -215,20 +215,31 @@ __device__ __forceinline__ void welford_stage(const RingT& ring, int s, int t, i
 enum { kModRing = 0, kModStaged = 1 };
 
 // Ring operands of the pipelined kernel: x (the residual when FUSED), then
-// the update (FUSED), then, in ring mode, scale, shift and the gate (FUSED).
-template <bool FUSED, int MODE>
+// the update (FUSED), then, in ring mode, the gate (FUSED) and, for fused rows
+// of more than 4096 elements, scale and shift.
+//
+// Per-row modulation is otherwise read from global memory into registers when
+// the row's data has landed (its latency hides behind the statistics), so it
+// takes no ring stages and more row groups fit in shared memory.  The fused
+// kernel's gate, used by its front pass at once, stays in the ring; so do its
+// scale and shift where the registers they would hold cost more than the ring
+// stages (measured): J >= 5, and the high variant at J = 4.
+constexpr bool ln_fused_direct(int J, bool high) { return J <= 3 || (J == 4 && !high); }
+constexpr int ln_ring_ops(bool fused, int mode, int J, bool high) {
+    return mode != kModRing ? (fused ? 2 : 1) : !fused ? 1 : ln_fused_direct(J, high) ? 3 : 5;
+}
+
+template <bool FUSED, int MODE, int J, bool HIGH>
 struct LnOps {
-    // unfused, per-row modulation: scale and shift are read from global memory
-    // into registers when the row's data has landed (their latency hides
-    // behind the statistics), so the ring carries x alone and more row
-    // groups fit in shared memory
-    static constexpr bool DIRECT = !FUSED && MODE == kModRing;
+    static constexpr bool DIRECT = MODE == kModRing && (!FUSED || ln_fused_direct(J, HIGH));
+    static constexpr bool RING_MOD = MODE == kModRing && FUSED && !DIRECT;  // scale, shift in the ring
     static constexpr int U = FUSED ? 1 : -1;
-    static constexpr int SC = MODE == kModRing && FUSED ? 2 : -1;
-    static constexpr int SH = MODE == kModRing && FUSED ? SC + 1 : -1;
-    static constexpr int G = MODE == kModRing && FUSED ? SH + 1 : -1;
-    static constexpr int N = 1 + (FUSED ? 1 : 0) + (MODE == kModRing && FUSED ? 3 : 0);
+    static constexpr int SC = RING_MOD ? 2 : -1;
+    static constexpr int SH = RING_MOD ? 3 : -1;
+    static constexpr int G = MODE == kModRing && FUSED ? (RING_MOD ? 4 : 2) : -1;
+    static constexpr int N = ln_ring_ops(FUSED, MODE, J, HIGH);
     static constexpr int SLOT = FUSED ? 3 : 2;  // staged arrays per sample: t, shift[, gate]
+    static_assert(N == 1 + (FUSED ? 1 : 0) + (G >= 0 ? 1 : 0) + (RING_MOD ? 2 : 0), "ring operands");
 };
 
 __device__ __forceinline__ void sts16(uint4* p, uint4 v) {
@@ -242,7 +253,7 @@ constexpr int kPrefetchRows = 2;
 template <int TPR, int J, int NS, bool HIGH, int MODE, bool FUSED, bool FP4>
 __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p, int64_t rows_per_cta) {
     using C = RowCfg<TPR, J, true>;
-    using O = LnOps<FUSED, MODE>;
+    using O = LnOps<FUSED, MODE, J, HIGH>;
     constexpr int NOPS = O::N;
     using R = Ring<C, NS, NOPS>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -290,12 +301,11 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
     auto issue = [&](int s, int64_t row) {
         ring.issue(s, 0, p.x + row * p.x_stride, t, nch);
         if constexpr (FUSED) ring.issue(s, O::U, p.update + row * p.update_stride, t, nch);
-        if constexpr (MODE == kModRing && FUSED) {
-            const int64_t mrow = next.q;
-            ring.issue(s, O::SC, p.scale + mrow * p.scale_stride, t, nch);
-            ring.issue(s, O::SH, p.shift + mrow * p.shift_stride, t, nch);
-            ring.issue(s, O::G, p.gate + mrow * p.gate_stride, t, nch);
+        if constexpr (O::RING_MOD) {
+            ring.issue(s, O::SC > 0 ? O::SC : 0, p.scale + next.q * p.scale_stride, t, nch);
+            ring.issue(s, O::SH > 0 ? O::SH : 0, p.shift + next.q * p.shift_stride, t, nch);
         }
+        if constexpr (MODE == kModRing && FUSED) ring.issue(s, O::G > 0 ? O::G : 0, p.gate + next.q * p.gate_stride, t, nch);
     };
 #pragma unroll
     for (int s = 0; s < NS - 1; ++s) {
@@ -555,7 +565,7 @@ template <int TPR, int J, int NS, bool HIGH, int MODE, bool FUSED, bool FP4>
 static cudaError_t launch_pipe(const LnModParams& p, cudaStream_t s) {
     auto k = ln_modulate_pipe_kernel<TPR, J, NS, HIGH, MODE, FUSED, FP4>;
     using C = RowCfg<TPR, J, true>;
-    using O = LnOps<FUSED, MODE>;
+    using O = LnOps<FUSED, MODE, J, HIGH>;
     using R = Ring<C, NS, O::N>;
     const int nch = p.D / kChunk;
     const int fixed = (MODE == kModStaged ? 2 * O::SLOT * nch * 16 : 0) + (FUSED && p.bias ? nch * 16 : 0);
@@ -595,19 +605,20 @@ static cudaError_t launch_pipe_d(const LnModParams& p, bool high, cudaStream_t s
 }
 
 // Whether the fused ring kernel keeps at least two row groups per SM: its
-// stages carry the residual and the update (and the modulation per token),
-// and per-sample modulation, gate and bias are staged.  At the widest rows
+// stages carry the residual and the update (per token also the gate, and
+// scale and shift where they are not loaded directly), and per-sample
+// modulation, gate and bias are staged.  At the widest rows
 // one group would remain, and two launches (gated add, then LN) move more
 // bytes but run faster.  Same arithmetic as launch_pipe.
-static bool fused_fits(const LnModParams& p) {
+static bool fused_fits(const LnModParams& p, bool high) {
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     const int J = chunks_per_lane(p.D), nch = p.D / kChunk;
     const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
-    const int nops = staged ? LnOps<true, kModStaged>::N : LnOps<true, kModRing>::N;
+    const int nops = ln_ring_ops(true, staged ? kModStaged : kModRing, J, high);
     const int per_group = (int)sizeof(TreeSmem) + 2 * nops * kLanes * J * 16;
-    const int fixed = (staged ? 2 * LnOps<true, kModStaged>::SLOT * nch * 16 : 0) + (p.bias ? nch * 16 : 0);
+    const int fixed = (staged ? 2 * LnOps<true, kModStaged, 1, false>::SLOT * nch * 16 : 0) + (p.bias ? nch * 16 : 0);
     return (optin - 8 * 1024 - fixed) / per_group >= 2;
 }
 
