@@ -207,8 +207,9 @@ __device__ __forceinline__ void welford_stage(const RingT& ring, int s, int t, i
 }
 
 // Modulation modes of the pipelined kernel:
-//   kModRing:   the modulation rows travel in the ring with x (per-token
-//               modulation, or samples that change within a CTA's rows);
+//   kModRing:   each row reads its own modulation row (per-token modulation,
+//               or samples that change within a CTA's rows): loaded into
+//               registers, or carried in the ring (see LnOps);
 //   kModStaged: a CTA's rows span at most two samples; their bf16(1+scale)
 //               (lossless) or scale (high) and shift are staged in shared
 //               memory once.
@@ -578,7 +579,7 @@ static cudaError_t launch_pipe(const LnModParams& p, cudaStream_t s) {
 template <int TPR, int J, int NS, bool FUSED, bool FP4>
 static cudaError_t launch_pipe_v(const LnModParams& p, bool high, cudaStream_t s) {
     // stage the modulation when each CTA's block of rows spans at most two
-    // samples (rows per CTA <= seq); otherwise carry it in the ring
+    // samples (rows per CTA <= seq); otherwise read it per row
     const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
     if (high)
         return staged ? launch_pipe<TPR, J, NS, true, kModStaged, FUSED, FP4>(p, s)

@@ -218,12 +218,12 @@ __global__ void __launch_bounds__(kBlock) rmsnorm_tanh_residual_kernel(RmsTanhPa
 // ------------------------------------------------------------------ pipelined path
 //
 // 16-byte-aligned rows: the same lanes, order and roundings as above, with x
-// (and every per-row operand) streamed through a per-row-group ring of
-// shared-memory stages by cp.async, and the weight row (plus per-sample
-// modulation rows, when a CTA's block of rows spans at most two samples)
-// staged once per CTA (for the tanh op, tanh of a per-sample gate is staged
-// instead of the gate).  OP 0: rmsnorm_scale (mod = scale);
-// OP 1: rmsnorm_tanh_residual (mod = gate, plus the residual in the ring).
+// streamed through a per-row-group ring of shared-memory stages by cp.async,
+// the weight row (plus per-sample modulation rows, when a CTA's block of rows
+// spans at most two samples) staged once per CTA (for the tanh op, tanh of a
+// per-sample gate is staged instead of the gate), and per-row modulation and
+// the tanh op's residual loaded into registers.  OP 0: rmsnorm_scale
+// (mod = scale); OP 1: rmsnorm_tanh_residual (mod = gate, plus the residual).
 enum { kRmsScale = 0, kRmsTanh = 1 };
 enum { kRmsModRing = 0, kRmsModStaged = 1 };
 
