@@ -73,3 +73,27 @@ def test_dependent_chain(mbx, B, S, D):
     assert_bits_equal(got["ln of in-place"], H, "ln of in-place")
     R2 = oracle.residual_gate_add(R, GT2, got["ln of in-place"])
     assert_bits_equal(got["rga in place 2"], R2, "rga in place 2")
+
+
+def test_cross_stream_event_order(mbx):
+    """A call on a second stream, ordered after the first stream's call by an
+    event, reads the finished output (the launch attribute relaxes only the
+    order between neighbours in one stream)."""
+    g = torch.Generator().manual_seed(5)
+    B, S, D = 2, 4352, 3072
+    x, y = _rand(g, (B * S, D)), _rand(g, (B * S, D))
+    sc, sh, gt = _rand(g, (B, D), 0.1), _rand(g, (B, D), 0.1), _rand(g, (B, D), 0.1)
+    d = [t.to(DEV) for t in (x, y, sc, sh, gt)]
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = torch.cuda.Event()
+    with torch.cuda.stream(s1):
+        a = mbx.ln_modulate(d[0], d[2], d[3])
+        ev.record(s1)
+    with torch.cuda.stream(s2):
+        s2.wait_event(ev)
+        b = mbx.residual_gate_add(a, d[4], d[1])
+    torch.cuda.synchronize()
+    A = oracle.ln_modulate(u16(x), u16(sc), u16(sh), 1e-6)
+    assert_bits_equal(u16(a), A, "ln on stream 1")
+    assert_bits_equal(u16(b), oracle.residual_gate_add(A, u16(gt), u16(y)), "rga on stream 2")
