@@ -339,8 +339,9 @@ MBX_API int mbx_check_qk_norm_rope_qkv_epilogue(
  * GPU's own correctly rounded binary32 operations (no counterpart on the
  * pages; it backs the bit-exactness of the lossless paths):
  *   which = 0: division by each Welford count k = 1..64 (the kernels'
- *              double-word reciprocal with Markstein's correction) vs
- *              div.rn, for every finite binary32 numerator;
+ *              multiply by a two-word reciprocal, one multiply and one
+ *              fused multiply-add) vs div.rn, for every finite binary32
+ *              numerator;
  *   which = 1: the bfloat16-pair multiply vs binary32 multiply + round, for
  *              every pair of bfloat16 operands;
  *   which = 2: the bfloat16-pair add vs binary32 add + round, every pair;

@@ -6,7 +6,7 @@
 // Lossless path (bit-exact to the eager BF16 chain, in the fixed order of
 // rowops.cuh):
 //   per lane, Welford over its elements: n += 1; d = x - mean;
-//     mean += d / n (correctly rounded, Markstein-corrected for the
+//     mean += d / n (correctly rounded: a two-word reciprocal of the
 //     compile-time count); m2 += d * (x - mean)
 //   fixed tree of Chan combines; var = m2 / D; rstd = 1 / sqrt(var + eps)
 //   nrm = bf16((x - mean) * rstd)          (the BF16 store between LN and modulate)

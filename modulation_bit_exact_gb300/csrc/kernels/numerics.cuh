@@ -115,22 +115,23 @@ __device__ __forceinline__ uint32_t pack2_rn(u64 v) { return pack_rn(f2lo(v), f2
 // ---------------------------------------------------------------- division by k
 
 // Correctly rounded d / K for a compile-time count K (1 <= K <= 64), by
-// Markstein's correction (P. Markstein, "Computation of elementary functions
-// on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990; also
-// Cornea-Hasegan, Golliver & Markstein, ARITH-14, 1999): with yh = RN(1/K),
-// q0 = RN(d*yh), the remainder r = d - q0*K is exact in one fused
-// multiply-add and q = RN(q0 + r*yh) is RN(d/K).  The exact remainder needs
-// d/K clear of the subnormal range: exhaustively, on this GPU, the fast form
-// equals div.rn.f32 for every K and every d with |d| >= 2^-100 and for
-// d = +0 (mbx_selftest(3)); the guarded form sends |d| < 2^-90 (zeros
-// included) to div.rn and equals it for every finite d (mbx_selftest(0)).
+// multiplication with the reciprocal split into two binary32 words
+// (Brisebarre, Muller & Raina, "Accelerating correctly rounded floating-point
+// division when the divisor is known in advance", IEEE Trans. Computers 53(8),
+// 2004): with yh = RN(1/K) and yl = RN(1/K - yh), q = RN(d*yh + RN(d*yl)),
+// one multiply and one fused multiply-add.  That paper shows the result is
+// RN(d/K) for most but not all divisors, and gives a test per divisor;
+// here the test is exhaustive on this GPU: the fast form equals div.rn.f32 for
+// every K and every d with |d| >= 2^-100 and for d = +0 (mbx_selftest(3)),
+// and the guarded form sends |d| < 2^-90 (zeros included) to div.rn and
+// equals it for every finite d (mbx_selftest(0)).
 // (A non-finite d only occurs in a row whose mean and M2 are already inf/NaN;
 // every output of such a row is the canonical NaN whatever the quotient.)
 template <int K>
 struct Recip {
     static_assert(K >= 1 && K <= 64, "Welford counts are 1..64");
     static constexpr float yh = 1.0f / (float)K;
-    static constexpr float negk = -(float)K;
+    static constexpr float yl = (float)(1.0 / (double)K - (double)yh);
 };
 
 constexpr float kDivTiny = 0x1p-90f;
@@ -144,9 +145,7 @@ template <int K>
 __device__ __forceinline__ float div_k_fast(float d) {
     if constexpr (K == 1) return d;
     if constexpr (kPow2<K>) return __fmul_rn(d, Recip<K>::yh);
-    float q0 = __fmul_rn(d, Recip<K>::yh);
-    float r = __fmaf_rn(q0, Recip<K>::negk, d);
-    return __fmaf_rn(r, Recip<K>::yh, q0);
+    return __fmaf_rn(d, Recip<K>::yh, __fmul_rn(d, Recip<K>::yl));
 }
 
 template <int K>
@@ -160,11 +159,7 @@ template <int K>
 __device__ __forceinline__ u64 div_k2_fast(u64 d) {
     if constexpr (K == 1) return d;
     if constexpr (kPow2<K>) return mul2(d, f2(Recip<K>::yh, Recip<K>::yh));
-    const u64 yh = f2(Recip<K>::yh, Recip<K>::yh);
-    const u64 nk = f2(Recip<K>::negk, Recip<K>::negk);
-    u64 q0 = mul2(d, yh);
-    u64 r = fma2(q0, nk, d);
-    return fma2(r, yh, q0);
+    return fma2(d, f2(Recip<K>::yh, Recip<K>::yh), mul2(d, f2(Recip<K>::yl, Recip<K>::yl)));
 }
 
 template <int K>
@@ -405,7 +400,7 @@ __device__ __forceinline__ float amax8_bf16(const uint4& o) {
 
 // NVFP4 block step: from the block's amax and the global scale gs, the E4M3
 // block scale s = e4m3(RN(RN(amax * gs) / 6)) and its value.  The division by
-// 6 is the guarded Markstein form (equal to div.rn for every finite numerator,
+// 6 is the guarded two-word reciprocal form (equal to div.rn for every finite numerator,
 // mbx_selftest(0)); an infinite or NaN numerator takes div.rn itself.
 __device__ __forceinline__ float div6(float d) {
     return isfinite(d) ? div_k<6>(d) : __fdiv_rn(d, 6.0f);

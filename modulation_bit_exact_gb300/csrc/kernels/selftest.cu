@@ -1,7 +1,7 @@
 // selftest.cu -- exhaustive checks of the arithmetic building blocks that the
 // lossless kernels rely on, against the GPU's own correctly rounded binary32
 // operations:
-//   0: div_k<K>(d) (double-word reciprocal + Markstein correction) ==
+//   0: div_k<K>(d) (two-word reciprocal: a multiply and a fused multiply-add) ==
 //      div.rn(d, K) for K = 1..64 and every finite binary32 d;
 //   1: mul.rn.bf16x2 == binary32 multiply then round, every operand pair;
 //   2: add.rn.bf16x2 == binary32 add then round, every operand pair;
