@@ -180,6 +180,160 @@ def test_welford_two_lanes_is_one_chan_combine(orc):
             assert orc.welford128(x) == tuple(float(v) for v in want)
 
 
+# The lane ownership and the halving tree beyond two lanes.  The fixed order
+# (chunk c = e // 8 on lane c mod 128, lanes visiting their chunks in ascending
+# order; then for s = 64, 32, ..., 1 every lane l < s takes combine(L[l],
+# L[l+s])) is the 128-thread Welford with a fixed shuffle tree that the tahou.com
+# SGLang diffusion article (section 扩散Kernel对数值精度的敏感性) names without
+# spelling out.  Each expected value below is that tree unrolled by hand for the
+# case at hand and evaluated with the textbook helpers above; the docstrings give
+# the unrolling.  Each test also shows that the plausible wrong orders (adjacent
+# pairing, swapped operands, another chunk-to-lane map) give other bits on the
+# same rows, so a mistake of that kind in the oracle cannot pass.
+
+
+def _Z(n):
+    """Welford state of n zero elements: mean 0, M2 0 (every step is exact)."""
+    f = np.float32
+    return f(0), f(0), f(n)
+
+
+def _W(xf):
+    return _welford_textbook(np.asarray(xf, np.float32))
+
+
+def _stats(t):
+    return tuple(float(v) for v in t)
+
+
+def _rows_lanes(rng, D, rows=60):
+    """Random bf16 rows of length D (binary32 values and bit patterns)."""
+    out = []
+    for _ in range(rows):
+        xf = (rng.standard_normal(D) * rng.choice([0.5, 3.0, 40.0]) + rng.choice([0.0, 2.0, -7.0]))
+        out.append(xf.astype(np.float32))
+    return out
+
+
+def test_welford_three_to_eight_lanes_follow_the_halving_tree(orc):
+    """Unrolled by hand (lanes with no element are skipped, being empty):
+      3 lanes (D 24, and ragged D 21):  s = 2: L0 = C(L0, L2);  s = 1: C(L0, L1)
+                                        -> C(C(W0, W2), W1)
+      4 lanes (D 32):  C(C(W0, W2), C(W1, W3))
+      5 lanes (D 40):  s = 4: L0 = C(W0, W4); s = 2: L0 = C(L0, W2), L1 = C(W1, W3)
+                       -> C(C(C(W0, W4), W2), C(W1, W3))
+      8 lanes (D 64):  C(C(C(W0, W4), C(W2, W6)), C(C(W1, W5), C(W3, W7)))
+    with W_l the textbook Welford of lane l's chunk (elements 8l .. 8l+7) and C
+    the Chan combine, its first operand the lower lane."""
+    C = _chan
+    rng = np.random.default_rng(31)
+    cases = {
+        21: lambda W: C(C(W[0], W[2]), W[1]),
+        24: lambda W: C(C(W[0], W[2]), W[1]),
+        32: lambda W: C(C(W[0], W[2]), C(W[1], W[3])),
+        40: lambda W: C(C(C(W[0], W[4]), W[2]), C(W[1], W[3])),
+        64: lambda W: C(C(C(W[0], W[4]), C(W[2], W[6])), C(C(W[1], W[5]), C(W[3], W[7]))),
+    }
+    # the same lanes combined in other orders: adjacent pairs first, or the
+    # higher lane as the first operand
+    wrong = {
+        21: [lambda W: C(C(W[0], W[1]), W[2]), lambda W: C(W[1], C(W[2], W[0]))],
+        24: [lambda W: C(C(W[0], W[1]), W[2]), lambda W: C(W[1], C(W[2], W[0]))],
+        32: [lambda W: C(C(W[0], W[1]), C(W[2], W[3])), lambda W: C(C(W[1], W[3]), C(W[0], W[2]))],
+        40: [lambda W: C(C(C(W[0], W[1]), C(W[2], W[3])), W[4]),
+             lambda W: C(C(W[0], W[2]), C(C(W[1], W[3]), W[4]))],
+        64: [lambda W: C(C(C(W[0], W[1]), C(W[2], W[3])), C(C(W[4], W[5]), C(W[6], W[7]))),
+             lambda W: C(C(C(W[4], W[0]), C(W[6], W[2])), C(C(W[5], W[1]), C(W[7], W[3])))],
+    }
+    for D, tree in cases.items():
+        differs = [0] * len(wrong[D])
+        for xf in _rows_lanes(rng, D):
+            x = orc.f32_to_bf16(xf)
+            xb = orc.bf16_to_f32(x)
+            W = [_W(xb[8 * l:8 * l + 8]) for l in range((D + 7) // 8)]
+            got = orc.welford128(x)
+            assert got == _stats(tree(W)), D
+            for i, w in enumerate(wrong[D]):
+                differs[i] += got != _stats(w(W))
+        assert all(differs), (D, differs)
+
+
+def test_welford_128_lanes_sparse_rows(orc):
+    """Full rows with a few non-zero lanes, every other lane all zeros (state
+    Z_n = (0, 0, n), and C(Z_n, Z_n) = Z_2n exactly), unrolled by hand:
+
+    D = 1024, non-zero lanes 0, 1, 64, 96 (one chunk each, n = 8):
+      s = 64: L0 = C(W0, W64), L1 = C(W1, Z8), L32 = C(Z8, W96), others Z16
+      s = 32: L0 = C(L0, L32), L1 = C(L1, Z16), others Z32
+      s = 16 .. 2: L0 = C(L0, Z_k), L1 = C(L1, Z_k) for k = 32, 64, 128, 256
+      s = 1: C(L0, L1)
+    D = 2048 (lane l owns chunks l and l+128, n = 16), non-zero chunks 0 and 128
+    (both lane 0), 192 (lane 64) and 1 (lane 1):
+      s = 64: L0 = C(W0, W64), L1 = C(W1, Z16), others Z32
+      s = 32 .. 2: L0 = C(L0, Z_k), L1 = C(L1, Z_k) for k = 32 .. 512;  s = 1: C(L0, L1)
+    D = 1030 (lane 0 owns chunk 0 and the 6-element chunk 128), non-zero chunks
+    0, 128 and 64:
+      s = 64: L0 = C(W0, W64) (n 14 + 8), others Z16
+      s = 32 .. 1: L0 = C(L0, Z_k) for k = 16, 32, 64, 128, 256, 512."""
+    C = _chan
+    rng = np.random.default_rng(32)
+
+    def chain(s, ks):
+        for k in ks:
+            s = C(s, _Z(k))
+        return s
+
+    def row(D, chunks):
+        xf = np.zeros(D, np.float32)
+        for c in chunks:
+            n = min(8, D - 8 * c)
+            xf[8 * c:8 * c + n] = rng.standard_normal(n) * rng.choice([0.3, 5.0]) + rng.choice([0.0, 3.0])
+        return xf
+
+    for _ in range(40):
+        x = orc.f32_to_bf16(row(1024, [0, 1, 64, 96]))
+        xb = orc.bf16_to_f32(x)
+        W = lambda l: _W(xb[8 * l:8 * l + 8])
+        left = chain(C(C(W(0), W(64)), C(_Z(8), W(96))), [32, 64, 128, 256])
+        right = chain(C(C(W(1), _Z(8)), _Z(16)), [32, 64, 128, 256])
+        assert orc.welford128(x) == _stats(C(left, right))
+
+        x = orc.f32_to_bf16(row(2048, [0, 128, 192, 1]))
+        xb = orc.bf16_to_f32(x)
+        lane = lambda l: _W(np.concatenate([xb[8 * l:8 * l + 8], xb[1024 + 8 * l:1024 + 8 * l + 8]]))
+        left = chain(C(lane(0), lane(64)), [32, 64, 128, 256, 512])
+        right = chain(C(lane(1), _Z(16)), [32, 64, 128, 256, 512])
+        assert orc.welford128(x) == _stats(C(left, right))
+
+        x = orc.f32_to_bf16(row(1030, [0, 128, 64]))
+        xb = orc.bf16_to_f32(x)
+        w0 = _W(np.concatenate([xb[0:8], xb[1024:1030]]))
+        want = chain(C(w0, _W(xb[512:520])), [16, 32, 64, 128, 256, 512])
+        assert orc.welford128(x) == _stats(want)
+
+
+def test_welford_128_lanes_crafted_row(orc):
+    """D = 1024; lane 0 holds eight 2^24, lanes 64 and 96 eight 1.0 each, every
+    other element is 0.  Each lane is constant, so its state is (c, 0, 8).
+    Derived by hand in binary32, nearest-even:
+      s = 64  L0 = C((2^24,0,8), (1,0,8)): d = 1 - 2^24 (exact), r = 1/2,
+              mean = 2^24 - (2^23 - 1/2) = 2^23 + 1/2 -> tie -> 2^23;
+              d*d = 2^48 - 2^25 + 1 -> 2^48 - 2^25; times nA*r = 4: M2 = 2^50 - 2^27
+              L32 = C(Z8, (1,0,8)) = (1/2, 4, 16)
+      s = 32  d = 1/2 - 2^23 (exact), mean = 2^23 - (2^22 - 1/4) = 2^22 + 1/4 -> tie -> 2^22;
+              M2A + M2B = 2^50 - 2^27 + 4 -> 2^50 - 2^27;  d*d -> 2^46 - 2^23, times 8;
+              M2 = 3*2^49 - 3*2^26 -> tie -> 3*2^49 - 2^28 (even significand)
+      s = 16 .. 1, each C(L0, Z_n) with n = 32 .. 512: mean halves (exact) and
+              M2 gains 2^48, 2^47, 2^46, 2^45, 2^44 (all exact at ulp 2^27)
+    Result: mean 2^17, M2 127*2^44 - 2^28, n 1024 (the exact mean is
+    2^17 + 2^-6).  Pairing lanes 64 and 96 before lane 0 keeps the 2^-6."""
+    x = np.zeros(1024, np.uint16)
+    x[0:8] = 0x4B80        # 2^24
+    x[512:520] = 0x3F80    # 1.0, chunk 64
+    x[768:776] = 0x3F80    # 1.0, chunk 96
+    assert orc.welford128(x) == (2.0 ** 17, float(127 * 2 ** 44 - 2 ** 28), 1024.0)
+
+
 @pytest.mark.parametrize("D", [1, 7, 8, 100, 512, 1000, 1024, 3072, 5120, 8192])
 def test_welford_against_float64(orc, D):
     rng = np.random.default_rng(D)
@@ -225,6 +379,80 @@ def test_sum128_against_float64(orc):
         assert abs(S - sq.sum()) <= 80 * 2.0 ** -24 * sq.sum()
         # and the rounding of the squares is really there (relative 2^-9 scale)
         assert abs(S - (xf * xf).sum()) <= 2.0 ** -8 * (xf * xf).sum()
+
+
+def test_sum128_crafted_rows_fix_tree_and_ownership(orc):
+    """Rows of 2^12 (square 2^24) and ones, every other element 0, where
+    2^24 + 1 rounds back to 2^24 (a tie, to the even significand) but
+    2^24 + 2 is exact; so the result tells whether the two ones met each other
+    before they met 2^24.  Derived by hand:
+      A  D 1024: 2^12 at element 0 (lane 0), 1 at 512 (lane 64) and 768 (lane 96).
+         s = 64: L0 = 2^24 + 1 -> 2^24, L32 = 1;  s = 32: 2^24 + 1 -> 2^24.  S = 2^24.
+         (Adjacent pairing adds lanes 64 and 96 first: 2^24 + 2.)
+      B  D 2048: 2^12 at 0, 1 at 8 (chunk 1) and 1032 (chunk 129): both ones on
+         lane 1, summed first to 2; s = 1: 2^24 + 2.  S = 2^24 + 2.
+         (Lane l owning chunks 2l, 2l+1 puts chunk 1 on lane 0 after 2^24 and
+         chunk 129 on lane 64: 2^24.)
+      C  D 1024: 2^12 at 0, 1 at 1 and 3: all in chunk 0 on lane 0, in element
+         order: 2^24 + 1 + 0 + 1 -> 2^24.  S = 2^24.
+         (Element e on lane e mod 128 adds the ones on lanes 1 and 3 first: 2^24 + 2.)
+      D  D 2048: 1 at 0 and 1, 2^12 at 1024 (chunk 128, lane 0's second chunk):
+         ascending chunks: 1 + 1 = 2, then 2 + 2^24 exact.  S = 2^24 + 2.
+         (Visiting chunk 128 first: 2^24.)"""
+    def row(D, ones, big):
+        x = np.zeros(D, np.uint16)
+        x[list(ones)] = 0x3F80  # 1.0
+        x[big] = 0x4580         # 2^12
+        return x
+
+    assert orc.sum128_sq(row(1024, (512, 768), 0)) == 2.0 ** 24
+    assert orc.sum128_sq(row(2048, (8, 1032), 0)) == 2.0 ** 24 + 2
+    assert orc.sum128_sq(row(1024, (1, 3), 0)) == 2.0 ** 24
+    assert orc.sum128_sq(row(2048, (0, 1), 1024)) == 2.0 ** 24 + 2
+
+
+def test_sum128_sparse_rows_unrolled(orc):
+    """The tree unrolled by hand on rows with a few non-zero lanes (a zero lane
+    adds exactly 0):
+      D 1024, lanes 0, 1, 64, 96:  s = 64: L0 = S0 + S64, L32 = S96;
+        s = 32: L0 = (S0 + S64) + S96;  s = 1: ((S0 + S64) + S96) + S1
+      D 2048, chunks 0 and 128 (lane 0), 192 (lane 64), 1 (lane 1):
+        (S_lane0 + S_lane64) + S_lane1
+    with S_l lane l's binary32 sum, in element order, of bf16(x*x) (PyTorch CPU
+    eager bf16 products)."""
+    rng = np.random.default_rng(33)
+    f = np.float32
+
+    def seq(q):
+        acc = f(0)
+        for v in q:
+            acc = f(acc + v)
+        return acc
+
+    def sq(x):
+        t = bf(x)
+        return (t * t).float().numpy()
+
+    differs = 0
+    for _ in range(60):
+        xf = np.zeros(1024, np.float32)
+        for c in (0, 1, 64, 96):
+            xf[8 * c:8 * c + 8] = rng.standard_normal(8) * rng.choice([0.5, 4.0, 30.0])
+        x = orc.f32_to_bf16(xf)
+        q = sq(x)
+        S = [seq(q[8 * l:8 * l + 8]) for l in range(128)]
+        got = orc.sum128_sq(x)
+        assert got == float(f(f(f(S[0] + S[64]) + S[96]) + S[1]))
+        differs += got != float(f(f(S[0] + S[1]) + f(S[64] + S[96])))
+
+        xf = np.zeros(2048, np.float32)
+        for c in (0, 128, 192, 1):
+            xf[8 * c:8 * c + 8] = rng.standard_normal(8) * rng.choice([0.5, 4.0, 30.0])
+        x = orc.f32_to_bf16(xf)
+        q = sq(x)
+        lane = lambda l: seq(np.concatenate([q[8 * l:8 * l + 8], q[1024 + 8 * l:1024 + 8 * l + 8]]))
+        assert orc.sum128_sq(x) == float(f(f(lane(0) + lane(64)) + lane(1)))
+    assert differs  # the adjacent grouping is not the same sum on these rows
 
 
 # ---------------------------------------------------------------- LN + modulate
