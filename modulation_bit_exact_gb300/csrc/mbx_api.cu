@@ -35,16 +35,35 @@ V of(const mbx_view* v) { return V{v->data, v->rows, v->cols, v->row_stride, v->
 
 int64_t esize(int32_t dtype) { return dtype == MBX_F32 ? 4 : (dtype == MBX_E4M3 || dtype == MBX_E2M1X2) ? 1 : 2; }
 
-int64_t extent_bytes(const V& v) { return ((v.rows - 1) * v.stride + v.cols) * esize(v.dtype); }
+// Bytes from a view's first element to one past its last.  Only called on
+// views that extent_ok() accepted, so nothing here can overflow.
+int64_t extent_bytes(const V& v) {
+    return ((v.rows > 1 ? (v.rows - 1) * v.stride : 0) + v.cols) * esize(v.dtype);
+}
 
-// Step 1 of a view: dtype, non-empty, stride, alignment.
+// A view whose extent does not fit in 63 bits, or whose end address would
+// wrap around, cannot lie inside any allocation: refused as out of bounds
+// before any other check does arithmetic on it.  rows, cols > 0 and
+// stride >= cols (for rows > 1) are checked first.
+int extent_ok(const V& v) {
+    int64_t span = 0, elems = 0, bytes = 0;
+    uintptr_t end = 0;
+    if (v.rows > 1 && __builtin_mul_overflow(v.rows - 1, v.stride, &span)) return MBX_E_BOUNDS;
+    if (__builtin_add_overflow(span, v.cols, &elems)) return MBX_E_BOUNDS;
+    if (__builtin_mul_overflow(elems, esize(v.dtype), &bytes)) return MBX_E_BOUNDS;
+    if (__builtin_add_overflow(reinterpret_cast<uintptr_t>(v.data), (uintptr_t)bytes, &end))
+        return MBX_E_BOUNDS;
+    return MBX_OK;
+}
+
+// Step 1 of a view: dtype, non-empty, stride, alignment, extent.
 int basic(const V& v) {
     if (v.data == nullptr) return MBX_E_NULL;
     if (v.dtype != MBX_BF16) return MBX_E_DTYPE;
     if (v.rows <= 0 || v.cols <= 0) return MBX_E_EMPTY;
     if (v.rows > 1 && v.stride < v.cols) return MBX_E_STRIDE;
     if (reinterpret_cast<uintptr_t>(v.data) % 2) return MBX_E_ALIGN;
-    return MBX_OK;
+    return extent_ok(v);
 }
 
 bool overlaps(const V& a, const V& b) {
@@ -69,7 +88,7 @@ int basic_any(const V& v) {
     if (v.rows <= 0 || v.cols <= 0) return MBX_E_EMPTY;
     if (v.rows > 1 && v.stride < v.cols) return MBX_E_STRIDE;
     if (reinterpret_cast<uintptr_t>(v.data) % esize(v.dtype)) return MBX_E_ALIGN;
-    return MBX_OK;
+    return extent_ok(v);
 }
 
 int check_variant_eps(int variant, float eps) {
@@ -112,8 +131,9 @@ int device_ok(const void* ptr, int64_t bytes, int dev) {
     if (fn(&base, &size, reinterpret_cast<CUdeviceptr>(ptr)) != CUDA_SUCCESS) {
         return a.type == cudaMemoryTypeManaged ? MBX_OK : MBX_E_BOUNDS;
     }
-    uintptr_t p0 = reinterpret_cast<uintptr_t>(ptr);
-    if (p0 + (uintptr_t)bytes > (uintptr_t)base + size) return MBX_E_BOUNDS;
+    // base <= ptr < base + size; compare the remaining room, never a sum
+    uintptr_t p0 = reinterpret_cast<uintptr_t>(ptr), b0 = (uintptr_t)base;
+    if (p0 < b0 || bytes < 0 || (uintptr_t)bytes > b0 + size - p0) return MBX_E_BOUNDS;
     return MBX_OK;
 }
 
@@ -298,6 +318,7 @@ int check_fp8(const mbx_view* out_fp8, const float* fp8_scale, const V* others, 
     if (q.dtype != MBX_E4M3) return MBX_E_DTYPE;
     if (q.rows <= 0 || q.cols <= 0) return MBX_E_EMPTY;
     if (q.rows > 1 && q.stride < q.cols) return MBX_E_STRIDE;
+    MBX_TRY(extent_ok(q));
     if (reinterpret_cast<uintptr_t>(fp8_scale) % 4) return MBX_E_ALIGN;
     if (q.rows != others[0].rows || q.cols != others[0].cols) return MBX_E_SHAPE;  // others[0] = out
     for (int i = 0; i < n; ++i)
@@ -318,6 +339,8 @@ int check_fp4(const mbx_view* out_fp4, const mbx_view* out_sf, const float* fp4_
     if (q.dtype != MBX_E2M1X2 || f.dtype != MBX_E4M3) return MBX_E_DTYPE;
     if (q.rows <= 0 || q.cols <= 0 || f.rows <= 0 || f.cols <= 0) return MBX_E_EMPTY;
     if ((q.rows > 1 && q.stride < q.cols) || (f.rows > 1 && f.stride != f.cols)) return MBX_E_STRIDE;
+    MBX_TRY(extent_ok(q));
+    MBX_TRY(extent_ok(f));
     if (reinterpret_cast<uintptr_t>(fp4_scale) % 4) return MBX_E_ALIGN;
     const int64_t rows = others[0].rows, D = others[0].cols;  // others[0] = out
     if (D % 16) return MBX_E_SHAPE;
@@ -415,6 +438,7 @@ int check_qkv(const mbx_view* joint, const mbx_cview* txt, const mbx_cview* img,
     for (const V* v : {&j, &t, &im, &w[0], &w[1], &w[2], &w[3]})
         if (v->dtype != MBX_BF16) return MBX_E_DTYPE;
     if (batch <= 0 || heads <= 0) return MBX_E_ARG;
+    if (batch >= (int64_t(1) << 31) || heads > (int64_t(1) << 20)) return MBX_E_ARG;  // no overflow below
     const int64_t hd = j.cols;
     if (hd != 64 && hd != 128 && hd != 256) return MBX_E_ARG;
     const int64_t width = 3 * heads * hd;
@@ -435,7 +459,7 @@ int check_qkv(const mbx_view* joint, const mbx_cview* txt, const mbx_cview* img,
     if (has_t && (t.cols != width || t.rows % batch)) return MBX_E_SHAPE;
     if (has_i && (im.cols != width || im.rows % batch)) return MBX_E_SHAPE;
     const int64_t s_txt = t.rows / batch, s_img = im.rows / batch;
-    if ((s_txt + s_img) * batch * heads >= (int64_t(1) << 31)) return MBX_E_ARG;  // 32-bit unit index
+    if (s_txt + s_img > ((int64_t(1) << 31) - 1) / (batch * heads)) return MBX_E_ARG;  // 32-bit unit index
     if (j.rows != batch * 3 * heads * (s_txt + s_img)) return MBX_E_SHAPE;
     if (j.rows > 1 && j.stride != hd) return MBX_E_STRIDE;  // joint is contiguous
     // 128-bit paths only: every row start 16-byte aligned

@@ -354,3 +354,43 @@ def test_nvfp4_producer_rejections(mbx):
     sc2, sh2 = V(BASE + 0x200000, 2, d2), V(BASE + 0x300000, 2, d2)
     assert st(o2, V(BASE + 0x400000, rows, d2 // 2, dtype=4), V(BASE + 0x500000, 256, 8, dtype=3),
               x2, sc2, sh2, gs) == -5
+
+
+def test_huge_extents_are_refused_not_wrapped(mbx):
+    """A view whose byte extent does not fit in 63 bits, or whose end address
+    would wrap, is refused as out of bounds (-10) by the host checks: the
+    overlap and bounds checks never see a wrapped size.  rows = 2^61 with
+    stride = cols = 8 would wrap to 0 bytes in 64-bit arithmetic."""
+    L = mbx.lib()
+    o, x, sc, sh = views(rows=4, cols=8)
+    huge = 1 << 61
+    assert ln_status(L, V(BASE, huge, 8), V(BASE + 0x100000, huge, 8), sc, sh) == -10
+    assert ln_status(L, o, V(BASE + 0x100000, 4, 8, stride=1 << 62), sc, sh) == -10
+    assert ln_status(L, o, V(BASE + 0x100000, 4, 8, stride=1 << 61), sc, sh) == -10  # 3*2^62 bytes
+    assert ln_status(L, o, V(0xFFFFFFFFFFFFFFF0, 4, 8), sc, sh) == -10     # end address wraps
+    assert ln_status(L, o, x, V(BASE + 0x200000, 2, 8, stride=1 << 62), sh) == -10
+    # the largest extent that fits is not refused by this check (the device check follows)
+    assert ln_status(L, o, V(BASE + 0x100000, 4, 8, stride=1 << 40), sc, sh) == -9
+    # FP8 / NVFP4 extra outputs and the table op's binary32 views take the same check
+    q = V(BASE + 0x400000, huge, 8, dtype=3)
+    fs = ctypes.c_void_p(BASE + 0x500000)
+    assert L.mbx_check_ln_modulate_fp8(ref(o), ref(q), ref(x), ref(sc), ref(sh), fs,
+                                       ctypes.c_float(1e-6), 0) in (-5, -10)
+    q = V(BASE + 0x400000, 4, 8, stride=1 << 62, dtype=3)
+    assert L.mbx_check_ln_modulate_fp8(ref(o), ref(q), ref(x), ref(sc), ref(sh), fs,
+                                       ctypes.c_float(1e-6), 0) == -10
+    t = V(BASE, 6, 8, dtype=2)
+    e = V(BASE + 0x100000, 4, 48, stride=1 << 61, dtype=2)
+    out = V(BASE + 0x200000, 24, 8, dtype=2)
+    assert L.mbx_check_modulation_table_add(ref(out), ref(t), ref(e)) == -10
+
+
+def test_qkv_huge_heads_or_batch_refused(mbx):
+    L = mbx.lib()
+    B, H, hd, st, si = 2, 4, 128, 8, 24
+    width = 3 * H * hd
+    joint = V(BASE, B * 3 * H * (st + si), hd)
+    txt = V(BASE + 0x1000000, B * st, width)
+    img = V(BASE + 0x2000000, B * si, width)
+    assert qkv_status(L, joint, txt, img, heads=1 << 61) == -12
+    assert qkv_status(L, joint, txt, img, batch=1 << 40) == -12
