@@ -153,12 +153,37 @@ struct QkvParams {
     FastDiv by_hpass;  // unit -> token
 };
 
+// Set while a composed call (several launches for one entry point) runs its
+// dispatch once without enqueueing anything: every launch is configured
+// (occupancy, shape, shared-memory opt-in) and launch_pdl returns before
+// cudaLaunchKernelEx.  One flag per host thread.
+inline thread_local bool t_dry_run = false;
+
+struct DryRun {
+    bool prev;
+    DryRun() : prev(t_dry_run) { t_dry_run = true; }
+    ~DryRun() { t_dry_run = prev; }
+};
+
+// Run a composed dispatch f() so that a configuration error is reported
+// before its first launch is enqueued: f() first runs dry, then for real.
+template <class F>
+inline cudaError_t launch_all_or_none(F&& f) {
+    {
+        DryRun dry;
+        const cudaError_t e = f();
+        if (e != cudaSuccess) return e;
+    }
+    return f();
+}
+
 // Launch with programmatic stream serialisation: the kernel may start while
 // the previous kernel in the stream drains, and calls grid_dep_wait() before
 // it touches global memory that kernel may use.
 template <class... KArgs, class... Args>
 inline cudaError_t launch_pdl(void (*k)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
                               Args... args) {
+    if (t_dry_run) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);

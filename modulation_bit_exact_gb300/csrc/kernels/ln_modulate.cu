@@ -237,10 +237,12 @@ cudaError_t launch_gated_residual_ln_modulate(const LnModParams& p, bool vec, bo
     // unaligned or ragged rows, or rows too wide for the fused ring: the same
     // definition as two steps, the gated residual into res_out, then
     // LayerNorm + modulate of res_out
-    LnModParams q;
-    const cudaError_t e = launch_gated_add_part(p, vec, s, &q);
-    if (e != cudaSuccess) return e;
-    return vec ? launch_pipe_d<false, false>(q, high, s) : launch_ln_modulate(q, false, high, s);
+    return launch_all_or_none([&]() {
+        LnModParams q;
+        const cudaError_t e = launch_gated_add_part(p, vec, s, &q);
+        if (e != cudaSuccess) return e;
+        return vec ? launch_pipe_d<false, false>(q, high, s) : launch_ln_modulate(q, false, high, s);
+    });
 }
 
 // The FP8 copy outside the pipelined kernel: quantise the bf16 output after it
@@ -259,19 +261,23 @@ static cudaError_t quantise_out(const LnModParams& p, cudaStream_t s) {
 
 cudaError_t launch_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
     if (vec) return launch_pipe_d<false, false>(p, high, s);
-    LnModParams q = p;
-    q.out_fp8 = nullptr;
-    cudaError_t e = launch_ln_modulate(q, false, high, s);
-    return e != cudaSuccess ? e : quantise_out(p, s);
+    return launch_all_or_none([&]() {
+        LnModParams q = p;
+        q.out_fp8 = nullptr;
+        const cudaError_t e = launch_ln_modulate(q, false, high, s);
+        return e != cudaSuccess ? e : quantise_out(p, s);
+    });
 }
 
 cudaError_t launch_gated_residual_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
     if (vec && fused_fits(p, high)) return launch_pipe_d<true, false>(p, high, s);
     if (vec) return launch_gated_residual_ln_modulate(p, true, high, s);  // composed; the LN pass writes the FP8 copy
-    LnModParams q = p;
-    q.out_fp8 = nullptr;
-    cudaError_t e = launch_gated_residual_ln_modulate(q, false, high, s);
-    return e != cudaSuccess ? e : quantise_out(p, s);
+    return launch_all_or_none([&]() {
+        LnModParams q = p;
+        q.out_fp8 = nullptr;
+        const cudaError_t e = launch_gated_residual_ln_modulate(q, false, high, s);
+        return e != cudaSuccess ? e : quantise_out(p, s);
+    });
 }
 
 cudaError_t launch_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s) {

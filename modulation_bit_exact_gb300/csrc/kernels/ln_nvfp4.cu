@@ -30,23 +30,29 @@ static cudaError_t quantise_out_fp4(const LnModParams& p, cudaStream_t s) {
 
 cudaError_t launch_ln_modulate_nvfp4(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
     if (vec) return launch_pipe_d<false, true>(p, high, s);
-    LnModParams q = p;
-    q.out_fp4 = nullptr;
-    cudaError_t e = launch_ln_modulate(q, false, high, s);
-    return e != cudaSuccess ? e : quantise_out_fp4(p, s);
+    return launch_all_or_none([&]() {
+        LnModParams q = p;
+        q.out_fp4 = nullptr;
+        const cudaError_t e = launch_ln_modulate(q, false, high, s);
+        return e != cudaSuccess ? e : quantise_out_fp4(p, s);
+    });
 }
 
 cudaError_t launch_gated_residual_ln_modulate_nvfp4(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
     if (vec && fused_fits(p, high)) return launch_pipe_d<true, true>(p, high, s);
     if (vec) {  // rows too wide for the fused ring: gated add, then the NVFP4 LN pass
-        LnModParams q;
-        const cudaError_t e = launch_gated_add_part(p, true, s, &q);
-        return e != cudaSuccess ? e : launch_pipe_d<false, true>(q, high, s);
+        return launch_all_or_none([&]() {
+            LnModParams q;
+            const cudaError_t e = launch_gated_add_part(p, true, s, &q);
+            return e != cudaSuccess ? e : launch_pipe_d<false, true>(q, high, s);
+        });
     }
-    LnModParams q = p;
-    q.out_fp4 = nullptr;
-    cudaError_t e = launch_gated_residual_ln_modulate(q, false, high, s);
-    return e != cudaSuccess ? e : quantise_out_fp4(p, s);
+    return launch_all_or_none([&]() {
+        LnModParams q = p;
+        q.out_fp4 = nullptr;
+        const cudaError_t e = launch_gated_residual_ln_modulate(q, false, high, s);
+        return e != cudaSuccess ? e : quantise_out_fp4(p, s);
+    });
 }
 
 }  // namespace mbx

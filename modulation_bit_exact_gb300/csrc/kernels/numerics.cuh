@@ -275,6 +275,16 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
                  : "l"(p));
     return v;
 }
+// 16-byte streaming load of an operand the same kernel may overwrite (an
+// exact in-place residual update): a weak, coherent load.  ld.global.nc is
+// reserved for data that stays read-only while the kernel runs.
+__device__ __forceinline__ uint4 ld_stream_rw(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
 // 16-byte load of data shared by many rows (kept in L1).
 __device__ __forceinline__ uint4 ld_shared_row(const void* p) {
     uint4 v;
@@ -367,6 +377,12 @@ __device__ __forceinline__ void st_v2(void* p, uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint16_t ld_u16(const void* p) {
     uint16_t v;
     asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+// Coherent 2-byte load (see ld_stream_rw).
+__device__ __forceinline__ uint16_t ld_u16_rw(const void* p) {
+    uint16_t v;
+    asm volatile("ld.global.u16 %0, [%1];" : "=h"(v) : "l"(p));
     return v;
 }
 __device__ __forceinline__ void st_u16(void* p, uint16_t v) {

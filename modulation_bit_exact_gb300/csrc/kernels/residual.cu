@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(kBlock) residual_gate_add_kernel(GateAddParams
         for (int j = 0; j < J; ++j) {
             int c = rl.t + kLanes * j;
             if (c < nch) {
-                xv[j] = load_chunk<VEC>(x_row, c, D, true);
+                xv[j] = load_chunk<VEC, true>(x_row, c, D, true);  // out may be x
                 yv[j] = load_chunk<VEC>(y_row, c, D, true);
                 gv[j] = load_chunk<VEC>(g_row, c, D, per_token);
                 if (p.bias) {  // internal use: the fused entry point's fallback
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kBlock) residual_gate_add_flat_kernel(GateAddP
             row[u] = fdiv_u(q, by_nch);
             col[u] = q - row[u] * nch;
             const unsigned mrow = fdiv_u(row[u], by_seq);
-            xv[u] = ld_stream(p.x + (int64_t)row[u] * p.x_stride + col[u] * kChunk);
+            xv[u] = ld_stream_rw(p.x + (int64_t)row[u] * p.x_stride + col[u] * kChunk);  // out may be x
             yv[u] = ld_stream(p.y + (int64_t)row[u] * p.y_stride + col[u] * kChunk);
             gv[u] = ld_shared_row(p.gate + (int64_t)mrow * p.gate_stride + col[u] * kChunk);
             if constexpr (BIAS) {

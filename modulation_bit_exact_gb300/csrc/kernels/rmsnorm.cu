@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kBlock) rmsnorm_tanh_residual_kernel(RmsTanhPa
                 if (c >= nch) continue;
                 uint4 w = load_chunk<VEC>(p.weight, c, D, false);
                 uint4 g = load_chunk<VEC>(g_row, c, D, per_token);
-                uint4 r = load_chunk<VEC>(r_row, c, D, true);
+                uint4 r = load_chunk<VEC, true>(r_row, c, D, true);  // out may be the residual
                 uint4 o;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeAr
                     const int c = t + C::TPR * m + kLanes * j;
                     if (c >= nch) continue;
                     if constexpr (DMOD) dMD[DMOD ? j : 0][DMOD ? m : 0] = ld_stream(md_row + (int64_t)c * kChunk);
-                    if constexpr (DRES) dRS[DRES ? j : 0][DRES ? m : 0] = ld_stream(rs_row + (int64_t)c * kChunk);
+                    if constexpr (DRES) dRS[DRES ? j : 0][DRES ? m : 0] = ld_stream_rw(rs_row + (int64_t)c * kChunk);
                 }
         }
 

@@ -47,19 +47,22 @@ __device__ __forceinline__ void group_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// Chunk c of a row: 8 elements, zero-filled past D.
-template <bool VEC>
+// Chunk c of a row: 8 elements, zero-filled past D.  RW: the row may be
+// overwritten by this kernel (an in-place residual), so it is read with
+// coherent loads.
+template <bool VEC, bool RW = false>
 __device__ __forceinline__ uint4 load_chunk(const uint16_t* row, int c, int D, bool stream) {
     if constexpr (VEC) {
         const uint16_t* p = row + (int64_t)c * kChunk;
+        if constexpr (RW) return ld_stream_rw(p);
         return stream ? ld_stream(p) : ld_shared_row(p);
     } else {
         uint4 v = make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             int e0 = c * kChunk + 2 * i;
-            uint32_t lo = e0 < D ? ld_u16(row + e0) : 0u;
-            uint32_t hi = e0 + 1 < D ? ld_u16(row + e0 + 1) : 0u;
+            uint32_t lo = e0 < D ? (RW ? ld_u16_rw(row + e0) : ld_u16(row + e0)) : 0u;
+            uint32_t hi = e0 + 1 < D ? (RW ? ld_u16_rw(row + e0 + 1) : ld_u16(row + e0 + 1)) : 0u;
             w_set(v, i, lo | (hi << 16));
         }
         return v;
