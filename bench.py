@@ -1,16 +1,20 @@
 """Benchmark of the DiT norm/modulation hot path (one JSON line on rank 0).
 
-Workload (one step): the image-DiT block norm path at Qwen-Image scale,
-  ln_modulate:       out1 = LN(x) * (1 + scale) + shift   x [2, 4352, 3072]
-  residual_gate_add: out2 = x' + gate * y                  x', y [2, 4352, 3072]
-with per-sample scale/shift/gate [2, 3072], bfloat16, lossless variant, every
-call through the C ABI of libmbx.so.  Inputs are synthetic (seeded, N(0,1)
-activations with 1 % outliers x20, N(0,0.1) modulation).
+Headline workload (one step): the video-DiT per-token modulation block at Wan
+scale, the largest single-GPU configuration,
+  ln_modulate:            out1 = LN(x) * (1 + scale) + shift        x [1, 32760, 5120]
+  rmsnorm_tanh_residual:  out2 = r + tanh(g) * RMSNorm(x) * w       g, r [1, 32760, 5120]
+with per-token scale/shift [1, 32760, 5120], w [5120], eps 1e-6, bfloat16,
+lossless variant, every call through the C ABI of libmbx.so.  Inputs are
+synthetic (seeded N(0,1) activations, N(0,0.1) modulation, 1+N(0,0.05) weight).
 
-L2 policy: three buffer sets of 267 MB each (x, out1, x', y, out2) are used
-in turn, so a step never reads a tensor the previous ~530 MB of traffic
-touched (L2 is 129 MB); the per-sample modulation vectors (36 KB) stay in L2,
-as they would in a model.
+Secondary workload (keys under "image_dit"): the image-DiT block norm path at
+Qwen-Image scale, ln_modulate on x [2, 4352, 3072] with per-sample
+scale/shift [2, 3072], then residual_gate_add x' + gate * y.
+
+L2 policy: every headline step streams 2.68 GB, far more than L2 (129 MB),
+and two buffer sets alternate; the image-DiT step rotates three 267 MB sets,
+so no step reads a tensor the previous ~530 MB of traffic touched.
 
 Metric: achieved HBM GB/s = algorithmic bytes (every input read once, every
 output written once) / device time, from CUDA events on the launching stream.
@@ -36,16 +40,37 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "achieved HBM GB/s (% of GB300 peak) and µs/call for LN+AdaLN modulate"
-B, S, D = 2, 4352, 3072
-ELEMS = B * S * D
-T_BYTES = ELEMS * 2                                  # one [2,4352,3072] bf16 tensor
-LN_BYTES = 2 * T_BYTES + 2 * B * D * 2               # read x, write out, scale + shift
-RGA_BYTES = 3 * T_BYTES + B * D * 2                  # read x', y, write out, gate
-STEP_BYTES = LN_BYTES + RGA_BYTES
-WORKLOAD = ("image-DiT block norm path: ln_modulate x[2,4352,3072] (per-sample scale/shift "
-            "[2,3072], eps 1e-6) then residual_gate_add x'[2,4352,3072] + gate[2,3072]*y, "
+
+# headline: video-DiT per-token modulation, [1, 32760, 5120]
+VS, VD = 32760, 5120
+V_T = VS * VD * 2                                    # one [1,32760,5120] bf16 tensor
+V_LN_BYTES = 4 * V_T                                 # read x, scale, shift; write out1
+V_TANH_BYTES = 4 * V_T + 2 * VD                      # read x, g, r, w; write out2
+V_STEP_BYTES = V_LN_BYTES + V_TANH_BYTES
+WORKLOAD = ("video-DiT per-token modulation: ln_modulate x[1,32760,5120] with per-token "
+            "scale/shift [1,32760,5120] (eps 1e-6), then rmsnorm_tanh_residual "
+            "out = r + tanh(g)*RMSNorm(x)*w with g, r [1,32760,5120], w [5120] (eps 1e-6), "
             "bf16, lossless")
-L2_NOTE = "3 rotating buffer sets of 267 MB (inputs larger than L2 per step, no re-read)"
+L2_NOTE = ("2 alternating buffer sets of 2.35 GB; each step streams 2.68 GB "
+           "(inputs larger than L2, no re-read)")
+
+# secondary: image-DiT block norm path, [2, 4352, 3072]
+IB, IS, ID = 2, 4352, 3072
+I_T = IB * IS * ID * 2                               # one [2,4352,3072] bf16 tensor
+I_LN_BYTES = 2 * I_T + 2 * IB * ID * 2               # read x, write out, scale + shift
+I_RGA_BYTES = 3 * I_T + IB * ID * 2                  # read x', y, write out, gate
+I_STEP_BYTES = I_LN_BYTES + I_RGA_BYTES
+I_WORKLOAD = ("image-DiT block norm path: ln_modulate x[2,4352,3072] (per-sample scale/shift "
+              "[2,3072], eps 1e-6) then residual_gate_add x'[2,4352,3072] + gate[2,3072]*y, "
+              "bf16, lossless")
+I_L2_NOTE = "3 rotating buffer sets of 267 MB (inputs larger than L2 per step, no re-read)"
+
+# kernel sources behind each timed operation (the key of the DRAM traffic table)
+_KERNEL_FILES = {
+    "ln_modulate": ["ln_pipe.cuh", "ln_modulate.cu"],
+    "rmsnorm_tanh_residual": ["rmsnorm.cu", "tanh_bf16_table.inc"],
+    "residual_gate_add": ["residual.cu"],
+}
 
 
 def peaks():
@@ -60,8 +85,7 @@ def peaks():
 
 def kernel_sha(op: str) -> str:
     k = os.path.join(ROOT, "modulation_bit_exact_gb300", "csrc", "kernels")
-    files = ["numerics.cuh", "rowops.cuh", "launch.h"] + {"ln_modulate": ["ln_pipe.cuh", "ln_modulate.cu"],
-                                               "residual_gate_add": ["residual.cu"]}[op]
+    files = ["numerics.cuh", "rowops.cuh", "launch.h"] + _KERNEL_FILES[op]
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(k, f), "rb") as fh:
@@ -69,9 +93,10 @@ def kernel_sha(op: str) -> str:
     return h.hexdigest()[:16]
 
 
-def dram_traffic(op: str):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+def dram_traffic(op: str, workload: str):
+    """Per-launch DRAM bytes (read + write) of `op` on `workload` from the
+    committed ncu summary, if it was taken on the current kernel source (else
+    None)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -79,8 +104,9 @@ def dram_traffic(op: str):
     with open(path) as f:
         for line in f:
             parts = line.split()
-            if len(parts) >= 3 and not line.startswith("#") and parts[0] == op and parts[2] == sha:
-                return int(parts[1])
+            if (len(parts) >= 4 and not line.startswith("#") and parts[0] == op and parts[1] == workload
+                    and parts[3] == sha):
+                return int(parts[2])
     return None
 
 
@@ -142,35 +168,51 @@ class Clocks:
                 "samples": len(sm)}
 
 
+
+
 # ---------------------------------------------------------------------- CPU oracle
 
 
-def oracle_rate(budget_s: float, rows_per_call: int = 64):
-    """GB/s of the CPU oracle on row samples of the workload (both operations),
-    over about budget_s seconds; returns (GB/s, rows done, seconds)."""
+def _video_sample(rows: int = 256):
+    """The headline workload's recipe on `rows` tokens (CPU): bf16 bit patterns
+    x, scale, shift, g, r [rows, 5120] and w [5120]."""
     import numpy as np
     import torch
 
-    import oracle
     import synth
-    d = synth.image_dit_block(seq=256)  # the same recipe, 512 rows
-    u = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1, D)
-    X, Y = u(d["x"]), u(d["y"])
-    SC, SH, G = u(d["scale"]), u(d["shift"]), u(d["gate"])
+    d = synth.video_dit_block(seq=rows)
+    u = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1, VD)
+    return (u(d["x"]), u(d["scale"]), u(d["shift"]), u(d["gate"]), u(d["residual"]),
+            u(d["weight"]).reshape(-1))
+
+
+def _oracle_step_rows(arrays, r0: int, n: int):
+    """Both operations of the headline step on rows [r0, r0 + n) of the sample."""
+    import oracle
+    X, SC, SH, G, R, W = arrays
+    oracle.ln_modulate(X[r0:r0 + n], SC[r0:r0 + n], SH[r0:r0 + n], 1e-6)
+    oracle.rmsnorm_tanh_residual(X[r0:r0 + n], G[r0:r0 + n], R[r0:r0 + n], W, 1e-6)
+
+
+ROW_BYTES = V_STEP_BYTES / VS  # algorithmic bytes of one token row of the step
+
+
+def oracle_rate(budget_s: float, rows_per_call: int = 16):
+    """GB/s of the CPU oracle, one thread, on row samples of the headline
+    workload (both operations), over about budget_s seconds; returns
+    (GB/s, rows done, seconds)."""
+    import oracle
+    arrays = _video_sample()
     oracle.lib()
+    nblk = arrays[0].shape[0] // rows_per_call
     done, t0 = 0, time.perf_counter()
     while True:
-        r0 = (done % (X.shape[0] // rows_per_call)) * rows_per_call
-        xs, ys = X[r0:r0 + rows_per_call], Y[r0:r0 + rows_per_call]
-        m = (r0 // 256)
-        oracle.ln_modulate(xs, SC[m:m + 1], SH[m:m + 1], 1e-6)
-        oracle.residual_gate_add(xs, G[m:m + 1], ys)
+        _oracle_step_rows(arrays, (done // rows_per_call % nblk) * rows_per_call, rows_per_call)
         done += rows_per_call
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    per_row = (2 * 2 * D) + (3 * 2 * D)  # ln: read + write; rga: 2 reads + write
-    return done * per_row / el / 1e9, done, el
+    return done * ROW_BYTES / el / 1e9, done, el
 
 
 def max_over_ranks(value: float, dist, device) -> float:
@@ -187,48 +229,35 @@ def max_over_ranks(value: float, dist, device) -> float:
 def _oracle_share(job):
     """One host process's share of the all-cores oracle baseline: rows
     [lo, hi) of the sample, both operations, for about `budget` seconds."""
-    X, Y, SC, SH, G, lo, hi, budget, rows_per_call, seq = job
+    arrays, lo, hi, budget, rows_per_call = job
     import oracle
     oracle.lib()
     done, t0 = 0, time.perf_counter()
     n = max(1, (hi - lo) // rows_per_call)
     while True:
-        r0 = lo + (done // rows_per_call % n) * rows_per_call
-        m = r0 // seq
-        oracle.ln_modulate(X[r0:r0 + rows_per_call], SC[m:m + 1], SH[m:m + 1], 1e-6)
-        oracle.residual_gate_add(X[r0:r0 + rows_per_call], G[m:m + 1], Y[r0:r0 + rows_per_call])
+        _oracle_step_rows(arrays, lo + (done // rows_per_call % n) * rows_per_call, rows_per_call)
         done += rows_per_call
         el = time.perf_counter() - t0
         if el >= budget:
             return done, el
 
 
-def oracle_rate_all_cores(budget_s: float, rows_per_call: int = 16):
+def oracle_rate_all_cores(budget_s: float, rows_per_call: int = 4):
     """The same oracle, one process per host core (a spawned pool: safe after
     CUDA is initialised), each on a static share of the sample rows; returns
     (GB/s, rows done, seconds, processes)."""
     import multiprocessing as mp
-
-    import numpy as np
-    import torch
-
-    import synth
-    seq = 256
-    d = synth.image_dit_block(seq=seq)
-    u = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1, D)
-    X, Y = u(d["x"]), u(d["y"])
-    SC, SH, G = u(d["scale"]), u(d["shift"]), u(d["gate"])
+    arrays = _video_sample()
     n = os.cpu_count() or 1
-    rows = X.shape[0]
+    rows = arrays[0].shape[0]
     share = max(rows_per_call, rows // n // rows_per_call * rows_per_call)
-    jobs = [(X, Y, SC, SH, G, (i * share) % rows, min(rows, (i * share) % rows + share), budget_s, rows_per_call, seq)
+    jobs = [(arrays, (i * share) % rows, min(rows, (i * share) % rows + share), budget_s, rows_per_call)
             for i in range(n)]
     with mp.get_context("spawn").Pool(n) as pool:
         res = pool.map(_oracle_share, jobs)
     done = sum(r[0] for r in res)
     el = max(r[1] for r in res)
-    per_row = (2 * 2 * D) + (3 * 2 * D)
-    return done * per_row / el / 1e9, done, el, n
+    return done * ROW_BYTES / el / 1e9, done, el, n
 
 
 _REF_DATA = None
@@ -242,13 +271,9 @@ def _ref_init(arrays):
 
 
 def _ref_rows(job):
-    """Both operations of the workload on rows [r0, r0 + rows) (one process)."""
-    import oracle
-    r0, rows, seq = job
-    X, Y, SC, SH, G = _REF_DATA
-    m = r0 // seq
-    oracle.ln_modulate(X[r0:r0 + rows], SC[m:m + 1], SH[m:m + 1], 1e-6)
-    oracle.residual_gate_add(X[r0:r0 + rows], G[m:m + 1], Y[r0:r0 + rows])
+    """Both operations of the headline step on rows [r0, r0 + rows) (one process)."""
+    r0, rows = job
+    _oracle_step_rows(_REF_DATA, r0, rows)
     return rows
 
 
@@ -260,33 +285,21 @@ def run_reference(args):
         return 0
     import multiprocessing as mp
 
-    import numpy as np
-    import torch
-
     import oracle
-    import synth
-    seq = 256
-    d = synth.image_dit_block(seq=seq)
-    u = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1, D)
-    X, Y = u(d["x"]), u(d["y"])
-    SC, SH, G = u(d["scale"]), u(d["shift"]), u(d["gate"])
+    arrays = _video_sample()
     oracle.lib()
     n = os.cpu_count() or 1
+    sample_rows = arrays[0].shape[0]
     # size a step so that warmup + steps take about 60 s in all
     t0 = time.perf_counter()
-    oracle.ln_modulate(X[:8], SC[:1], SH[:1], 1e-6)
-    oracle.residual_gate_add(X[:8], G[:1], Y[:8])
-    per_row = (time.perf_counter() - t0) / 8
-    per_proc = int(max(1, min(seq, 60.0 / max(1, args.steps + args.warmup) / max(per_row, 1e-9))))
+    _oracle_step_rows(arrays, 0, 4)
+    per_row = (time.perf_counter() - t0) / 4
+    per_proc = int(max(1, min(sample_rows, 60.0 / max(1, args.steps + args.warmup) / max(per_row, 1e-9))))
     rows = per_proc * n
 
-    with mp.get_context("spawn").Pool(n, initializer=_ref_init, initargs=((X, Y, SC, SH, G),)) as pool:
+    with mp.get_context("spawn").Pool(n, initializer=_ref_init, initargs=(arrays,)) as pool:
         def step(i):
-            jobs = []
-            for k in range(n):
-                r0 = ((i * n + k) * per_proc) % (X.shape[0] - per_proc + 1)
-                r0 = min(r0, (r0 // seq) * seq + seq - per_proc)  # stay inside one sample
-                jobs.append((r0, per_proc, seq))
+            jobs = [(((i * n + k) * per_proc) % (sample_rows - per_proc + 1), per_proc) for k in range(n)]
             pool.map(_ref_rows, jobs)
 
         for i in range(args.warmup):
@@ -295,10 +308,9 @@ def run_reference(args):
         for i in range(args.steps):
             step(i)
         el = time.perf_counter() - t0
-    bytes_per_step = rows * ((2 * 2 * D) + (3 * 2 * D))
-    gbs = bytes_per_step * args.steps / el / 1e9
-    sample = (f"{rows} rows of x[2,4352,3072] per step (both operations; the full step is "
-              f"8704 rows), {n} processes, one per host core, {per_proc} rows each")
+    gbs = rows * ROW_BYTES * args.steps / el / 1e9
+    sample = (f"{rows} token rows of the step per step (both operations; the full step is "
+              f"{VS} rows of [1,32760,5120]), {n} processes, one per host core, {per_proc} rows each")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -317,13 +329,65 @@ def run_reference(args):
 # ---------------------------------------------------------------------- GPU arm
 
 
+def _video_sets(mbx, dev, rank, n=2):
+    """Buffer sets of the headline step, created on the device."""
+    import torch
+
+    import synth
+    sets = []
+    for i in range(n):
+        d = synth.video_dit_block(seed=4 + 100 * i + 1000 * rank, device=dev)
+        s = dict(x=d["x"], scale=d["scale"], shift=d["shift"], out1=torch.empty_like(d["x"]),
+                 g=d["gate"], r=d["residual"], w=d["weight"], out2=torch.empty_like(d["x"]))
+        sets.append((s, {k: mbx._view(t) for k, t in s.items()}))
+    return sets
+
+
+def _image_sets(mbx, dev, rank, n=3):
+    """Buffer sets of the image-DiT step, created on the device."""
+    import torch
+
+    import synth
+    sets = []
+    for i in range(n):
+        d = synth.image_dit_block(seed=2 + 100 * i + 1000 * rank, device=dev)
+        d2 = synth.image_dit_block(seed=3 + 100 * i + 1000 * rank, device=dev)
+        s = dict(x=d["x"], scale=d["scale"], shift=d["shift"], out1=torch.empty_like(d["x"]),
+                 xb=d2["x"], gate=d["gate"], y=d["y"], out2=torch.empty_like(d["x"]))
+        sets.append((s, {k: mbx._view(t) for k, t in s.items()}))
+    return sets
+
+
+def _time_loops(stream, K, step, calls):
+    """K steps with events at the two ends only (an event between the calls
+    would stop each from overlapping its launch with the previous one's
+    drain), then each call alone K times back to back, events at the ends.
+    Returns (step ms total, [call ms total], status)."""
+    import torch
+    st = 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        st |= step(i)
+    e1.record(stream)
+    per_call = []
+    for fn in calls:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(K):
+            st |= fn(i)
+        b.record(stream)
+        per_call.append((a, b))
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1), [a.elapsed_time(b) for a, b in per_call], st
+
+
 def run_gpu(args):
     import ctypes
 
     import torch
 
     import modulation_bit_exact_gb300 as mbx
-    import synth
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -338,43 +402,39 @@ def run_gpu(args):
     L = mbx.lib()
     stream = torch.cuda.current_stream(dev)
     sptr = ctypes.c_void_p(stream.cuda_stream)
-
-    # three buffer sets
-    sets = []
-    for i in range(3):
-        d = synth.image_dit_block(seed=2 + 100 * i + 1000 * rank, device=dev)
-        d2 = synth.image_dit_block(seed=3 + 100 * i + 1000 * rank, device=dev)
-        s = dict(x=d["x"], scale=d["scale"], shift=d["shift"], out1=torch.empty_like(d["x"]),
-                 xb=d2["x"], gate=d["gate"], y=d["y"], out2=torch.empty_like(d["x"]))
-        v = {k: mbx._view(t) for k, t in s.items()}
-        sets.append((s, v))
-    del d, d2
-    torch.cuda.synchronize(dev)
     eps = ctypes.c_float(1e-6)
     ref = ctypes.byref
 
-    def ln(i):
-        v = sets[i % 3][1]
+    vsets = _video_sets(mbx, dev, rank)
+    isets = _image_sets(mbx, dev, rank)
+    torch.cuda.synchronize(dev)
+
+    def v_ln(i):
+        v = vsets[i % 2][1]
         return L.mbx_ln_modulate(ref(v["out1"]), ref(v["x"]), ref(v["scale"]), ref(v["shift"]), eps, 0, sptr)
 
-    def rga(i):
-        v = sets[i % 3][1]
+    def v_tanh(i):
+        v = vsets[i % 2][1]
+        return L.mbx_rmsnorm_tanh_residual(ref(v["out2"]), ref(v["x"]), ref(v["g"]), ref(v["r"]), ref(v["w"]),
+                                           eps, 0, sptr)
+
+    def i_ln(i):
+        v = isets[i % 3][1]
+        return L.mbx_ln_modulate(ref(v["out1"]), ref(v["x"]), ref(v["scale"]), ref(v["shift"]), eps, 0, sptr)
+
+    def i_rga(i):
+        v = isets[i % 3][1]
         return L.mbx_residual_gate_add(ref(v["out2"]), ref(v["xb"]), ref(v["gate"]), ref(v["y"]), 0, sptr)
 
-    def launch(i):
-        return ln(i) | rga(i)
+    v_step = lambda i: v_ln(i) | v_tanh(i)
+    i_step = lambda i: i_ln(i) | i_rga(i)
 
     for i in range(args.warmup):
-        if launch(i) != 0:
+        if v_step(i) | i_step(i):
             raise RuntimeError("launch failed")
     torch.cuda.synchronize(dev)
 
-    # Timed region: K steps with events at the two ends only (an event between
-    # the two calls would stop the second from overlapping its launch with the
-    # first one's drain); then, for the roofline, each call alone K times back
-    # to back, its average launch duration from events at the ends.
     K = args.steps
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
     gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
     if not gpu_uuid.startswith("GPU-"):
         gpu_uuid = "GPU-" + gpu_uuid
@@ -382,54 +442,40 @@ def run_gpu(args):
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    st = 0
     with clocks:
-        ev[0].record(stream)
-        for i in range(K):
-            st |= launch(i)
-        ev[1].record(stream)
-        torch.cuda.synchronize(dev)
-        if dist:
-            dist.barrier()
-        for j, fn in enumerate((ln, rga)):
-            ev[2 + 2 * j].record(stream)
-            for i in range(K):
-                st |= fn(i)
-            ev[3 + 2 * j].record(stream)
-        torch.cuda.synchronize(dev)
-    if st != 0:
+        v_ms, (v_ln_ms, v_tanh_ms), st_v = _time_loops(stream, K, v_step, (v_ln, v_tanh))
+        i_ms, (i_ln_ms, i_rga_ms), st_i = _time_loops(stream, K, i_step, (i_ln, i_rga))
+    if st_v | st_i:
         raise RuntimeError("launch failed")
     if dist:
         dist.barrier()
-    total_ms = ev[0].elapsed_time(ev[1])
-    ln_ms = ev[2].elapsed_time(ev[3])
-    rga_ms = ev[4].elapsed_time(ev[5])
-    total_ms = max_over_ranks(total_ms, dist, dev)
+    v_ms = max_over_ranks(v_ms, dist, dev)
+    i_ms = max_over_ranks(i_ms, dist, dev)
 
-    # End to end: every step copies its inputs in from pinned host memory,
-    # runs both calls through the C ABI and copies its outputs back to pinned
-    # host memory.  Copies in, compute and copies out run on three streams
-    # with two device buffer sets, so step i+1's inputs travel while step i
-    # computes and step i-1's outputs return (the way a serving loop overlaps
-    # them); events order each set's reuse.  Every rank measures its own
-    # replica; the slowest is reported.
-    names_in = ("x", "xb", "y", "scale", "shift", "gate")
-    host = {k: torch.empty(sets[0][0][k].shape, dtype=torch.bfloat16, pin_memory=True)
-            for k in names_in + ("out1", "out2")}
+    # End to end on the headline step: every step copies its inputs in from
+    # pinned host memory, runs both calls through the C ABI and copies its
+    # outputs back to pinned host memory.  Copies in, compute and copies out
+    # run on three streams with two device buffer sets, so step i+1's inputs
+    # travel while step i computes and step i-1's outputs return (the way a
+    # serving loop overlaps them); events order each set's reuse.  Every rank
+    # measures its own replica; the slowest is reported.
+    names_in = ("x", "scale", "shift", "g", "r", "w")
+    names_out = ("out1", "out2")
+    host = {k: torch.empty(vsets[0][0][k].shape, dtype=torch.bfloat16, pin_memory=True)
+            for k in names_in + names_out}
     for k in names_in:
-        host[k].copy_(sets[0][0][k])
-    dsets = [sets[0], sets[1]]
+        host[k].copy_(vsets[0][0][k])
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
     cptr = ctypes.c_void_p(s_cmp.cuda_stream)
     ev_in, ev_cmp, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
     for e in ev_in + ev_cmp + ev_out:
         e.record(stream)
     torch.cuda.synchronize(dev)
-    n_e2e = max(4, min(50, K // 100))
+    n_e2e = 4
 
     def e2e_step(i):
         b = i % 2
-        t, v = dsets[b]
+        t, v = vsets[b]
         s_in.wait_event(ev_cmp[b])  # the calls that last read this set are done
         with torch.cuda.stream(s_in):
             for k in names_in:
@@ -438,21 +484,22 @@ def run_gpu(args):
         s_cmp.wait_event(ev_in[b])
         s_cmp.wait_event(ev_out[b])  # this set's outputs have been copied out
         st = L.mbx_ln_modulate(ref(v["out1"]), ref(v["x"]), ref(v["scale"]), ref(v["shift"]), eps, 0, cptr)
-        st |= L.mbx_residual_gate_add(ref(v["out2"]), ref(v["xb"]), ref(v["gate"]), ref(v["y"]), 0, cptr)
+        st |= L.mbx_rmsnorm_tanh_residual(ref(v["out2"]), ref(v["x"]), ref(v["g"]), ref(v["r"]), ref(v["w"]),
+                                          eps, 0, cptr)
         if st != 0:
             raise RuntimeError("launch failed")
         ev_cmp[b].record(s_cmp)
         s_out.wait_event(ev_cmp[b])
         with torch.cuda.stream(s_out):
-            host["out1"].copy_(t["out1"], non_blocking=True)
-            host["out2"].copy_(t["out2"], non_blocking=True)
+            for k in names_out:
+                host[k].copy_(t[k], non_blocking=True)
         ev_out[b].record(s_out)
 
-    for i in range(4):
+    for i in range(2):
         e2e_step(i)
     torch.cuda.synchronize(dev)
-    # three runs of n_e2e steps, the median reported: the host link is shared
-    # with the machine's other GPUs and a single run can catch their traffic
+    # three runs, the median reported: the host link is shared with the
+    # machine's other GPUs and a single run can catch their traffic
     runs = []
     for _ in range(3):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -464,12 +511,13 @@ def run_gpu(args):
         runs.append(e0.elapsed_time(e1) / n_e2e)
     e2e_ms = max_over_ranks(sorted(runs)[1], dist, dev)
     h2d = sum(host[k].numel() * 2 for k in names_in)
-    d2h = sum(host[k].numel() * 2 for k in ("out1", "out2"))
-    e2e = {"value": round(STEP_BYTES * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+    d2h = sum(host[k].numel() * 2 for k in names_out)
+    e2e = {"value": round(V_STEP_BYTES * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": round(e2e_ms, 4), "steps": n_e2e,
            "runs_ms_per_step": [round(r, 4) for r in runs], "of_runs": "median of 3",
            "overlap": "copies in, compute, copies out on three streams, two device buffer sets"}
+    del host
 
     if rank != 0:
         if dist:
@@ -477,19 +525,24 @@ def run_gpu(args):
         return 0
 
     peak, peak_kind = peaks()
-    ln_us = ln_ms / K * 1e3
-    rga_us = rga_ms / K * 1e3
-    kern = {
-        "ln_modulate": {"us_per_call": round(ln_us, 3), "bytes": LN_BYTES,
-                        "gbs": round(LN_BYTES / (ln_us * 1e-6) / 1e9, 1)},
-        "residual_gate_add": {"us_per_call": round(rga_us, 3), "bytes": RGA_BYTES,
-                              "gbs": round(RGA_BYTES / (rga_us * 1e-6) / 1e9, 1)},
-    }
-    for k in kern.values():
-        k["frac"] = round(k["gbs"] / peak, 4)
-    dom = max(kern, key=lambda k: kern[k]["us_per_call"])
-    roof = {"bound": "hbm", "achieved": kern[dom]["gbs"], "peak": peak, "unit": "GB/s",
-            "frac": kern[dom]["frac"], "traffic": dram_traffic(dom), "kernel": dom,
+
+    def kern(name, ms, nbytes, workload):
+        us = ms / K * 1e3
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return {"us_per_call": round(us, 3), "bytes": nbytes, "gbs": round(gbs, 1),
+                "frac": round(gbs / peak, 4), "frac_of_8tbs_spec": round(gbs / 8000.0, 4),
+                "traffic": dram_traffic(name, workload)}
+
+    v_kern = {"ln_modulate": kern("ln_modulate", v_ln_ms, V_LN_BYTES, "video"),
+              "rmsnorm_tanh_residual": kern("rmsnorm_tanh_residual", v_tanh_ms, V_TANH_BYTES, "video")}
+    i_kern = {"ln_modulate": kern("ln_modulate", i_ln_ms, I_LN_BYTES, "image"),
+              "residual_gate_add": kern("residual_gate_add", i_rga_ms, I_RGA_BYTES, "image")}
+    dom = max(v_kern, key=lambda k: v_kern[k]["us_per_call"])
+    roof = {"bound": "hbm", "achieved": v_kern[dom]["gbs"], "peak": peak, "unit": "GB/s",
+            "frac": v_kern[dom]["frac"], "traffic": v_kern[dom]["traffic"], "kernel": dom,
+            "bytes_per_launch": v_kern[dom]["bytes"],
+            "traffic_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, null unless "
+                            "captured on the current kernel source",
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
             else "fallback 6.8 TB/s"}
     cpu = None
@@ -497,28 +550,35 @@ def run_gpu(args):
         cpu_gbs, cpu_rows, cpu_s = oracle_rate(args.cpu_seconds)
         all_gbs, all_rows, all_s, all_n = oracle_rate_all_cores(args.cpu_seconds)
         cpu = {"value": round(all_gbs, 4), "unit": "GB/s", "cores": all_n, "kind": "oracle",
-               "sample": f"{all_rows} rows of the workload (both operations) in {all_s:.1f} s, "
-                         f"{all_n} processes, one per host core, each on a static share of the "
-                         f"rows; single thread: {cpu_gbs:.4f} GB/s ({cpu_rows} rows in {cpu_s:.1f} s)",
+               "sample": f"{all_rows} token rows of the headline step (both operations, [rows,5120]) "
+                         f"in {all_s:.1f} s, {all_n} processes, one per host core, each on a static "
+                         f"share of a 256-row sample; single thread: {cpu_gbs:.4f} GB/s "
+                         f"({cpu_rows} rows in {cpu_s:.1f} s)",
                "value_1_thread": round(cpu_gbs, 4)}
-    value = STEP_BYTES * K * world / (total_ms * 1e-3) / 1e9
+    value = V_STEP_BYTES * K * world / (v_ms * 1e-3) / 1e9
+    i_value = I_STEP_BYTES * K * world / (i_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5),
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(v_ms / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "l2": L2_NOTE, "variant": "lossless",
                    "parallelism": f"replicas x{world} (row-independent, no data-path collective)"},
-        "ln_modulate_us_per_call": kern["ln_modulate"]["us_per_call"],
+        "ln_modulate_us_per_call": v_kern["ln_modulate"]["us_per_call"],
         "frac_of_hbm_peak": round(value / world / peak, 4),
         "frac_of_8tbs_spec": round(value / world / 8000.0, 4),
-        "kernels": kern,
+        "kernels": v_kern,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 2 * K * world,
-        "kernel_timing": {"how": "each call alone, K launches back to back after the step loop, events at the ends",
-                          "launches": 2 * K * world},
+        "image_dit": {
+            "workload": I_WORKLOAD, "l2": I_L2_NOTE, "value": round(i_value, 2), "unit": "GB/s",
+            "ms_per_step": round(i_ms / K, 5), "frac_of_hbm_peak": round(i_value / world / peak, 4),
+            "ln_modulate_us_per_call": i_kern["ln_modulate"]["us_per_call"], "kernels": i_kern},
+        "gpu_launches": 8 * K * world,
+        "kernel_timing": {"how": "per workload: K steps with events at the ends, then each call alone, "
+                                 "K launches back to back, events at the ends",
+                          "launches": 8 * K * world},
         "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -754,6 +814,29 @@ def run_profile_calls(args):
                   lambda: mbx.gated_residual_ln_modulate(res, gt, upd, sc, sh, bias=b, out=out, residual_out=out2),
                   lambda: mbx.ln_modulate_fp8(res, sc, sh, s8, out=out, out_fp8=q8),
                   lambda: mbx.modulation_table_add(table, temb, out=tout)]
+    elif args.profile_calls == "video":  # the headline step, one buffer set: 2.35 GB on the device
+        d = synth.video_dit_block(device=dev)
+        out1, out2 = torch.empty_like(d["x"]), torch.empty_like(d["x"])
+        calls += [lambda: mbx.ln_modulate(d["x"], d["scale"], d["shift"], out=out1),
+                  lambda: mbx.rmsnorm_tanh_residual(d["x"], d["gate"], d["residual"], d["weight"], out=out2)]
+    elif args.profile_calls == "rms":  # both RMSNorm ops at image-DiT size, per-sample modulation
+        x, res, gtok = r(8704, 3072), r(8704, 3072), r(8704, 3072)
+        sc = r(2, 3072, std=0.1)
+        w = (torch.randn(3072, generator=g, device=dev) * 0.05 + 1).to(torch.bfloat16)
+        out = torch.empty_like(x)
+        calls += [lambda: mbx.rmsnorm_scale(x, w, sc, out=out),
+                  lambda: mbx.rmsnorm_tanh_residual(x, gtok, res, w, out=out)]
+    elif args.profile_calls == "nvfp4":  # the NVFP4 producers at image-DiT size
+        x, res, upd = r(8704, 3072), r(8704, 3072), r(8704, 3072)
+        gt, sc, sh = (r(2, 3072, std=0.1) for _ in range(3))
+        b = r(1, 3072, std=0.5)
+        out, out2 = torch.empty_like(x), torch.empty_like(x)
+        q4 = torch.empty(8704, 1536, dtype=torch.uint8, device=dev)
+        sf4 = torch.zeros(mbx.nvfp4_sf_shape(8704, 3072), dtype=torch.uint8, device=dev)
+        g4 = torch.full((1,), 60.0, dtype=torch.float32, device=dev)
+        calls += [lambda: mbx.ln_modulate_nvfp4(x, sc, sh, g4, out=out, out_fp4=q4, out_sf=sf4),
+                  lambda: mbx.gated_residual_ln_modulate_nvfp4(res, gt, upd, sc, sh, g4, bias=b, out=out,
+                                                               residual_out=out2, out_fp4=q4, out_sf=sf4)]
     for _ in range(args.steps):
         for c in calls:
             c()
@@ -765,15 +848,15 @@ def run_profile_calls(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="mbx", choices=["mbx", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only", default=None, help="with --suite: run only the named groups (tiny, image, video, table)")
     ap.add_argument("--suite", action="store_true",
                     help="time every operation and variant on the configurations' shapes "
                          "(one JSON line per case) instead of the benchmark step")
-    ap.add_argument("--profile-calls", default=None, choices=["ln", "image", "next"],
+    ap.add_argument("--profile-calls", default=None, choices=["ln", "image", "next", "video", "rms", "nvfp4"],
                     help="launch a fixed set of calls --steps times, untimed, for a profiler")
     args = ap.parse_args()
     if args.profile_calls:

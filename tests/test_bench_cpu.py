@@ -65,17 +65,30 @@ def test_gpu_arm_fails_without_gpu():
 
 def test_dram_traffic_table():
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    ops = []
+    rows = []
     with open(path) as f:
         for line in f:
             if line.startswith("#") or not line.strip():
                 continue
-            op, nbytes, sha = line.split()
+            op, workload, nbytes, sha = line.split()
+            assert op in bench._KERNEL_FILES and workload in ("video", "image")
             assert int(nbytes) > 0 and len(sha) == 16 and int(sha, 16) >= 0
-            ops.append((op, int(nbytes), sha))
-    assert {op for op, _, _ in ops} == {"ln_modulate", "residual_gate_add"}
-    for op, nbytes, sha in ops:
+            rows.append((op, workload, int(nbytes), sha))
+    assert rows
+    for op, workload, nbytes, sha in rows:
         cur = bench.kernel_sha(op)
         assert len(cur) == 16
         # reported only while the sources hash to the captured value
-        assert bench.dram_traffic(op) == (nbytes if cur == sha else None)
+        assert bench.dram_traffic(op, workload) == (nbytes if cur == sha else None)
+
+
+def test_step_bytes_are_the_algorithmic_bytes():
+    """Every input read once and every output written once, bf16."""
+    T = 32760 * 5120 * 2
+    assert bench.V_LN_BYTES == 4 * T                  # x, scale, shift, out
+    assert bench.V_TANH_BYTES == 4 * T + 5120 * 2     # x, g, r, out + weight
+    assert bench.V_STEP_BYTES == 8 * T + 10240 == 2_683_709_440
+    assert abs(bench.ROW_BYTES * 32760 - bench.V_STEP_BYTES) < 1e-3
+    t = 2 * 4352 * 3072 * 2
+    assert bench.I_LN_BYTES == 2 * t + 2 * 2 * 3072 * 2
+    assert bench.I_RGA_BYTES == 3 * t + 2 * 3072 * 2
