@@ -57,3 +57,34 @@ def guarded(shape, device, fill=0x7E7E, pad=4096):
         assert np.all(b[:pad] == fill) and np.all(b[pad + n:] == fill), "write outside the view"
 
     return view, check
+
+
+def par_rows(fn, rows: int, seq=None, align: int = 1, parts=None) -> list:
+    """Call fn(lo, hi) on disjoint row ranges that cover [0, rows), from a pool
+    of host threads, and return the results in row order.
+
+    The oracle is plain C called through ctypes, which releases the GIL for the
+    call, and it keeps no state between calls, so the ranges run on every host
+    core at once.  Each output row depends only on its own input rows and its
+    modulation row, so splitting the rows changes no bit of the result.  Ranges
+    start at multiples of `align` (128 keeps NVFP4 scale tiles whole) and never
+    cross a multiple of `seq` (so a range has one per-sample modulation row)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    n = parts or max(1, 4 * (os.cpu_count() or 1))
+    length = max(align, -(-rows // n))
+    length = -(-length // align) * align
+    bounds = []
+    for s0 in range(0, rows, seq or rows):
+        s1 = min(rows, s0 + (seq or rows))
+        for lo in range(s0, s1, length):
+            bounds.append((lo, min(s1, lo + length)))
+    with ThreadPoolExecutor(max_workers=os.cpu_count() or 1) as ex:
+        futs = [ex.submit(fn, lo, hi) for lo, hi in bounds]
+        return [f.result() for f in futs]
+
+
+def host_rows(t: torch.Tensor) -> np.ndarray:
+    """bfloat16 bit patterns of a device tensor as a contiguous [rows, D] host array."""
+    return u16(t).reshape(-1, t.shape[-1])

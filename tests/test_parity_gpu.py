@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import synth
-from tests.gpu_util import assert_bits_equal, assert_high_close, guarded, u16
+from tests.gpu_util import assert_bits_equal, assert_high_close, guarded, host_rows, par_rows, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -52,9 +52,10 @@ def test_image_dit_block_full_size(mbx):
     X, SC, SH, G, Y = _rows2(d["x"]), u16(d["scale"]), u16(d["shift"]), u16(d["gate"]), _rows2(d["y"])
     assert_bits_equal(_rows2(mbx.ln_modulate(x, sc, sh)), oracle.ln_modulate(X, SC, SH, 1e-6), "ln")
     assert_bits_equal(_rows2(mbx.residual_gate_add(x, g, y)), oracle.residual_gate_add(X, G, Y), "rga")
-    rows = np.r_[0:64, 4352 - 32:4352 + 32, 8704 - 64:8704]
-    ex, mag = oracle.ln_modulate_f64(X[rows], SC[rows // 4352], SH[rows // 4352], 1e-6)
-    assert_high_close(_rows2(mbx.ln_modulate(x, sc, sh, variant="high"))[rows], ex, mag, what="ln high")
+    got = _rows2(mbx.ln_modulate(x, sc, sh, variant="high"))
+    par_rows(lambda lo, hi: assert_high_close(
+        got[lo:hi], *oracle.ln_modulate_f64(X[lo:hi], SC[lo // 4352:lo // 4352 + 1], SH[lo // 4352:lo // 4352 + 1],
+                                            1e-6), what=f"ln high rows {lo}:{hi}"), 8704, seq=4352)
     ex, mag = oracle.residual_gate_add_f64(X, G, Y)
     assert_high_close(_rows2(mbx.residual_gate_add(x, g, y, variant="high")), ex, mag, what="rga high")
 
@@ -126,74 +127,71 @@ def test_qkv_epilogue_image_only_and_guard_zone(mbx):
 # ------------------------------------------------------------------ config 4
 
 
-def _sample_rows(T, n=384, seed=0):
-    rng = np.random.default_rng(seed)
-    r = np.unique(np.r_[0, 1, T // 2, T - 2, T - 1, rng.integers(0, T, size=n)])
-    return r[(r >= 0) & (r < T)]
-
-
 def test_video_dit_per_token_full_size(mbx):
+    """Video-DiT per-token modulation at its full size, as the benchmark runs
+    it: every element of both operations, lossless bit for bit and high
+    within 2 ulps of the binary64 result."""
     d = synth.video_dit_block(device=DEV)
     x, sc, sh, g, r, w = (d[k] for k in ("x", "scale", "shift", "gate", "residual", "weight"))
-    rows = _sample_rows(32760)
-    idx = torch.from_numpy(rows).to(DEV)
+    X, SC, SH, G, R, W = (host_rows(t) for t in (x, sc, sh, g, r, w))
+    W = W.reshape(-1)
+    T = X.shape[0]
 
-    def pick(t):
-        return u16(t.reshape(-1, 5120).index_select(0, idx))
-
-    X, SC, SH, G, R, W = pick(x), pick(sc), pick(sh), pick(g), pick(r), u16(w)
-    out = mbx.ln_modulate(x, sc, sh)
-    assert_bits_equal(pick(out), oracle.ln_modulate(X, SC, SH, 1e-6), "ln per-token")
-    out = mbx.rmsnorm_tanh_residual(x, g, r, w)
-    assert_bits_equal(pick(out), oracle.rmsnorm_tanh_residual(X, G, R, W, 1e-6), "tanh residual")
-    ex, mag = oracle.ln_modulate_f64(X, SC, SH, 1e-6)
-    assert_high_close(pick(mbx.ln_modulate(x, sc, sh, variant="high")), ex, mag, what="ln high")
-    ex, mag = oracle.rmsnorm_tanh_residual_f64(X, G, R, W, 1e-6)
-    assert_high_close(pick(mbx.rmsnorm_tanh_residual(x, g, r, w, variant="high")), ex, mag,
-                      what="tanh residual high")
+    got = host_rows(mbx.ln_modulate(x, sc, sh))
+    par_rows(lambda lo, hi: assert_bits_equal(
+        got[lo:hi], oracle.ln_modulate(X[lo:hi], SC[lo:hi], SH[lo:hi], 1e-6), f"ln per-token rows {lo}:{hi}"), T)
+    got = host_rows(mbx.ln_modulate(x, sc, sh, variant="high"))
+    par_rows(lambda lo, hi: assert_high_close(
+        got[lo:hi], *oracle.ln_modulate_f64(X[lo:hi], SC[lo:hi], SH[lo:hi], 1e-6), what=f"ln high rows {lo}:{hi}"), T)
+    got = host_rows(mbx.rmsnorm_tanh_residual(x, g, r, w))
+    par_rows(lambda lo, hi: assert_bits_equal(
+        got[lo:hi], oracle.rmsnorm_tanh_residual(X[lo:hi], G[lo:hi], R[lo:hi], W, 1e-6),
+        f"tanh residual rows {lo}:{hi}"), T)
+    got = host_rows(mbx.rmsnorm_tanh_residual(x, g, r, w, variant="high"))
+    par_rows(lambda lo, hi: assert_high_close(
+        got[lo:hi], *oracle.rmsnorm_tanh_residual_f64(X[lo:hi], G[lo:hi], R[lo:hi], W, 1e-6),
+        what=f"tanh residual high rows {lo}:{hi}"), T)
 
 
 # ------------------------------------------------------------------ config 5 (sweep)
 
 
-def _sweep_ops(mbx, d, rows=None, variant="lossless"):
-    """Run all four row operations on a sweep cell; returns {op: (gpu bits, oracle thunk)}."""
+def _sweep_ops(mbx, d):
+    """The four row operations on a sweep cell: {op: (gpu call(variant), oracle(lo, hi), binary64(lo, hi))}
+    with the oracle sides reading host copies of the inputs."""
     x, y, gt, r, sc, sh, g, w = (d[k] for k in ("x", "y", "gate_tok", "residual", "scale", "shift", "gate", "weight"))
-    T, D = x.shape
-    sel = slice(None) if rows is None else rows
-    pick = (lambda t: u16(t)[sel]) if rows is None else (lambda t: u16(t.index_select(0, torch.from_numpy(rows).to(t.device))))
-    xs, ys, gts, rs = pick(x), pick(y), pick(gt), pick(r)
+    X, Y, GT, R = (host_rows(t) for t in (x, y, gt, r))
     SC, SH, G, W = u16(sc), u16(sh), u16(g), u16(w)
-    res = {}
-    res["ln_modulate"] = (pick(mbx.ln_modulate(x, sc, sh, variant=variant)),
-                          lambda: oracle.ln_modulate(xs, SC, SH, 1e-6),
-                          lambda: oracle.ln_modulate_f64(xs, SC, SH, 1e-6))
-    res["rmsnorm_scale"] = (pick(mbx.rmsnorm_scale(x, w, sc, variant=variant)),
-                            lambda: oracle.rmsnorm_scale(xs, W, SC, 1e-6),
-                            lambda: oracle.rmsnorm_scale_f64(xs, W, SC, 1e-6))
-    res["rmsnorm_tanh_residual"] = (pick(mbx.rmsnorm_tanh_residual(x, gt, r, w, variant=variant)),
-                                    lambda: oracle.rmsnorm_tanh_residual(xs, gts, rs, W, 1e-6),
-                                    lambda: oracle.rmsnorm_tanh_residual_f64(xs, gts, rs, W, 1e-6))
-    res["residual_gate_add"] = (pick(mbx.residual_gate_add(x, g, y, variant=variant)),
-                                lambda: oracle.residual_gate_add(xs, G, ys),
-                                lambda: oracle.residual_gate_add_f64(xs, G, ys))
-    return res
+    return {
+        "ln_modulate": (lambda v: mbx.ln_modulate(x, sc, sh, variant=v),
+                        lambda lo, hi: oracle.ln_modulate(X[lo:hi], SC, SH, 1e-6),
+                        lambda lo, hi: oracle.ln_modulate_f64(X[lo:hi], SC, SH, 1e-6)),
+        "rmsnorm_scale": (lambda v: mbx.rmsnorm_scale(x, w, sc, variant=v),
+                          lambda lo, hi: oracle.rmsnorm_scale(X[lo:hi], W, SC, 1e-6),
+                          lambda lo, hi: oracle.rmsnorm_scale_f64(X[lo:hi], W, SC, 1e-6)),
+        "rmsnorm_tanh_residual": (lambda v: mbx.rmsnorm_tanh_residual(x, gt, r, w, variant=v),
+                                  lambda lo, hi: oracle.rmsnorm_tanh_residual(X[lo:hi], GT[lo:hi], R[lo:hi], W, 1e-6),
+                                  lambda lo, hi: oracle.rmsnorm_tanh_residual_f64(X[lo:hi], GT[lo:hi], R[lo:hi], W,
+                                                                                  1e-6)),
+        "residual_gate_add": (lambda v: mbx.residual_gate_add(x, g, y, variant=v),
+                              lambda lo, hi: oracle.residual_gate_add(X[lo:hi], G, Y[lo:hi]),
+                              lambda lo, hi: oracle.residual_gate_add_f64(X[lo:hi], G, Y[lo:hi])),
+    }
 
 
 @pytest.mark.parametrize("D", synth.SWEEP_D)
 @pytest.mark.parametrize("T", synth.SWEEP_T)
 def test_sweep(mbx, D, T):
-    big = T * D > 64 * 1024 * 1024
-    d = synth.sweep_case(D, T, device=DEV if big else "cpu")
-    if not big:
-        d = {k: (v.to(DEV) if torch.is_tensor(v) else v) for k, v in d.items()}
-    rows = _sample_rows(T, n=96, seed=D) if big else None
-    for name, (got, want, _) in _sweep_ops(mbx, d, rows).items():
-        assert_bits_equal(got, want(), f"{name} D={D} T={T}")
-    rows_h = rows if big else _sample_rows(T, n=48, seed=D)
-    for name, (got, _, exact) in _sweep_ops(mbx, d, rows_h, variant="high").items():
-        ex, mag = exact()
-        assert_high_close(got, ex, mag, what=f"{name} high D={D} T={T}")
+    """Every element of every cell (T up to 65536 rows of D up to 8192), both
+    variants, padded input rows with NaN sentinels in the pad."""
+    d = synth.sweep_case(D, T, device=DEV)
+    for name, (gpu, want, exact) in _sweep_ops(mbx, d).items():
+        got = host_rows(gpu("lossless"))
+        par_rows(lambda lo, hi: assert_bits_equal(got[lo:hi], want(lo, hi), f"{name} D={D} T={T} rows {lo}:{hi}"), T)
+        got = host_rows(gpu("high"))
+        par_rows(lambda lo, hi: assert_high_close(got[lo:hi], *exact(lo, hi),
+                                                  what=f"{name} high D={D} T={T} rows {lo}:{hi}"), T)
+        del got
 
 
 @pytest.mark.parametrize("D", [1024, 4096, 8192])
