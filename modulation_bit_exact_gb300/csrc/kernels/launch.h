@@ -218,6 +218,7 @@ struct PipeShape {
 int64_t pipe_rows_per_cta(int64_t rows);
 bool pipe_shape(const void* kernel, int tpr, int smem_per_group, int smem_fixed, int64_t rows, PipeShape* out);
 
+
 // Per-token modulation table: out[k*rows + r][d] = table[k][d] + temb[r][k*D + d].
 struct ModTableParams {
     float* out;

@@ -213,7 +213,12 @@ __device__ __forceinline__ void welford_stage(const RingT& ring, int s, int t, i
 //   kModStaged: a CTA's rows span at most two samples; their bf16(1+scale)
 //               (lossless) or scale (high) and shift are staged in shared
 //               memory once.
-enum { kModRing = 0, kModStaged = 1 };
+//   kModL1:     the gated kernel on rows too wide to stage the per-sample
+//               vectors beside a two-operand ring: gate, scale, shift and the
+//               bias are read from global memory where they are used (a
+//               sample's vectors are shared by all its rows, so they stay in
+//               L1 and L2), leaving shared memory to the ring.
+enum { kModRing = 0, kModStaged = 1, kModL1 = 2 };
 
 // Ring operands of the pipelined kernel: x (the residual when FUSED), then
 // the update (FUSED), then, in ring mode, the gate (FUSED) and, for fused rows
@@ -262,11 +267,11 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
     const int g = threadIdx.x / TPR, t = threadIdx.x % TPR;
     const int D = p.D;
     const int nch = D / kChunk;
-    TreeSmem& sm = reinterpret_cast<TreeSmem*>(smem_raw)[g];
-    uint4* mod = reinterpret_cast<uint4*>(smem_raw + groups * sizeof(TreeSmem));  // [2 slots][t|shift[|gate]][nch]
+    TreeAll<TPR>& sm = reinterpret_cast<TreeAll<TPR>*>(smem_raw)[g];
+    uint4* mod = reinterpret_cast<uint4*>(smem_raw + groups * sizeof(TreeAll<TPR>));  // [2 slots][t|shift[|gate]][nch]
     const int mod_chunks = MODE == kModStaged ? 2 * O::SLOT * nch : 0;
     uint4* bias_sm = mod + mod_chunks;  // [nch] when FUSED with a bias
-    const int bias_chunks = FUSED && p.bias != nullptr ? nch : 0;
+    const int bias_chunks = FUSED && MODE != kModL1 && p.bias != nullptr ? nch : 0;
     const R ring{bias_sm + bias_chunks + (size_t)g * (R::kBytes / 16)};
     const int bar_id = 1 + g;
     const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
@@ -276,6 +281,8 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
     const int64_t first = r0 + g;
     RowDiv next(first, groups, p.seq);  // modulation row of the next row to issue
     RowDiv here(first, groups, p.seq);  // modulation row of the row being processed
+    // (advanced per row in the modes that read a row's modulation from global memory)
+    constexpr bool kHere = O::DIRECT || MODE == kModL1;
     // while the previous kernel in the stream drains, bring this group's first
     // rows into L2; then wait for it before reading anything it may write
     if (t == 0)
@@ -344,7 +351,7 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
     }
     if constexpr (MODE == kModStaged || FUSED || FP4) __syncthreads();
 
-    int cur = 0;
+    int cur = 0, par = 0;
     for (int64_t row = first; row < r1; row += groups) {
         const int64_t rn = row + (NS - 1) * groups;
         const int sn = cur == 0 ? NS - 1 : cur - 1;
@@ -363,10 +370,9 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
 #pragma unroll
                 for (int m = 0; m < C::M; ++m) {
                     const int c = t + C::TPR * m + kLanes * j;
-                    if (c < nch) {
-                        dT[j][m] = ld_stream(sc_row + (int64_t)c * kChunk);
-                        dSH[j][m] = ld_stream(sh_row + (int64_t)c * kChunk);
-                    }
+                    const bool ok = c < nch;
+                    dT[j][m] = ok ? ld_stream(sc_row + (int64_t)c * kChunk) : make_uint4(0, 0, 0, 0);
+                    dSH[j][m] = ok ? ld_stream(sh_row + (int64_t)c * kChunk) : make_uint4(0, 0, 0, 0);
                 }
         }
 
@@ -374,6 +380,7 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
             // front pass: the new residual r' = bf16(x + bf16(gate * a)), written
             // out and back over x in this thread's own ring chunks
             const uint4* gm = MODE == kModStaged ? mod + (slot * O::SLOT + 2) * nch : nullptr;
+            const uint16_t* g_row = MODE == kModL1 ? p.gate + here.q * p.gate_stride : nullptr;
             uint16_t* res_row = p.res_out + row * p.res_out_stride;
 #pragma unroll
             for (int j = 0; j < C::J; ++j)
@@ -383,12 +390,13 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                     if (c >= nch) continue;
                     const uint4 X = lds16(ring.at(cur, 0, c));
                     uint4 U = lds16(ring.at(cur, O::U, c));
-                    if (bias_chunks) {
-                        const uint4 B = lds16(bias_sm + c);
+                    if (MODE == kModL1 ? p.bias != nullptr : bias_chunks != 0) {
+                        const uint4 B = MODE == kModL1 ? ld_shared_row(p.bias + (int64_t)c * kChunk) : lds16(bias_sm + c);
                         U = make_uint4(badd(U.x, B.x), badd(U.y, B.y), badd(U.z, B.z), badd(U.w, B.w));
                     }
                     uint4 G;
                     if constexpr (MODE == kModStaged) G = lds16(gm + c);
+                    else if constexpr (MODE == kModL1) G = ld_shared_row(g_row + (int64_t)c * kChunk);
                     else G = lds16(ring.at(cur, O::G > 0 ? O::G : 0, c));
                     const uint4 Y = make_uint4(badd(X.x, bmul(G.x, U.x)), badd(X.y, bmul(G.y, U.y)),
                                                badd(X.z, bmul(G.z, U.z)), badd(X.w, bmul(G.w, U.w)));
@@ -402,13 +410,11 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
             Wf L[C::M];
             const bool full = nch == kLanes * C::J;
             welford_stage<C, !FUSED && (J == 1 || J == 3)>(ring, cur, t, nch, full, L, f2(p.neg_zero, p.neg_zero));
-            const Wf s = full ? tree_reduce<C>(L, t, sm, bar_id, wf_combine_eq)
-                              : tree_reduce<C>(L, t, sm, bar_id, wf_combine);
+            const Wf s = full ? tree_allreduce_full<C>(L, t, sm, bar_id, par)
+                              : tree_allreduce<C>(L, t, sm, bar_id, par, D, wf_combine);
             mean = s.mean;
-            if (t == 0) {
-                const float var = __fdiv_rn(s.m2, (float)D);
-                rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, p.eps)));
-            }
+            const float var = __fdiv_rn(s.m2, (float)D);
+            rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, p.eps)));
         } else {
             if constexpr (C::J <= 2) {
                 // short rows: two passes (mean, then squared deviations), two trees
@@ -425,9 +431,11 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                         for (int i = 0; i < 4; ++i) acc[m] += lo_f(w_of(v, i)) + hi_f(w_of(v, i));
                     }
                 }
-                float dummy = 0.0f;
-                mean = tree_reduce<C>(acc, t, sm, bar_id, sum_combine) / (float)D;
-                group_bcast<C>(mean, dummy, t, sm, bar_id);
+                // (one warp per row at J <= 2: both trees are shuffles only)
+                static_assert(C::TPR == 32, "two trees per row need one warp per row");
+                mean = tree_w0_sum<C>(acc, t, sm, bar_id, par, [&](float S) {
+                    return make_float2(S / (float)D, 0.0f);
+                }).x;
 #pragma unroll
                 for (int m = 0; m < C::M; ++m) {
                     acc[m] = 0.0f;
@@ -443,8 +451,9 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                         }
                     }
                 }
-                const float q = tree_reduce<C>(acc, t, sm, bar_id, sum_combine);
-                if (t == 0) rstd = rsqrtf(q / (float)D + p.eps);
+                rstd = tree_w0_sum<C>(acc, t, sm, bar_id, par, [&](float q) {
+                    return make_float2(rsqrtf(q / (float)D + p.eps), 0.0f);
+                }).x;
             } else {
                 // longer rows: each lane's mean and sum of squared deviations
                 // from its own elements (two passes over the lane's chunks),
@@ -484,16 +493,17 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                     L[m] = Wf{lm, f2lo(q) + f2hi(q), (float)n};
                 }
                 const bool full = nch == kLanes * C::J;
-                const Wf st = full ? tree_reduce<C>(L, t, sm, bar_id, wf_combine_eq)
-                                   : tree_reduce<C>(L, t, sm, bar_id, wf_combine);
+                const Wf st = full ? tree_allreduce_full<C>(L, t, sm, bar_id, par)
+                                   : tree_allreduce<C>(L, t, sm, bar_id, par, D, wf_combine);
                 mean = st.mean;
-                if (t == 0) rstd = rsqrtf(st.m2 / (float)D + p.eps);
+                rstd = rsqrtf(st.m2 / (float)D + p.eps);
             }
             }
-        group_bcast<C>(mean, rstd, t, sm, bar_id);
 
         const uint4* tm = MODE == kModStaged ? mod + (slot * O::SLOT + 0) * nch : nullptr;
         const uint4* sh = MODE == kModStaged ? tm + nch : nullptr;
+        const uint16_t* sc_l1 = MODE == kModL1 ? p.scale + here.q * p.scale_stride : nullptr;
+        const uint16_t* sh_l1 = MODE == kModL1 ? p.shift + here.q * p.shift_stride : nullptr;
         uint16_t* out_row = p.out + row * p.out_stride;
         uint8_t* const q_row = FP4 ? p.out_fp4 + row * p.out_fp4_stride : nullptr;
         uint8_t* const sf_row = FP4 ? p.out_sf + nvfp4_sf_row(row, p.sf_col_tiles) : nullptr;
@@ -503,17 +513,27 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
 #pragma unroll
             for (int m = 0; m < C::M; ++m) {
                 const int c = t + C::TPR * m + kLanes * j;
-                const bool valid = c < nch;
-                if constexpr (!FP4) {
-                    if (!valid) continue;
+                // FP4 and L1 modes: a chunk past the end of a short row is
+                // computed from whatever its ring slot holds with only its
+                // stores skipped (no branch: every lane takes part in the FP4
+                // block shuffle, and the L1 loads can be issued early).
+                // Otherwise each chunk is tested and a missing one skipped:
+                // measured faster there (the compiler then keeps each chunk's
+                // loads beside its use).
+                constexpr bool kNoBranch = FP4 || MODE == kModL1;
+                if constexpr (!kNoBranch) {
+                    if (c >= nch) continue;
                 }
-                uint4 o = make_uint4(0, 0, 0, 0);
-                if (valid) {
+                const bool valid = !kNoBranch || j < C::J - 1 || c < nch;
+                const int cv = valid ? c : 0;  // FP4 reads of a missing chunk stay in its row's slots
                 const uint4 X = lds16(ring.at(cur, 0, c));
                 uint4 T, SH;
                 if constexpr (MODE == kModStaged) {
-                    T = lds16(tm + c);
-                    SH = lds16(sh + c);
+                    T = lds16(tm + cv);
+                    SH = lds16(sh + cv);
+                } else if constexpr (MODE == kModL1) {
+                    T = ld_shared_row(sc_l1 + (int64_t)cv * kChunk);
+                    SH = ld_shared_row(sh_l1 + (int64_t)cv * kChunk);
                 } else if constexpr (O::DIRECT) {
                     T = dT[O::DIRECT ? j : 0][O::DIRECT ? m : 0];
                     SH = dSH[O::DIRECT ? j : 0][O::DIRECT ? m : 0];
@@ -521,13 +541,14 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                     T = lds16(ring.at(cur, O::SC > 0 ? O::SC : 0, c));
                     SH = lds16(ring.at(cur, O::SH > 0 ? O::SH : 0, c));
                 }
+                uint4 o;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint32_t xw = w_of(X, i), tw = w_of(T, i), hw = w_of(SH, i);
                     uint32_t ow;
                     if constexpr (!HIGH) {
                         const uint32_t nrm = pack2_rn(mul2(sub2(widen2(xw), mean2), rstd2));
-                        // ring mode carries scale itself: round 1 + scale here
+                        // ring and L1 modes carry scale itself: round 1 + scale here
                         const uint32_t tt = MODE == kModStaged ? tw : badd(0x3f803f80u, tw);
                         ow = badd(bmul(nrm, tt), hw);
                     } else {
@@ -536,26 +557,27 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                     }
                     w_set(o, i, ow);
                 }
-                st_v4(out_row + (int64_t)c * kChunk, o);
-                if (p.out_fp8 != nullptr)
-                    st_v2(p.out_fp8 + row * p.out_fp8_stride + (int64_t)c * kChunk, e4m3x4_of_bf16(o.x, o.y, inv8),
-                          e4m3x4_of_bf16(o.z, o.w, inv8));
+                if (!kNoBranch || valid) {
+                    st_v4(out_row + (int64_t)c * kChunk, o);
+                    if (p.out_fp8 != nullptr)
+                        st_v2(p.out_fp8 + row * p.out_fp8_stride + (int64_t)c * kChunk, e4m3x4_of_bf16(o.x, o.y, inv8),
+                              e4m3x4_of_bf16(o.z, o.w, inv8));
                 }
                 if constexpr (FP4) {
                     // a 16-element block is chunks 2b and 2b+1, held by lanes
-                    // t and t^1 of the same warp (every lane takes part)
+                    // t and t^1 of the same warp
                     const float a8 = valid ? amax8_bf16(o) : 0.0f;
                     const float a16 = max_nan(a8, __shfl_xor_sync(0xffffffffu, a8, 1));
                     float esc;
                     const uint32_t sc = nvfp4_block_scale_tab(a16, gs4, fp4_tab, esc);
-                    if (valid) {
-                        st_u32(q_row + c * 4, nvfp4_codes_esc(o, sc, esc));
-                        if ((c & 1) == 0) sf_row[nvfp4_sf_block(c >> 1)] = (uint8_t)sc;
-                    }
+                    const uint32_t q = nvfp4_codes_esc(o, sc, esc);
+                    if (valid) st_u32(q_row + c * 4, q);
+                    if (valid && (c & 1) == 0) sf_row[nvfp4_sf_block(c >> 1)] = (uint8_t)sc;
                 }
             }
         cur = cur + 1 == NS ? 0 : cur + 1;
-        if constexpr (O::DIRECT) here.advance();
+        par ^= 1;
+        if constexpr (kHere) here.advance();
     }
     cp_async_wait<0>();
 }
@@ -569,18 +591,56 @@ static cudaError_t launch_pipe(const LnModParams& p, cudaStream_t s) {
     using O = LnOps<FUSED, MODE, J, HIGH>;
     using R = Ring<C, NS, O::N>;
     const int nch = p.D / kChunk;
-    const int fixed = (MODE == kModStaged ? 2 * O::SLOT * nch * 16 : 0) + (FUSED && p.bias ? nch * 16 : 0);
+    const int fixed = (MODE == kModStaged ? 2 * O::SLOT * nch * 16 : 0) + (FUSED && MODE != kModL1 && p.bias ? nch * 16 : 0);
     PipeShape sh;
-    if (!pipe_shape(reinterpret_cast<const void*>(k), TPR, (int)sizeof(TreeSmem) + R::kBytes, fixed, p.rows, &sh))
+    if (!pipe_shape(reinterpret_cast<const void*>(k), TPR, (int)sizeof(TreeAll<TPR>) + R::kBytes, fixed, p.rows, &sh))
         return cudaErrorInvalidConfiguration;
     return launch_pdl(k, sh.grid, sh.groups * TPR, sh.smem, s, p, sh.rows_per_cta);
 }
+
+// Row groups of the fused kernel that fit in shared memory in a modulation
+// mode: its stages carry the residual and the update (per token also the
+// gate, and scale and shift where they are not loaded directly); staged
+// per-sample modulation, gate and bias take a fixed share.  Same arithmetic
+// as launch_pipe.
+static int fused_groups(const LnModParams& p, bool high, int mode) {
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    const int J = chunks_per_lane(p.D), nch = p.D / kChunk;
+    const int nops = ln_ring_ops(true, mode, J, high);
+    const int tpr = J <= 2 ? 32 : J <= 4 ? 64 : 128;  // as launch_pipe_d chooses
+    const int tree = tpr == 32 ? (int)sizeof(TreeAll<32>) : tpr == 64 ? (int)sizeof(TreeAll<64>) : (int)sizeof(TreeAll<128>);
+    const int per_group = tree + 2 * nops * kLanes * J * 16;
+    const int fixed = (mode == kModStaged ? 2 * LnOps<true, kModStaged, 1, false>::SLOT * nch * 16 : 0) +
+                      (mode != kModL1 && p.bias ? nch * 16 : 0);
+    return (optin - 8 * 1024 - fixed) / per_group;
+}
+
+// The fused kernel's modulation mode, or -1 when no mode keeps at least two
+// row groups per SM (then two launches, gated add and LN, run faster).
+// Per-sample rows stage their vectors while that leaves two groups, and read
+// them from L1 beyond (rows of more than 4096 elements).
+static int fused_mode(const LnModParams& p, bool high) {
+    const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
+    if (!staged) return fused_groups(p, high, kModRing) >= 2 ? kModRing : -1;
+    if (fused_groups(p, high, kModStaged) >= 2) return kModStaged;
+    if (chunks_per_lane(p.D) >= 5 && fused_groups(p, high, kModL1) >= 2) return kModL1;
+    return -1;
+}
+
+static bool fused_fits(const LnModParams& p, bool high) { return fused_mode(p, high) >= 0; }
 
 template <int TPR, int J, int NS, bool FUSED, bool FP4>
 static cudaError_t launch_pipe_v(const LnModParams& p, bool high, cudaStream_t s) {
     // stage the modulation when each CTA's block of rows spans at most two
     // samples (rows per CTA <= seq); otherwise read it per row
     const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
+    if constexpr (FUSED && J >= 5) {
+        if (staged && fused_mode(p, high) == kModL1)
+            return high ? launch_pipe<TPR, J, NS, true, kModL1, FUSED, FP4>(p, s)
+                        : launch_pipe<TPR, J, NS, false, kModL1, FUSED, FP4>(p, s);
+    }
     if (high)
         return staged ? launch_pipe<TPR, J, NS, true, kModStaged, FUSED, FP4>(p, s)
                       : launch_pipe<TPR, J, NS, true, kModRing, FUSED, FP4>(p, s);
@@ -603,24 +663,6 @@ static cudaError_t launch_pipe_d(const LnModParams& p, bool high, cudaStream_t s
         case 8: return launch_pipe_v<128, 8, 2, FUSED, FP4>(p, high, s);
         default: return cudaErrorInvalidValue;
     }
-}
-
-// Whether the fused ring kernel keeps at least two row groups per SM: its
-// stages carry the residual and the update (per token also the gate, and
-// scale and shift where they are not loaded directly), and per-sample
-// modulation, gate and bias are staged.  At the widest rows
-// one group would remain, and two launches (gated add, then LN) move more
-// bytes but run faster.  Same arithmetic as launch_pipe.
-static bool fused_fits(const LnModParams& p, bool high) {
-    int dev = 0, optin = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    const int J = chunks_per_lane(p.D), nch = p.D / kChunk;
-    const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
-    const int nops = ln_ring_ops(true, staged ? kModStaged : kModRing, J, high);
-    const int per_group = (int)sizeof(TreeSmem) + 2 * nops * kLanes * J * 16;
-    const int fixed = (staged ? 2 * LnOps<true, kModStaged, 1, false>::SLOT * nch * 16 : 0) + (p.bias ? nch * 16 : 0);
-    return (optin - 8 * 1024 - fixed) / per_group >= 2;
 }
 
 }  // namespace mbx

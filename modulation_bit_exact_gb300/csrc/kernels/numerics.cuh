@@ -406,12 +406,20 @@ __device__ __forceinline__ uint32_t bmax_nan(uint32_t a, uint32_t b) {
     return d;
 }
 
-// |largest| of the eight bf16 values of a chunk, NaN propagating: the sign
-// bits cleared, pairwise bf16 maxima, then the larger half.
+// max.NaN.xorsign.abs of two bf16 pairs: per half, the larger magnitude (an
+// exact selection), NaN propagating; the sign bit is the xor of the operands'
+// signs, so callers clear it.
+__device__ __forceinline__ uint32_t bmaxabs_nan(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// |largest| of the eight bf16 values of a chunk, NaN propagating: pairwise
+// magnitude maxima, then the larger of the two halves with the sign cleared.
 __device__ __forceinline__ float amax8_bf16(const uint4& o) {
-    const uint32_t m = 0x7fff7fffu;
-    const uint32_t a = bmax_nan(bmax_nan(o.x & m, o.y & m), bmax_nan(o.z & m, o.w & m));
-    return max_nan(lo_f(a), hi_f(a));
+    const uint32_t a = bmaxabs_nan(bmaxabs_nan(o.x, o.y), bmaxabs_nan(o.z, o.w));
+    return max_nan(fabsf(lo_f(a)), fabsf(hi_f(a)));
 }
 
 // NVFP4 block step: from the block's amax and the global scale gs, the E4M3
@@ -427,18 +435,30 @@ __device__ __forceinline__ uint32_t nvfp4_block_scale(float amax16, float gs, fl
     return s;
 }
 
+// The E4M3 code of RN(d / 6), without a branch.  For |d| >= 2^-100 the
+// unguarded two-word quotient is RN(d / 6) (mbx_selftest(3)).  Below that
+// both it and RN(d / 6) have magnitude under 2^-102, far below half the
+// smallest E4M3 subnormal (2^-10), and carry the sign of d, so both convert
+// to the same signed zero.  An infinite or NaN d gives an infinite or NaN
+// quotient either way, which converts to the same code (saturated 0x7E / 0xFE,
+// or 0x7F for NaN).
+__device__ __forceinline__ uint32_t e4m3_of_div6(float d) {
+    const float q = div_k_fast<6>(d);
+    return e4m3x2(0.0f, isfinite(d) ? q : d) & 0xffu;
+}
+
 // The same step with the element factor gs / value(s) looked up in a table of
 // all 256 codes (built once per CTA by nvfp4_fill_table): returns s and sets
 // esc.
 __device__ __forceinline__ uint32_t nvfp4_block_scale_tab(float amax16, float gs, const float* tab, float& esc) {
-    const uint32_t s = e4m3x2(0.0f, div6(__fmul_rn(amax16, gs))) & 0xffu;
+    const uint32_t s = e4m3_of_div6(__fmul_rn(amax16, gs));
     esc = tab[s];
     return s;
 }
 __device__ __forceinline__ void nvfp4_fill_table(float* tab, float gs) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) {
         const float sv = e4m3_value((uint32_t)i);
-        tab[i] = __fdiv_rn(gs, sv);  // the entries of the two zero codes are never used
+        tab[i] = __fdiv_rn(gs, sv);  // the two zero codes' entries only feed discarded codes
     }
 }
 
@@ -447,7 +467,6 @@ __device__ __forceinline__ void nvfp4_fill_table(float* tab, float gs) {
 // +0 or -0), whatever esc.  The products are packed (each one rounding; they
 // feed conversions, not sums).
 __device__ __forceinline__ uint32_t nvfp4_codes_esc(const uint4& o, uint32_t s, float esc) {
-    if ((s & 0x7fu) == 0u) return 0u;
     const u64 e2 = f2(esc, esc);
     float v[8];
 #pragma unroll
@@ -456,7 +475,8 @@ __device__ __forceinline__ uint32_t nvfp4_codes_esc(const uint4& o, uint32_t s, 
         v[2 * i] = f2lo(pr);
         v[2 * i + 1] = f2hi(pr);
     }
-    return e2m1x8(v);
+    const uint32_t q = e2m1x8(v);
+    return (s & 0x7fu) != 0u ? q : 0u;  // selected, not branched
 }
 
 // The eight E2M1 codes of a chunk, e2m1(RN(y * RN(gs / sv))); 0 when sv is 0.

@@ -331,8 +331,8 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeAr
     const int g = threadIdx.x / TPR, t = threadIdx.x % TPR;
     const int D = p.D;
     const int nch = D / kChunk;
-    TreeSmem& sm = reinterpret_cast<TreeSmem*>(smem_raw)[g];
-    uint4* wsm = reinterpret_cast<uint4*>(smem_raw + groups * sizeof(TreeSmem));  // weight [nch]
+    TreeAll<TPR>& sm = reinterpret_cast<TreeAll<TPR>*>(smem_raw)[g];
+    uint4* wsm = reinterpret_cast<uint4*>(smem_raw + groups * sizeof(TreeAll<TPR>));  // weight [nch]
     uint4* msm = wsm + nch;                                                       // mod [2][nch]
     unsigned short* tab = reinterpret_cast<unsigned short*>(msm + (MODE == kRmsModStaged ? 2 * nch : 0));
     constexpr int kTab = OP == kRmsTanh && MODE == kRmsModRing ? (MBX_TANH_HI - MBX_TANH_LO) : 0;
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeAr
         for (int i = threadIdx.x; i < kTab; i += blockDim.x) tab[i] = kTanhBf16[i];
     __syncthreads();
 
-    int cur = 0;
+    int cur = 0, par = 0;
     for (int64_t row = first; row < r1; row += groups) {
         const int64_t rn = row + (NS - 1) * groups;
         const int sn = cur == 0 ? NS - 1 : cur - 1;
@@ -415,18 +415,17 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeAr
         float L[C::M];
         if constexpr (!HIGH) sumsq_stage<C>(ring, cur, t, nch, L);
         else sumsq_stage_f32<C>(ring, cur, t, nch, L);
-        const float S = tree_reduce<C>(L, t, sm, bar_id, sum_combine);
-        float rstd = 0.0f, unused = 0.0f;
-        if (t == 0) {
+        const float rstd = tree_w0_sum<C>(L, t, sm, bar_id, par, [&](float S) {
+            float r;
             if constexpr (!HIGH) {
                 const float ms = lo_f(pack_rn(__fdiv_rn(S, (float)D), 0.0f));
                 const float inner = lo_f(pack_rn(__fadd_rn(ms, p.eps), 0.0f));
-                rstd = lo_f(pack_rn(__fdiv_rn(1.0f, __fsqrt_rn(inner)), 0.0f));
+                r = lo_f(pack_rn(__fdiv_rn(1.0f, __fsqrt_rn(inner)), 0.0f));
             } else {
-                rstd = rsqrtf(S / (float)D + p.eps);
+                r = rsqrtf(S / (float)D + p.eps);
             }
-        }
-        group_bcast<C>(rstd, unused, t, sm, bar_id);
+            return make_float2(r, 0.0f);
+        }).x;
         const uint32_t r2 = bf16_bits(rstd);
         const uint4* mrow = MODE == kRmsModStaged ? msm + (row >= split ? nch : 0) : nullptr;
         uint16_t* out_row = p.out + row * p.out_stride;
@@ -470,6 +469,7 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeAr
                 st_v4(out_row + (int64_t)c * kChunk, o);
             }
         cur = cur + 1 == NS ? 0 : cur + 1;
+        par ^= 1;
         if constexpr (DMOD) here.advance();
     }
     cp_async_wait<0>();
@@ -484,7 +484,7 @@ static cudaError_t launch_rms_pipe(const typename RmsPipeArgs<OP>::P& p, cudaStr
     const int tab_bytes = OP == kRmsTanh && MODE == kRmsModRing ? (((MBX_TANH_HI - MBX_TANH_LO) + 7) / 8) * 16 : 0;
     const int fixed = nch * 16 + (MODE == kRmsModStaged ? 2 * nch * 16 : 0) + tab_bytes;
     PipeShape sh;
-    if (!pipe_shape(reinterpret_cast<const void*>(k), TPR, (int)sizeof(TreeSmem) + R::kBytes, fixed, p.rows, &sh))
+    if (!pipe_shape(reinterpret_cast<const void*>(k), TPR, (int)sizeof(TreeAll<TPR>) + R::kBytes, fixed, p.rows, &sh))
         return cudaErrorInvalidConfiguration;
     return launch_pdl(k, sh.grid, sh.groups * TPR, sh.smem, s, p, sh.rows_per_cta);
 }

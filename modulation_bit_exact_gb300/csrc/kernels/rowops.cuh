@@ -288,6 +288,214 @@ __device__ __forceinline__ void group_bcast(float& a, float& b, int t, TreeSmem&
     }
 }
 
+// ------------------------------------------------------------------ single-barrier tree
+//
+// The same tree with its result in every thread of the group, at one barrier
+// per row.  After the levels inside each thread, every thread publishes its
+// lane value; after one barrier each warp reads the values it needs and
+// computes the cross-warp levels itself (warp w's thread i forms the same
+// combine(L[l], L[l+s]) that warp 0's thread i forms, with the same operands,
+// so every warp holds the same bits), runs the shuffle levels, and takes the
+// result from its lane 0.  The published values are double-buffered by row
+// parity: a slot is written again two rows later, after the next row's
+// barrier, which every reader of the older row has passed.
+
+template <int TPR>
+struct TreeAll {
+    float v[2][2][TPR];  // [row parity][mean | m2, or the sum][thread]
+};
+template <>
+struct TreeAll<32> {  // one warp per row: shuffles only
+    float unused[4];
+};
+
+// Published values.  A Wf's count is not stored: the reader recomputes it from
+// the publishing thread's lanes (n_of).
+template <int N>
+__device__ __forceinline__ void tall_put(float (&a)[2][N], int i, float v) { a[0][i] = v; }
+template <int N>
+__device__ __forceinline__ void tall_put(float (&a)[2][N], int i, Wf v) {
+    a[0][i] = v.mean; a[1][i] = v.m2;
+}
+template <int N>
+__device__ __forceinline__ void tall_get(const float (&a)[2][N], int i, float& v, float) { v = a[0][i]; }
+template <int N>
+__device__ __forceinline__ void tall_get(const float (&a)[2][N], int i, Wf& v, float n) {
+    v.mean = a[0][i]; v.m2 = a[1][i]; v.n = n;
+}
+__device__ __forceinline__ float shfl_idx0(float v) { return __shfl_sync(0xffffffffu, v, 0); }
+__device__ __forceinline__ Wf shfl_idx0(Wf v) {
+    return Wf{__shfl_sync(0xffffffffu, v.mean, 0), __shfl_sync(0xffffffffu, v.m2, 0),
+              __shfl_sync(0xffffffffu, v.n, 0)};
+}
+
+// The cross-warp levels and the shuffle levels of the tree, after the levels
+// inside each thread (v = this thread's lane value, lane t), with the result
+// returned in every thread, as described above.  PUT(i, x) publishes thread
+// i's value, GET(i) reads it, COMB at level S combines, SHFL(x, s) shuffles
+// down, BCAST(x) takes lane 0's value.
+template <int TPR, class T, class Put, class Get, class Comb, class Shfl, class Bcast>
+__device__ __forceinline__ T tree_cross(T v, int t, int bar_id, Put put, Get get, Comb comb, Shfl shfl, Bcast bcast) {
+    if constexpr (TPR == 64) {
+        put(t, v);
+        group_bar(bar_id, TPR);
+        const T o = get(t ^ 32);
+        v = t < 32 ? comb(std::integral_constant<int, 32>{}, v, o) : comb(std::integral_constant<int, 32>{}, o, v);
+    } else if constexpr (TPR == 128) {
+        put(t, v);
+        group_bar(bar_id, TPR);
+        const int lo = t & 31;
+        const T a = get(lo), b = get(lo + 32), c = get(lo + 64), d = get(lo + 96);
+        // s = 64 for lanes lo and lo + 32, then s = 32
+        v = comb(std::integral_constant<int, 32>{}, comb(std::integral_constant<int, 64>{}, a, c),
+                 comb(std::integral_constant<int, 64>{}, b, d));
+    }
+    static_for<0, 5>([&](auto lc) {
+        constexpr int S = 16 >> decltype(lc)::value;
+        v = comb(std::integral_constant<int, S>{}, v, shfl(v, S));
+    });
+    return bcast(v);
+}
+
+// D: the row length, for the element counts of published Welford values
+// (thread i holds lanes i + TPR*m after the levels inside the thread).
+template <class C, class T, class Comb>
+__device__ __forceinline__ T tree_allreduce(T (&L)[C::M], int t, TreeAll<C::TPR>& sm, int bar_id, int par, int D,
+                                            Comb comb) {
+#pragma unroll
+    for (int s = 64; s >= C::TPR; s /= 2) {
+#pragma unroll
+        for (int m = 0; m < s / C::TPR; ++m) L[m] = comb(L[m], L[m + s / C::TPR]);
+    }
+    return tree_cross<C::TPR>(
+        L[0], t, bar_id,
+        [&](int i, T x) {
+            if constexpr (C::TPR > 32) tall_put(sm.v[par], i, x);
+        },
+        [&](int i) {
+            T x{};
+            if constexpr (C::TPR > 32) {
+                float n = 0.0f;
+                if constexpr (std::is_same<T, Wf>::value) {
+#pragma unroll
+                    for (int m = 0; m < C::M; ++m) n += (float)lane_count(i + C::TPR * m, D);
+                }
+                tall_get(sm.v[par], i, x, n);
+            }
+            return x;
+        },
+        [&](auto, T a, T b) { return comb(a, b); }, [](T x, int s) { return shfl_down_t(x, s); },
+        [](T x) { return shfl_idx0(x); });
+}
+
+// The Welford tree of a full row (every lane holds N0 = 8*J elements) with
+// its result in every thread: at level s both operands hold N0*64/s elements,
+// so wf_combine_eq's counts are compile-time constants (na/2 exact), and only
+// mean and M2 are published and shuffled.  Same operations on the same
+// operands as tree_reduce with wf_combine_eq: the same bits.
+template <int NA2>
+__device__ __forceinline__ Wf wf_combine_k(Wf a, Wf b) {
+    const float d = __fsub_rn(b.mean, a.mean);
+    return Wf{__fadd_rn(a.mean, __fmul_rn(d, 0.5f)),
+              __fadd_rn(__fadd_rn(a.m2, b.m2), __fmul_rn(__fmul_rn(d, d), (float)NA2)), 0.0f};
+}
+
+// The other realisation: warp 0 alone computes the cross-warp and shuffle
+// levels (a barrier per cross-warp level), thread 0 applies FIN to the result
+// (a scalar chain such as the RMSNorm rstd) and publishes two floats, and a
+// last barrier hands them to the group.  Fewer instructions than every warp
+// computing the tree and FIN, more waiting; measured faster for the RMSNorm
+// kernels and for the short-row two-pass statistics.
+template <int TPR, class T, class Put, class Get, class Comb, class Shfl, class Fin>
+__device__ __forceinline__ float2 tree_w0(T v, int t, int bar_id, Put put, Get get, Comb comb, Shfl shfl, Fin fin,
+                                          float* pub) {
+    if constexpr (TPR == 128) {
+        if (t >= 64) put(t, v);
+        group_bar(bar_id, TPR);
+        if (t < 64) v = comb(std::integral_constant<int, 64>{}, v, get(t + 64));
+        if (t >= 32 && t < 64) put(t, v);
+        group_bar(bar_id, TPR);
+        if (t < 32) v = comb(std::integral_constant<int, 32>{}, v, get(t + 32));
+    } else if constexpr (TPR == 64) {
+        if (t >= 32) put(t, v);
+        group_bar(bar_id, TPR);
+        if (t < 32) v = comb(std::integral_constant<int, 32>{}, v, get(t + 32));
+    }
+    float2 r = make_float2(0.0f, 0.0f);
+    if (t < 32) {
+        static_for<0, 5>([&](auto lc) {
+            constexpr int S = 16 >> decltype(lc)::value;
+            v = comb(std::integral_constant<int, S>{}, v, shfl(v, S));
+        });
+        if (t == 0) r = fin(v);
+    }
+    if constexpr (TPR == 32) {
+        return make_float2(__shfl_sync(0xffffffffu, r.x, 0), __shfl_sync(0xffffffffu, r.y, 0));
+    } else {
+        if (t == 0) {
+            pub[0] = r.x;
+            pub[1] = r.y;
+        }
+        group_bar(bar_id, TPR);
+        return make_float2(pub[0], pub[1]);
+    }
+}
+
+template <class C, class Fin>
+__device__ __forceinline__ float2 tree_w0_sum(float (&L)[C::M], int t, TreeAll<C::TPR>& sm, int bar_id, int par, Fin fin) {
+#pragma unroll
+    for (int s = 64; s >= C::TPR; s /= 2) {
+#pragma unroll
+        for (int m = 0; m < s / C::TPR; ++m) L[m] = sum_combine(L[m], L[m + s / C::TPR]);
+    }
+    float* pub = nullptr;
+    if constexpr (C::TPR > 32) pub = &sm.v[par][1][0];  // a sum uses only the first row
+    return tree_w0<C::TPR>(
+        L[0], t, bar_id,
+        [&](int i, float x) {
+            if constexpr (C::TPR > 32) sm.v[par][0][i] = x;
+        },
+        [&](int i) {
+            float x = 0.0f;
+            if constexpr (C::TPR > 32) x = sm.v[par][0][i];
+            return x;
+        },
+        [](auto, float a, float b) { return sum_combine(a, b); }, [](float x, int s) { return shfl_down_t(x, s); },
+        fin, pub);
+}
+
+template <class C>
+__device__ __forceinline__ Wf tree_allreduce_full(Wf (&L)[C::M], int t, TreeAll<C::TPR>& sm, int bar_id, int par) {
+    constexpr int N0 = kChunk * C::J;
+    static_for<0, 7>([&](auto lc) {  // levels s = 64 >> lc kept inside the thread
+        constexpr int S = 64 >> decltype(lc)::value;
+        if constexpr (S >= C::TPR) {
+#pragma unroll
+            for (int m = 0; m < S / C::TPR; ++m) L[m] = wf_combine_k<N0 * 32 / S>(L[m], L[m + S / C::TPR]);
+        }
+    });
+    Wf r = tree_cross<C::TPR>(
+        L[0], t, bar_id,
+        [&](int i, Wf x) {
+            if constexpr (C::TPR > 32) {
+                sm.v[par][0][i] = x.mean;
+                sm.v[par][1][i] = x.m2;
+            }
+        },
+        [&](int i) {
+            Wf x{0.0f, 0.0f, 0.0f};
+            if constexpr (C::TPR > 32) x = Wf{sm.v[par][0][i], sm.v[par][1][i], 0.0f};
+            return x;
+        },
+        [](auto sc, Wf a, Wf b) { return wf_combine_k<N0 * 32 / decltype(sc)::value>(a, b); },
+        [](Wf x, int s) {
+            return Wf{__shfl_down_sync(0xffffffffu, x.mean, s), __shfl_down_sync(0xffffffffu, x.m2, s), 0.0f};
+        },
+        [](Wf x) { return Wf{__shfl_sync(0xffffffffu, x.mean, 0), __shfl_sync(0xffffffffu, x.m2, 0), 0.0f}; });
+    r.n = (float)(kLanes * N0);
+    return r;
+}
+
 // Grid-wide row-group loop parameters.
 struct RowLoop {
     int t;       // thread index within the row group
