@@ -607,6 +607,7 @@ def run_suite(args):
     torch.cuda.set_device(dev)
     peak, _ = peaks()
     L2 = 129 * 2 ** 20
+    want_ops = set(args.ops.split(",")) if getattr(args, "ops", None) else None
 
     spread = {}  # min and max of the five repeats of the last case timed
 
@@ -703,6 +704,8 @@ def run_suite(args):
                 residual_out=s["out2"], out_fp4=s["q4"], out_sf=s["sf4"])),
         }
         for op, (nb, fn) in ops.items():
+            if want_ops and op not in want_ops:
+                continue
             for v in ("lossless", "high"):
                 us = time_cases(make, nb, lambda st: fn(st, v))
                 gbs = nb / (us * 1e-6) / 1e9
@@ -756,6 +759,11 @@ def run_suite(args):
             row_case("image-DiT [2,4352,3072]", 2, 4352, 3072, False)
         if "video" in only:
             row_case("video-DiT [1,32760,5120] per-token", 1, 32760, 5120, True)
+        if "qkv" in only:
+            qkv_case("QKV epilogue [2,256+64x64,24x128]", 2, 256, 64, 64, 24)
+        if "sweep" in only:
+            for D in (1024, 3072, 4096, 8192):
+                row_case(f"sweep [65536,{D}]", 1, 65536, D, False)
         return 0
     row_case("tiny [2,256,512]", 2, 256, 512, False)
     row_case("sweep [77,3072]", 1, 77, 3072, False)
@@ -852,7 +860,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="mbx", choices=["mbx", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", default=None, help="with --suite: run only the named groups (tiny, image, video, table)")
+    ap.add_argument("--only", default=None,
+                    help="with --suite: run only the named groups (tiny, image, video, qkv, sweep, table)")
+    ap.add_argument("--ops", default=None, help="with --suite: run only the named operations (comma list)")
     ap.add_argument("--suite", action="store_true",
                     help="time every operation and variant on the configurations' shapes "
                          "(one JSON line per case) instead of the benchmark step")
