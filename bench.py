@@ -761,8 +761,11 @@ def run_suite(args):
             row_case("video-DiT [1,32760,5120] per-token", 1, 32760, 5120, True)
         if "qkv" in only:
             qkv_case("QKV epilogue [2,256+64x64,24x128]", 2, 256, 64, 64, 24)
-        if "sweep" in only:
+        if "sweep" in only.split(","):
             for D in (1024, 3072, 4096, 8192):
+                row_case(f"sweep [65536,{D}]", 1, 65536, D, False)
+        if "sweep2" in only.split(","):
+            for D in (2048, 5120, 6144):
                 row_case(f"sweep [65536,{D}]", 1, 65536, D, False)
         return 0
     row_case("tiny [2,256,512]", 2, 256, 512, False)
@@ -861,7 +864,7 @@ def main():
     ap.add_argument("--impl", default="mbx", choices=["mbx", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only", default=None,
-                    help="with --suite: run only the named groups (tiny, image, video, qkv, sweep, table)")
+                    help="with --suite: run only the named groups (tiny, image, video, qkv, sweep, sweep2, table)")
     ap.add_argument("--ops", default=None, help="with --suite: run only the named operations (comma list)")
     ap.add_argument("--suite", action="store_true",
                     help="time every operation and variant on the configurations' shapes "

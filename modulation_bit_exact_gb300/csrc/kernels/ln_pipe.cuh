@@ -9,6 +9,8 @@
 // the FP8/NVFP4 stores follow the section 将FP8量化融合到前序算子 and the
 // gated-residual chain of section Qwen-Image FP8和NVFP4优化 of the same article.
 #pragma once
+#include <algorithm>
+
 #include "launch.h"
 #include "rowops.cuh"
 
@@ -220,9 +222,13 @@ __device__ __forceinline__ void welford_stage(const RingT& ring, int s, int t, i
 //               L1 and L2), leaving shared memory to the ring.
 enum { kModRing = 0, kModStaged = 1, kModL1 = 2 };
 
-// Ring operands of the pipelined kernel: x (the residual when FUSED), then
-// the update (FUSED), then, in ring mode, the gate (FUSED) and, for fused rows
-// of more than 4096 elements, scale and shift.
+// Ring operands of the pipelined kernel: x (the residual when FUSED), then,
+// in ring mode, the gate (FUSED) and, for fused rows of more than 4096
+// elements, scale and shift.  The fused kernel's update is read once, by the
+// front pass, so it has a single stage of its own: the next row's update is
+// copied in right after the front pass has consumed the current one, and
+// lands while the statistics and the output pass run.  That frees a ring
+// operand's second stage, so more row groups fit.
 //
 // Per-row modulation is otherwise read from global memory into registers when
 // the row's data has landed (its latency hides behind the statistics), so it
@@ -231,21 +237,28 @@ enum { kModRing = 0, kModStaged = 1, kModL1 = 2 };
 // scale and shift where the registers they would hold cost more than the ring
 // stages (measured): J >= 5, and the high variant at J = 4.
 constexpr bool ln_fused_direct(int J, bool high) { return J <= 3 || (J == 4 && !high); }
+// Whether the fused kernel's update takes the one-stage buffer (measured per
+// row width: faster except at 4096 and 5120 elements, where the update keeps
+// its two ring stages).
+constexpr bool ln_update_one_stage(int J) { return J != 4 && J != 5; }
 constexpr int ln_ring_ops(bool fused, int mode, int J, bool high) {
-    return mode != kModRing ? (fused ? 2 : 1) : !fused ? 1 : ln_fused_direct(J, high) ? 3 : 5;
+    const int u = fused && !ln_update_one_stage(J) ? 1 : 0;
+    return u + (mode != kModRing ? 1 : !fused ? 1 : ln_fused_direct(J, high) ? 2 : 4);
 }
 
 template <bool FUSED, int MODE, int J, bool HIGH>
 struct LnOps {
     static constexpr bool DIRECT = MODE == kModRing && (!FUSED || ln_fused_direct(J, HIGH));
     static constexpr bool RING_MOD = MODE == kModRing && FUSED && !DIRECT;  // scale, shift in the ring
-    static constexpr int U = FUSED ? 1 : -1;
-    static constexpr int SC = RING_MOD ? 2 : -1;
-    static constexpr int SH = RING_MOD ? 3 : -1;
-    static constexpr int G = MODE == kModRing && FUSED ? (RING_MOD ? 4 : 2) : -1;
+    static constexpr bool USTAGE = FUSED && ln_update_one_stage(J);  // update in its own one-stage buffer
+    static constexpr int U = FUSED && !USTAGE ? 1 : -1;                 // else in the ring, after x
+    static constexpr int B = U > 0 ? 2 : 1;                              // first modulation operand
+    static constexpr int SC = RING_MOD ? B : -1;
+    static constexpr int SH = RING_MOD ? B + 1 : -1;
+    static constexpr int G = MODE == kModRing && FUSED ? (RING_MOD ? B + 2 : B) : -1;
     static constexpr int N = ln_ring_ops(FUSED, MODE, J, HIGH);
     static constexpr int SLOT = FUSED ? 3 : 2;  // staged arrays per sample: t, shift[, gate]
-    static_assert(N == 1 + (FUSED ? 1 : 0) + (G >= 0 ? 1 : 0) + (RING_MOD ? 2 : 0), "ring operands");
+    static_assert(N == 1 + (U > 0 ? 1 : 0) + (G >= 0 ? 1 : 0) + (RING_MOD ? 2 : 0), "ring operands");
 };
 
 __device__ __forceinline__ void sts16(uint4* p, uint4 v) {
@@ -273,6 +286,9 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
     uint4* bias_sm = mod + mod_chunks;  // [nch] when FUSED with a bias
     const int bias_chunks = FUSED && MODE != kModL1 && p.bias != nullptr ? nch : 0;
     const R ring{bias_sm + bias_chunks + (size_t)g * (R::kBytes / 16)};
+    // the fused kernel's one-stage update buffers, after every group's ring
+    const Ring<C, 1, 1> ustage{bias_sm + bias_chunks + (size_t)groups * (R::kBytes / 16) +
+                               (size_t)g * (O::USTAGE ? Ring<C, 1, 1>::kBytes / 16 : 0)};
     const int bar_id = 1 + g;
     const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
     const int64_t r1 = r0 + rows_per_cta < p.rows ? r0 + rows_per_cta : p.rows;
@@ -308,7 +324,7 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
 
     auto issue = [&](int s, int64_t row) {
         ring.issue(s, 0, p.x + row * p.x_stride, t, nch);
-        if constexpr (FUSED) ring.issue(s, O::U, p.update + row * p.update_stride, t, nch);
+        if constexpr (O::U > 0) ring.issue(s, O::U, p.update + row * p.update_stride, t, nch);
         if constexpr (O::RING_MOD) {
             ring.issue(s, O::SC > 0 ? O::SC : 0, p.scale + next.q * p.scale_stride, t, nch);
             ring.issue(s, O::SH > 0 ? O::SH : 0, p.shift + next.q * p.shift_stride, t, nch);
@@ -320,6 +336,10 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
         const int64_t r = first + s * groups;
         if (r < r1) issue(s, r);
         if constexpr (MODE == kModRing) next.advance();
+        cp_async_commit();
+    }
+    if constexpr (O::USTAGE) {  // the first row's update, a commit group of its own
+        if (first < r1) ustage.issue(0, 0, p.update + first * p.update_stride, t, nch);
         cp_async_commit();
     }
     // the first rows are on their way; stage the modulation meanwhile
@@ -389,7 +409,7 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                     const int c = t + C::TPR * m + kLanes * j;
                     if (c >= nch) continue;
                     const uint4 X = lds16(ring.at(cur, 0, c));
-                    uint4 U = lds16(ring.at(cur, O::U, c));
+                    uint4 U = O::USTAGE ? lds16(ustage.at(0, 0, c)) : lds16(ring.at(cur, O::U > 0 ? O::U : 0, c));
                     if (MODE == kModL1 ? p.bias != nullptr : bias_chunks != 0) {
                         const uint4 B = MODE == kModL1 ? ld_shared_row(p.bias + (int64_t)c * kChunk) : lds16(bias_sm + c);
                         U = make_uint4(badd(U.x, B.x), badd(U.y, B.y), badd(U.z, B.z), badd(U.w, B.w));
@@ -403,6 +423,12 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                     st_v4(res_row + (int64_t)c * kChunk, Y);
                     sts16(ring.at(cur, 0, c), Y);
                 }
+            if constexpr (O::USTAGE) {
+                // this thread has consumed its update chunks: copy the next row's in
+                // (the commit group the next row's wait completes together with x)
+                if (row + groups < r1) ustage.issue(0, 0, p.update + (row + groups) * p.update_stride, t, nch);
+                cp_async_commit();
+            }
         }
 
         float mean = 0.0f, rstd = 0.0f;
@@ -593,7 +619,8 @@ static cudaError_t launch_pipe(const LnModParams& p, cudaStream_t s) {
     const int nch = p.D / kChunk;
     const int fixed = (MODE == kModStaged ? 2 * O::SLOT * nch * 16 : 0) + (FUSED && MODE != kModL1 && p.bias ? nch * 16 : 0);
     PipeShape sh;
-    if (!pipe_shape(reinterpret_cast<const void*>(k), TPR, (int)sizeof(TreeAll<TPR>) + R::kBytes, fixed, p.rows, &sh))
+    const int per_group = (int)sizeof(TreeAll<TPR>) + R::kBytes + (O::USTAGE ? Ring<C, 1, 1>::kBytes : 0);
+    if (!pipe_shape(reinterpret_cast<const void*>(k), TPR, per_group, fixed, p.rows, &sh))
         return cudaErrorInvalidConfiguration;
     return launch_pdl(k, sh.grid, sh.groups * TPR, sh.smem, s, p, sh.rows_per_cta);
 }
@@ -611,7 +638,7 @@ static int fused_groups(const LnModParams& p, bool high, int mode) {
     const int nops = ln_ring_ops(true, mode, J, high);
     const int tpr = J <= 2 ? 32 : J <= 4 ? 64 : 128;  // as launch_pipe_d chooses
     const int tree = tpr == 32 ? (int)sizeof(TreeAll<32>) : tpr == 64 ? (int)sizeof(TreeAll<64>) : (int)sizeof(TreeAll<128>);
-    const int per_group = tree + 2 * nops * kLanes * J * 16;
+    const int per_group = tree + (2 * nops + (ln_update_one_stage(J) ? 1 : 0)) * kLanes * J * 16;  // + the update's one stage
     const int fixed = (mode == kModStaged ? 2 * LnOps<true, kModStaged, 1, false>::SLOT * nch * 16 : 0) +
                       (mode != kModL1 && p.bias ? nch * 16 : 0);
     return (optin - 8 * 1024 - fixed) / per_group;
@@ -619,14 +646,18 @@ static int fused_groups(const LnModParams& p, bool high, int mode) {
 
 // The fused kernel's modulation mode, or -1 when no mode keeps at least two
 // row groups per SM (then two launches, gated add and LN, run faster).
-// Per-sample rows stage their vectors while that leaves two groups, and read
-// them from L1 beyond (rows of more than 4096 elements).
+// Per-sample rows stage their vectors unless reading them from L1 fits at
+// least twice the row groups (rows of more than 4096 elements).
 static int fused_mode(const LnModParams& p, bool high) {
     const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
     if (!staged) return fused_groups(p, high, kModRing) >= 2 ? kModRing : -1;
-    if (fused_groups(p, high, kModStaged) >= 2) return kModStaged;
-    if (chunks_per_lane(p.D) >= 5 && fused_groups(p, high, kModL1) >= 2) return kModL1;
-    return -1;
+    const int cap = chunks_per_lane(p.D) >= 5 ? 4 : 8;  // 512 threads per CTA
+    const int gs = std::min(fused_groups(p, high, kModStaged), cap);
+    const int gl = chunks_per_lane(p.D) >= 5 ? std::min(fused_groups(p, high, kModL1), cap) : 0;
+    // the L1 mode's global reads cost more than the staged form's shared ones:
+    // taken where it fits at least twice the row groups (measured)
+    if (gs >= 2 && gl < 2 * gs) return kModStaged;
+    return gl >= 2 ? kModL1 : -1;
 }
 
 static bool fused_fits(const LnModParams& p, bool high) { return fused_mode(p, high) >= 0; }

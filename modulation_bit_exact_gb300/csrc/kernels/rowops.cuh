@@ -308,6 +308,10 @@ template <>
 struct TreeAll<32> {  // one warp per row: shuffles only
     float unused[4];
 };
+// The kernels place 16-byte-aligned arrays (modulation, ring stages) right
+// after the groups' tree buffers.
+static_assert(sizeof(TreeAll<32>) % 16 == 0 && sizeof(TreeAll<64>) % 16 == 0 && sizeof(TreeAll<128>) % 16 == 0,
+              "tree buffers keep the 16-byte alignment of what follows them");
 
 // Published values.  A Wf's count is not stored: the reader recomputes it from
 // the publishing thread's lanes (n_of).
