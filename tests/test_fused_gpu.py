@@ -151,6 +151,27 @@ def test_in_place_and_guard_zones(mbx):
     assert_bits_equal(u16(out), want_o, "in-place out")
 
 
+@pytest.mark.parametrize("D,bias", [(8192, False), (6144, True), (2048, True)])
+def test_wide_rows_modes(mbx, D, bias):
+    """Rows whose per-sample vectors are read through L1 instead of staged
+    (8192, 6144 by the mode policy) and the update's one-stage buffer, with and
+    without a bias, over more rows than row groups."""
+    _check(mbx, _case(2, 300, D, bias=bias), f"D={D} bias={bias}")
+
+
+def test_in_place_wide_rows(mbx):
+    """In place on the residual at the widest rows (L1 mode)."""
+    c = _case(2, 97, 8192)
+    (want_r, want_o), _ = _oracle(c)
+    d = {k: (v.to(DEV) if torch.is_tensor(v) else v) for k, v in c.items()}
+    res = d["residual"]
+    r, o = mbx.gated_residual_ln_modulate(res, d["gate"], d["update"], d["scale"], d["shift"], bias=d["bias"],
+                                          residual_out=res)
+    torch.cuda.synchronize()
+    assert_bits_equal(u16(res), want_r, "in-place residual")
+    assert_bits_equal(u16(o), want_o, "in-place out")
+
+
 def test_equals_the_two_kernels(mbx):
     """Without a bias the fused call gives exactly residual_gate_add followed
     by ln_modulate of the CUDA path."""
