@@ -294,13 +294,27 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
     const int64_t r1 = r0 + rows_per_cta < p.rows ? r0 + rows_per_cta : p.rows;
     const int64_t m0 = r0 / p.seq;
     const int64_t split = (m0 + 1) * p.seq;  // staged: rows from here use slot 1
-    const int64_t first = r0 + g;
+    // rows go to the groups in reverse order, so a block's extra rows (its row
+    // count mod the groups) fall to the highest-numbered groups, whose warps
+    // the schedulers serve first (measured: they finish a round earliest)
+    const int64_t first = r0 + (groups - 1 - g);
     RowDiv next(first, groups, p.seq);  // modulation row of the next row to issue
     RowDiv here(first, groups, p.seq);  // modulation row of the row being processed
     // (advanced per row in the modes that read a row's modulation from global memory)
     constexpr bool kHere = O::DIRECT || MODE == kModL1;
-    // while the previous kernel in the stream drains, bring this group's first
-    // rows into L2; then wait for it before reading anything it may write
+    // while the previous kernel in the stream drains, bring the per-sample
+    // vectors of this block's rows (first: every row group needs them before
+    // its first row) and this group's first rows into L2; then wait for it
+    // before reading anything it may write
+    if (t == 0 && g == 0 && MODE != kModRing && r1 > r0) {
+        const int64_t m_last = (r1 - 1) / p.seq;
+        for (int64_t m = m0; m <= m_last && m <= m0 + 1; ++m) {
+            prefetch_l2_bulk(p.scale + m * p.scale_stride, (uint32_t)D * 2);
+            prefetch_l2_bulk(p.shift + m * p.shift_stride, (uint32_t)D * 2);
+            if constexpr (FUSED) prefetch_l2_bulk(p.gate + m * p.gate_stride, (uint32_t)D * 2);
+        }
+    }
+    if (FUSED && t == 0 && g == 0 && p.bias != nullptr) prefetch_l2_bulk(p.bias, (uint32_t)D * 2);
     if (t == 0)
 #pragma unroll
         for (int s = 0; s < kPrefetchRows; ++s) {

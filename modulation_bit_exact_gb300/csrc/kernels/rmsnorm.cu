@@ -344,10 +344,23 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeAr
     const int64_t split = (m0 + 1) * p.seq;  // staged: rows from here use slot 1
     const uint16_t* modp = A::mod(p);
     const int64_t mod_stride = A::mod_stride(p);
-    const int64_t first = r0 + g;
+    // rows go to the groups in reverse order, so a block's extra rows (its row
+    // count mod the groups) fall to the highest-numbered groups, whose warps
+    // the schedulers serve first (measured: they finish a round earliest)
+    const int64_t first = r0 + (groups - 1 - g);
     RowDiv here(first, groups, p.seq);  // modulation row of the row being processed
-    // while the previous kernel in the stream drains, bring this group's first
-    // rows into L2; then wait for it before reading anything it may write
+    // while the previous kernel in the stream drains, bring the weight and the
+    // per-sample modulation of this block's rows (first: every row group needs
+    // them before its first row) and this group's first rows into L2, and copy
+    // the tanh table (constant) into shared memory; then wait for it before
+    // reading anything it may write
+    if (t == 0 && g == 0 && r1 > r0) {
+        prefetch_l2_bulk(p.weight, (uint32_t)D * 2);
+        if constexpr (MODE == kRmsModStaged) {
+            const int64_t m_last = (r1 - 1) / p.seq;
+            for (int64_t m = m0; m <= m_last && m <= m0 + 1; ++m) prefetch_l2_bulk(modp + m * mod_stride, (uint32_t)D * 2);
+        }
+    }
     if (t == 0)
 #pragma unroll
         for (int s = 0; s < kRmsPrefetchRows; ++s) {
@@ -356,6 +369,8 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeAr
             prefetch_l2_bulk(p.x + r * p.x_stride, (uint32_t)D * 2);
             if constexpr (DRES) prefetch_l2_bulk(A::residual(p) + r * A::res_stride(p), (uint32_t)D * 2);
         }
+    if constexpr (OP == kRmsTanh && !HIGH && MODE == kRmsModRing)
+        for (int i = threadIdx.x; i < kTab; i += blockDim.x) tab[i] = kTanhBf16[i];
     grid_dep_wait();
     grid_dep_launch();
 
@@ -383,8 +398,6 @@ __global__ void __launch_bounds__(512, 1) rmsnorm_pipe_kernel(typename RmsPipeAr
             msm[slot * nch + c] = v;
         }
     }
-    if constexpr (OP == kRmsTanh && !HIGH && MODE == kRmsModRing)
-        for (int i = threadIdx.x; i < kTab; i += blockDim.x) tab[i] = kTanhBf16[i];
     __syncthreads();
 
     int cur = 0, par = 0;
