@@ -696,12 +696,23 @@ static cudaError_t launch_pipe_v(const LnModParams& p, bool high, cudaStream_t s
 template <bool FUSED, bool FP4>
 static cudaError_t launch_pipe_d(const LnModParams& p, bool high, cudaStream_t s) {
     // one warp per row up to 2048 elements, two up to 4096 (measured fastest
-    // at 3072: fewer, longer row rounds), four above
+    // at 3072: fewer, longer row rounds), four above.  The unfused kernel
+    // without the NVFP4 store takes four warps at 4096 (measured faster there,
+    // most of all with the FP8 copy), and with the FP8 copy also at 3072 on
+    // 32768 rows or more (faster at 65536 rows, slower at 8704).
+    constexpr bool kPlain = !FUSED && !FP4;
+    const bool fp8 = p.out_fp8 != nullptr;
     switch (chunks_per_lane(p.D)) {
         case 1: return launch_pipe_v<32, 1, 2, FUSED, FP4>(p, high, s);
         case 2: return launch_pipe_v<32, 2, 2, FUSED, FP4>(p, high, s);
-        case 3: return launch_pipe_v<64, 3, 2, FUSED, FP4>(p, high, s);
-        case 4: return launch_pipe_v<64, 4, 2, FUSED, FP4>(p, high, s);
+        case 3:
+            if constexpr (kPlain) {
+                if (fp8 && p.rows >= 32768) return launch_pipe_v<128, 3, 2, FUSED, FP4>(p, high, s);
+            }
+            return launch_pipe_v<64, 3, 2, FUSED, FP4>(p, high, s);
+        case 4:
+            if constexpr (kPlain) return launch_pipe_v<128, 4, 2, FUSED, FP4>(p, high, s);
+            else return launch_pipe_v<64, 4, 2, FUSED, FP4>(p, high, s);
         case 5: return launch_pipe_v<128, 5, 2, FUSED, FP4>(p, high, s);
         case 6: return launch_pipe_v<128, 6, 2, FUSED, FP4>(p, high, s);
         case 7: return launch_pipe_v<128, 7, 2, FUSED, FP4>(p, high, s);
