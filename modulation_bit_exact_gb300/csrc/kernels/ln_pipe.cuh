@@ -456,8 +456,9 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
             const float var = __fdiv_rn(s.m2, (float)D);
             rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, p.eps)));
         } else {
-            if constexpr (C::J <= 2) {
-                // short rows: two passes (mean, then squared deviations), two trees
+            if constexpr (C::J <= 2 && C::TPR == 32) {
+                // short rows, one warp per row: two passes (mean, then squared
+                // deviations), two trees
                 float acc[C::M];
 #pragma unroll
                 for (int m = 0; m < C::M; ++m) {
@@ -471,8 +472,7 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                         for (int i = 0; i < 4; ++i) acc[m] += lo_f(w_of(v, i)) + hi_f(w_of(v, i));
                     }
                 }
-                // (one warp per row at J <= 2: both trees are shuffles only)
-                static_assert(C::TPR == 32, "two trees per row need one warp per row");
+                // (one warp per row: both trees are shuffles only)
                 mean = tree_w0_sum<C>(acc, t, sm, bar_id, par, [&](float S) {
                     return make_float2(S / (float)D, 0.0f);
                 }).x;
@@ -495,9 +495,10 @@ __global__ void __launch_bounds__(512, 1) ln_modulate_pipe_kernel(LnModParams p,
                     return make_float2(rsqrtf(q / (float)D + p.eps), 0.0f);
                 }).x;
             } else {
-                // longer rows: each lane's mean and sum of squared deviations
-                // from its own elements (two passes over the lane's chunks),
-                // then one tree of Chan combines (measured faster from J = 3)
+                // longer rows, or more than one warp per row: each lane's mean
+                // and sum of squared deviations from its own elements (two
+                // passes over the lane's chunks), then one tree of Chan
+                // combines (measured faster from J = 3)
                 // (element pairs of a word in f32x2, two accumulators per pass:
                 // short dependency chains)
                 Wf L[C::M];
@@ -639,6 +640,28 @@ static cudaError_t launch_pipe(const LnModParams& p, cudaStream_t s) {
     return launch_pdl(k, sh.grid, sh.groups * TPR, sh.smem, s, p, sh.rows_per_cta);
 }
 
+// Threads per row of the ring kernel for rows of J chunks per lane, measured
+// per row width and kind of kernel (plain LN and its FP8 copy share one
+// kernel; the NVFP4 copy and the fused gated kernel have their own):
+//   J = 1 (D <= 1024):  fused 64; otherwise 32
+//   J = 2 (D <= 2048):  plain lossless and FP8 64; otherwise 32
+//   J = 3 (D <= 3072):  fused 128; FP8 128 from 32768 rows; otherwise 64
+//   J = 4 (D <= 4096):  plain and FP8 128; otherwise 64
+//   J >= 5:             128
+// One warp per row keeps the high variant's short rows on two shuffle-only
+// trees (plain LN, J <= 2); with more warps it takes the lane two-pass form of
+// longer rows.
+static int ln_tpr(int J, bool fused, bool fp4, bool fp8, bool high, int64_t rows) {
+    const bool plain = !fused && !fp4;
+    switch (J) {
+        case 1: return fused ? 64 : 32;
+        case 2: return plain && (fp8 || !high) ? 64 : 32;
+        case 3: return fused || (plain && fp8 && rows >= 32768) ? 128 : 64;
+        case 4: return plain ? 128 : 64;
+        default: return 128;
+    }
+}
+
 // Row groups of the fused kernel that fit in shared memory in a modulation
 // mode: its stages carry the residual and the update (per token also the
 // gate, and scale and shift where they are not loaded directly); staged
@@ -650,7 +673,7 @@ static int fused_groups(const LnModParams& p, bool high, int mode) {
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     const int J = chunks_per_lane(p.D), nch = p.D / kChunk;
     const int nops = ln_ring_ops(true, mode, J, high);
-    const int tpr = J <= 2 ? 32 : J <= 4 ? 64 : 128;  // as launch_pipe_d chooses
+    const int tpr = ln_tpr(J, true, false, false, high, p.rows);  // as launch_pipe_d chooses
     const int tree = tpr == 32 ? (int)sizeof(TreeAll<32>) : tpr == 64 ? (int)sizeof(TreeAll<64>) : (int)sizeof(TreeAll<128>);
     const int per_group = tree + (2 * nops + (ln_update_one_stage(J) ? 1 : 0)) * kLanes * J * 16;  // + the update's one stage
     const int fixed = (mode == kModStaged ? 2 * LnOps<true, kModStaged, 1, false>::SLOT * nch * 16 : 0) +
@@ -665,7 +688,7 @@ static int fused_groups(const LnModParams& p, bool high, int mode) {
 static int fused_mode(const LnModParams& p, bool high) {
     const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
     if (!staged) return fused_groups(p, high, kModRing) >= 2 ? kModRing : -1;
-    const int cap = chunks_per_lane(p.D) >= 5 ? 4 : 8;  // 512 threads per CTA
+    const int cap = 512 / ln_tpr(chunks_per_lane(p.D), true, false, false, high, p.rows);  // 512 threads per CTA
     const int gs = std::min(fused_groups(p, high, kModStaged), cap);
     const int gl = chunks_per_lane(p.D) >= 5 ? std::min(fused_groups(p, high, kModL1), cap) : 0;
     // the L1 mode's global reads cost more than the staged form's shared ones:
@@ -695,21 +718,29 @@ static cudaError_t launch_pipe_v(const LnModParams& p, bool high, cudaStream_t s
 
 template <bool FUSED, bool FP4>
 static cudaError_t launch_pipe_d(const LnModParams& p, bool high, cudaStream_t s) {
-    // one warp per row up to 2048 elements, two up to 4096 (measured fastest
-    // at 3072: fewer, longer row rounds), four above.  The unfused kernel
-    // without the NVFP4 store takes four warps at 4096 (measured faster there,
-    // most of all with the FP8 copy), and with the FP8 copy also at 3072 on
-    // 32768 rows or more (faster at 65536 rows, slower at 8704).
+    // threads per row from ln_tpr; `if constexpr` keeps each kind of kernel to
+    // the instantiations its table entries name
     constexpr bool kPlain = !FUSED && !FP4;
-    const bool fp8 = p.out_fp8 != nullptr;
-    switch (chunks_per_lane(p.D)) {
-        case 1: return launch_pipe_v<32, 1, 2, FUSED, FP4>(p, high, s);
-        case 2: return launch_pipe_v<32, 2, 2, FUSED, FP4>(p, high, s);
-        case 3:
+    const int J = chunks_per_lane(p.D);
+    const int tpr = ln_tpr(J, FUSED, FP4, p.out_fp8 != nullptr, high, p.rows);
+    switch (J) {
+        case 1:
+            if constexpr (FUSED) return launch_pipe_v<64, 1, 2, FUSED, FP4>(p, high, s);
+            else return launch_pipe_v<32, 1, 2, FUSED, FP4>(p, high, s);
+        case 2:
             if constexpr (kPlain) {
-                if (fp8 && p.rows >= 32768) return launch_pipe_v<128, 3, 2, FUSED, FP4>(p, high, s);
+                if (tpr == 64) return launch_pipe_v<64, 2, 2, FUSED, FP4>(p, high, s);
             }
-            return launch_pipe_v<64, 3, 2, FUSED, FP4>(p, high, s);
+            return launch_pipe_v<32, 2, 2, FUSED, FP4>(p, high, s);
+        case 3:
+            if constexpr (FUSED) {
+                return launch_pipe_v<128, 3, 2, FUSED, FP4>(p, high, s);
+            } else {
+                if constexpr (kPlain) {
+                    if (tpr == 128) return launch_pipe_v<128, 3, 2, FUSED, FP4>(p, high, s);
+                }
+                return launch_pipe_v<64, 3, 2, FUSED, FP4>(p, high, s);
+            }
         case 4:
             if constexpr (kPlain) return launch_pipe_v<128, 4, 2, FUSED, FP4>(p, high, s);
             else return launch_pipe_v<64, 4, 2, FUSED, FP4>(p, high, s);
