@@ -770,6 +770,10 @@ def run_suite(args):
         if "sweep4k" in only.split(","):
             for D in (1024, 3072, 4096, 8192):
                 row_case(f"sweep [4096,{D}]", 1, 4096, D, False)
+        if "sweepmid" in only.split(","):
+            for T in (16384, 32768):
+                for D in (2048, 3072, 4096):
+                    row_case(f"sweep [{T},{D}]", 1, T, D, False)
         return 0
     row_case("tiny [2,256,512]", 2, 256, 512, False)
     row_case("sweep [77,3072]", 1, 77, 3072, False)
@@ -867,7 +871,7 @@ def main():
     ap.add_argument("--impl", default="mbx", choices=["mbx", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only", default=None,
-                    help="with --suite: run only the named groups (tiny, image, video, qkv, sweep, sweep2, sweep4k, table)")
+                    help="with --suite: run only the named groups (tiny, image, video, qkv, sweep, sweep2, sweep4k, sweepmid, table)")
     ap.add_argument("--ops", default=None, help="with --suite: run only the named operations (comma list)")
     ap.add_argument("--suite", action="store_true",
                     help="time every operation and variant on the configurations' shapes "
