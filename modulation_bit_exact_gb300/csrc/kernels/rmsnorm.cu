@@ -512,18 +512,33 @@ static cudaError_t launch_rms_pipe_v(const typename RmsPipeArgs<OP>::P& p, bool 
                   : launch_rms_pipe<TPR, J, NS, false, OP, kRmsModRing>(p, s);
 }
 
+// Threads per row and ring stages, measured per row width, operation and
+// row count: three stages at 2048 and 3072 (and for the tanh op at 8192),
+// two elsewhere; one warp per row
+// up to 2048 elements (two for the tanh op at 2048), two at 3072 and 4096,
+// four above; four warps at 3072 for rmsnorm_scale from 32768 rows and at
+// 4096 from 16384 rows (faster there, slower on fewer rows).
 template <int OP>
 static cudaError_t launch_rms_pipe_d(const typename RmsPipeArgs<OP>::P& p, bool high, cudaStream_t s) {
     switch (chunks_per_lane(p.D)) {
         case 1: return launch_rms_pipe_v<OP, 32, 1, 2>(p, high, s);
-        // three stages measured faster at 2048 and 3072, two elsewhere
-        case 2: return launch_rms_pipe_v<OP, 32, 2, 3>(p, high, s);
-        case 3: return launch_rms_pipe_v<OP, 64, 3, 3>(p, high, s);
-        case 4: return launch_rms_pipe_v<OP, 64, 4, 2>(p, high, s);
+        case 2:
+            if constexpr (OP == kRmsTanh) return launch_rms_pipe_v<OP, 64, 2, 3>(p, high, s);
+            else return launch_rms_pipe_v<OP, 32, 2, 3>(p, high, s);
+        case 3:
+            if constexpr (OP == kRmsScale) {
+                if (p.rows >= 32768) return launch_rms_pipe_v<OP, 128, 3, 3>(p, high, s);
+            }
+            return launch_rms_pipe_v<OP, 64, 3, 3>(p, high, s);
+        case 4:
+            if (p.rows >= 16384) return launch_rms_pipe_v<OP, 128, 4, 2>(p, high, s);
+            return launch_rms_pipe_v<OP, 64, 4, 2>(p, high, s);
         case 5: return launch_rms_pipe_v<OP, 128, 5, 2>(p, high, s);
         case 6: return launch_rms_pipe_v<OP, 128, 6, 2>(p, high, s);
         case 7: return launch_rms_pipe_v<OP, 128, 7, 2>(p, high, s);
-        case 8: return launch_rms_pipe_v<OP, 128, 8, 2>(p, high, s);
+        case 8:
+            if constexpr (OP == kRmsTanh) return launch_rms_pipe_v<OP, 128, 8, 3>(p, high, s);
+            else return launch_rms_pipe_v<OP, 128, 8, 2>(p, high, s);
         default: return cudaErrorInvalidValue;
     }
 }
