@@ -647,17 +647,19 @@ static cudaError_t launch_pipe(const LnModParams& p, cudaStream_t s) {
 //   J = 2 (D <= 2048):  plain lossless and FP8 64; otherwise 32
 //   J = 3 (D <= 3072):  fused 128; FP8 128 from 32768 rows; otherwise 64
 //   J = 4 (D <= 4096):  plain and FP8 128; otherwise 64
-//   J >= 5:             128
+//   J = 5 (D <= 5120):  fused high with per-row modulation 64; otherwise 128
+//   J >= 6:             128
 // One warp per row keeps the high variant's short rows on two shuffle-only
 // trees (plain LN, J <= 2); with more warps it takes the lane two-pass form of
-// longer rows.
-static int ln_tpr(int J, bool fused, bool fp4, bool fp8, bool high, int64_t rows) {
+// longer rows.  `ring`: each row reads its own modulation row (kModRing).
+static int ln_tpr(int J, bool fused, bool fp4, bool fp8, bool high, int64_t rows, bool ring) {
     const bool plain = !fused && !fp4;
     switch (J) {
         case 1: return fused ? 64 : 32;
         case 2: return plain && (fp8 || !high) ? 64 : 32;
         case 3: return fused || (plain && fp8 && rows >= 32768) ? 128 : 64;
         case 4: return plain ? 128 : 64;
+        case 5: return fused && !fp4 && high && ring ? 64 : 128;
         default: return 128;
     }
 }
@@ -673,7 +675,7 @@ static int fused_groups(const LnModParams& p, bool high, int mode) {
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     const int J = chunks_per_lane(p.D), nch = p.D / kChunk;
     const int nops = ln_ring_ops(true, mode, J, high);
-    const int tpr = ln_tpr(J, true, false, false, high, p.rows);  // as launch_pipe_d chooses
+    const int tpr = ln_tpr(J, true, false, false, high, p.rows, mode == kModRing);  // as launch_pipe_d chooses
     const int tree = tpr == 32 ? (int)sizeof(TreeAll<32>) : tpr == 64 ? (int)sizeof(TreeAll<64>) : (int)sizeof(TreeAll<128>);
     const int per_group = tree + (2 * nops + (ln_update_one_stage(J) ? 1 : 0)) * kLanes * J * 16;  // + the update's one stage
     const int fixed = (mode == kModStaged ? 2 * LnOps<true, kModStaged, 1, false>::SLOT * nch * 16 : 0) +
@@ -688,7 +690,7 @@ static int fused_groups(const LnModParams& p, bool high, int mode) {
 static int fused_mode(const LnModParams& p, bool high) {
     const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
     if (!staged) return fused_groups(p, high, kModRing) >= 2 ? kModRing : -1;
-    const int cap = 512 / ln_tpr(chunks_per_lane(p.D), true, false, false, high, p.rows);  // 512 threads per CTA
+    const int cap = 512 / ln_tpr(chunks_per_lane(p.D), true, false, false, high, p.rows, false);  // 512 threads per CTA
     const int gs = std::min(fused_groups(p, high, kModStaged), cap);
     const int gl = chunks_per_lane(p.D) >= 5 ? std::min(fused_groups(p, high, kModL1), cap) : 0;
     // the L1 mode's global reads cost more than the staged form's shared ones:
@@ -722,7 +724,8 @@ static cudaError_t launch_pipe_d(const LnModParams& p, bool high, cudaStream_t s
     // the instantiations its table entries name
     constexpr bool kPlain = !FUSED && !FP4;
     const int J = chunks_per_lane(p.D);
-    const int tpr = ln_tpr(J, FUSED, FP4, p.out_fp8 != nullptr, high, p.rows);
+    const bool ring = pipe_rows_per_cta(p.rows) > p.seq;  // as launch_pipe_v decides
+    const int tpr = ln_tpr(J, FUSED, FP4, p.out_fp8 != nullptr, high, p.rows, ring);
     switch (J) {
         case 1:
             if constexpr (FUSED) return launch_pipe_v<64, 1, 2, FUSED, FP4>(p, high, s);
@@ -744,7 +747,11 @@ static cudaError_t launch_pipe_d(const LnModParams& p, bool high, cudaStream_t s
         case 4:
             if constexpr (kPlain) return launch_pipe_v<128, 4, 2, FUSED, FP4>(p, high, s);
             else return launch_pipe_v<64, 4, 2, FUSED, FP4>(p, high, s);
-        case 5: return launch_pipe_v<128, 5, 2, FUSED, FP4>(p, high, s);
+        case 5:
+            if constexpr (FUSED && !FP4) {
+                if (tpr == 64) return launch_pipe<64, 5, 2, true, kModRing, FUSED, FP4>(p, s);
+            }
+            return launch_pipe_v<128, 5, 2, FUSED, FP4>(p, high, s);
         case 6: return launch_pipe_v<128, 6, 2, FUSED, FP4>(p, high, s);
         case 7: return launch_pipe_v<128, 7, 2, FUSED, FP4>(p, high, s);
         case 8:
