@@ -5,9 +5,10 @@ size, every element compared.
 Each D takes its own instantiation of the ring kernel (chunks per lane J =
 D / 1024), so these cells cover every row-block and ring-round boundary the
 production sizes reach.  Lossless: every bf16, E4M3, E2M1 and block-scale byte
-equals the oracle's.  High: r' is exact, the norm is within 2 bfloat16 ulps of
-the binary64 LN + modulate of the oracle's r', and the FP8 / NVFP4 copies are
-the quantisation of the bf16 output the kernel wrote (PyTorch float8 witness
+equals the oracle's.  High: r' is exact, every bf16 output (plain and gated,
+of the FP8 and NVFP4 producers too, which may split rows otherwise than the
+plain LN) is within 2 bfloat16 ulps of the binary64 LN + modulate, and the
+FP8 / NVFP4 copies are the quantisation of the bf16 output the kernel wrote (PyTorch float8 witness
 for E4M3, a decode within one E2M1 half-step for NVFP4).  The oracle runs on
 every host core (gpu_util.par_rows).
 """
@@ -124,6 +125,10 @@ def test_fp8_producers(mbx, D):
         want = oracle.ln_modulate(h["X"][lo:hi], h["SC"], h["SH"], 1e-6)
         assert_bits_equal(ln["lossless"][0][lo:hi], want, "ln bf16 " + what)
         assert_bits_equal(ln["lossless"][1][lo:hi], oracle.quant_e4m3(want, FP8_SCALE), "ln e4m3 " + what)
+        # the FP8 producer may run another row split than the plain LN (threads
+        # per row, stages): its bf16 output is held to the high bound on its own
+        assert_high_close(ln["high"][0][lo:hi], *oracle.ln_modulate_f64(h["X"][lo:hi], h["SC"], h["SH"], 1e-6),
+                          what="ln bf16 (high) " + what)
         _fp8_consistent(ln["high"][0][lo:hi], ln["high"][1][lo:hi], FP8_SCALE)
         wr, wo = oracle.gated_residual_ln_modulate(h["R"][lo:hi], h["G"], h["U"][lo:hi], h["B"], h["SC"],
                                                    h["SH"], 1e-6)
@@ -131,6 +136,8 @@ def test_fp8_producers(mbx, D):
         assert_bits_equal(gated["lossless"][1][lo:hi], wo, "gated bf16 " + what)
         assert_bits_equal(gated["lossless"][2][lo:hi], oracle.quant_e4m3(wo, FP8_SCALE), "gated e4m3 " + what)
         assert_bits_equal(gated["high"][0][lo:hi], wr, "gated residual (high) " + what)
+        assert_high_close(gated["high"][1][lo:hi], *oracle.ln_modulate_f64(wr, h["SC"], h["SH"], 1e-6),
+                          what="gated bf16 (high) " + what)
         _fp8_consistent(gated["high"][1][lo:hi], gated["high"][2][lo:hi], FP8_SCALE)
 
     par_rows(chk, T)
@@ -158,6 +165,8 @@ def test_nvfp4_producers(mbx, D):
         assert_bits_equal(q[lo:hi], wq, "ln e2m1 " + what)
         assert_bits_equal(_sf_chunk(sf, lo, hi, D), wsf, "ln block scales " + what)
         o, q, sf = ln["high"]
+        assert_high_close(o[lo:hi], *oracle.ln_modulate_f64(h["X"][lo:hi], h["SC"], h["SH"], 1e-6),
+                          what="ln bf16 (high) " + what)
         _nvfp4_decode_close(o[lo:hi], q[lo:hi], _sf_chunk(sf, lo, hi, D), GS)
         wr, wo = oracle.gated_residual_ln_modulate(h["R"][lo:hi], h["G"], h["U"][lo:hi], h["B"], h["SC"],
                                                    h["SH"], 1e-6)
@@ -169,6 +178,8 @@ def test_nvfp4_producers(mbx, D):
         assert_bits_equal(_sf_chunk(sf, lo, hi, D), wsf, "gated block scales " + what)
         r, o, q, sf = gated["high"]
         assert_bits_equal(r[lo:hi], wr, "gated residual (high) " + what)
+        assert_high_close(o[lo:hi], *oracle.ln_modulate_f64(wr, h["SC"], h["SH"], 1e-6),
+                          what="gated bf16 (high) " + what)
         _nvfp4_decode_close(o[lo:hi], q[lo:hi], _sf_chunk(sf, lo, hi, D), GS)
 
     par_rows(chk, T, align=128)
