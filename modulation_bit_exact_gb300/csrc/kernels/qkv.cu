@@ -22,6 +22,8 @@
 // rstd = bf16(1/sqrt(bf16(ms+eps))), n = bf16(bf16(x*rstd)*w)), then for each
 // pair (2i, 2i+1): o0 = bf16(n0*c - n1*s), o1 = bf16(n0*s + n1*c) in binary32
 // with c, s the token's table entries for pair i.  V is a bit copy.
+#include <type_traits>
+
 #include "launch.h"
 #include "rowops.cuh"
 #include "rstd_bf16_table.inc"
@@ -51,30 +53,35 @@ __device__ __forceinline__ float rstd_bf16(float inner) {
 }
 
 // One unit of work: the heads [hp*slots, hp*slots + slots) of one token.
+// Index arithmetic in I: 32-bit unsigned when every element offset of the
+// call fits (the launcher checks), else 64-bit.
+template <class I>
 struct QkvUnit {
-    int64_t b, s, sb;
+    I b, s, sb;
     bool txt;
     const uint16_t* src;
     const float* cos_row;
     const float* sin_row;
 };
 
-template <int HD>
-__device__ __forceinline__ QkvUnit qkv_unit(const QkvParams& p, int64_t tok) {
-    QkvUnit u;
-    const int64_t s_tot = p.s_txt + p.s_img;
-    u.b = fast_div((unsigned)tok, p.by_stot);
+template <int HD, class I>
+__device__ __forceinline__ QkvUnit<I> qkv_unit(const QkvParams& p, I tok) {
+    QkvUnit<I> u;
+    const I s_txt = (I)p.s_txt, s_tot = (I)(p.s_txt + p.s_img);
+    u.b = (I)fast_div((unsigned)tok, p.by_stot);
     u.s = tok - u.b * s_tot;  // position in the joint sequence
-    u.txt = u.s < p.s_txt;
-    u.sb = u.txt ? u.s : u.s - p.s_txt;  // position within the branch
-    u.src = u.txt ? p.txt + (u.b * p.s_txt + u.sb) * p.txt_stride : p.img + (u.b * p.s_img + u.sb) * p.img_stride;
-    u.cos_row = (u.txt ? p.cos_txt : p.cos_img) + u.sb * (HD / 2);
-    u.sin_row = (u.txt ? p.sin_txt : p.sin_img) + u.sb * (HD / 2);
+    u.txt = u.s < s_txt;
+    u.sb = u.txt ? u.s : u.s - s_txt;  // position within the branch
+    u.src = u.txt ? p.txt + (u.b * s_txt + u.sb) * (I)p.txt_stride
+                  : p.img + (u.b * (I)p.s_img + u.sb) * (I)p.img_stride;
+    u.cos_row = (u.txt ? p.cos_txt : p.cos_img) + u.sb * (I)(HD / 2);
+    u.sin_row = (u.txt ? p.sin_txt : p.sin_img) + u.sb * (I)(HD / 2);
     return u;
 }
 
-template <int TPH, bool HIGH>
+template <int TPH, bool HIGH, bool I32>
 __global__ void __launch_bounds__(512) qkv_epilogue_kernel(QkvParams p) {
+    using I = typename std::conditional<I32, uint32_t, int64_t>::type;
     grid_dep_wait();  // launched programmatically: the previous kernel has finished
     grid_dep_launch();
     constexpr int HD = TPH * kChunk;
@@ -82,23 +89,23 @@ __global__ void __launch_bounds__(512) qkv_epilogue_kernel(QkvParams p) {
     const int slot = threadIdx.x / TPH;  // head unit within the CTA
     const int slots = blockDim.x / TPH;
     const int H = p.heads;
-    const int64_t s_tot = p.s_txt + p.s_img;
+    const I s_tot = (I)(p.s_txt + p.s_img);
     const int hpasses = p.hpasses;
-    const int64_t units = p.batch * s_tot * hpasses;
-    const int64_t part_stride = (int64_t)H * HD;  // columns between Q, K and V
+    const int64_t units = p.batch * (p.s_txt + p.s_img) * hpasses;
+    const I part_stride = (I)H * HD;  // columns between Q, K and V
 
     // software pipeline: the next unit's chunks and table entries are in
     // flight while the current one is computed
     uint4 nx[3];
     float4 nc, ns;
     auto fetch = [&](int64_t unit) {
-        const int64_t tok = hpasses == 1 ? unit : fast_div((unsigned)unit, p.by_hpass);
-        const int hp = (int)(unit - tok * hpasses);
-        const QkvUnit u = qkv_unit<HD>(p, tok);
+        const I tok = hpasses == 1 ? (I)unit : (I)fast_div((unsigned)unit, p.by_hpass);
+        const int hp = (int)((I)unit - tok * (I)hpasses);
+        const QkvUnit<I> u = qkv_unit<HD, I>(p, tok);
         const int h = hp * slots + slot;
 #pragma unroll
         for (int part = 0; part < 3; ++part)
-            nx[part] = h < H ? ld_stream(u.src + part * part_stride + (int64_t)h * HD + l * kChunk)
+            nx[part] = h < H ? ld_stream(u.src + ((I)part * part_stride + (I)h * HD + (I)(l * kChunk)))
                              : make_uint4(0, 0, 0, 0);
         nc = ld_f4(u.cos_row + 4 * l);
         ns = ld_f4(u.sin_row + 4 * l);
@@ -110,13 +117,13 @@ __global__ void __launch_bounds__(512) qkv_epilogue_kernel(QkvParams p) {
         const float4 c4 = nc, s4 = ns;
         if (unit + gridDim.x < units) fetch(unit + gridDim.x);
 
-        const int64_t tok = hpasses == 1 ? unit : fast_div((unsigned)unit, p.by_hpass);
-        const int hp = (int)(unit - tok * hpasses);
-        const QkvUnit u = qkv_unit<HD>(p, tok);
+        const I tok = hpasses == 1 ? (I)unit : (I)fast_div((unsigned)unit, p.by_hpass);
+        const int hp = (int)((I)unit - tok * (I)hpasses);
+        const QkvUnit<I> u = qkv_unit<HD, I>(p, tok);
         const int h = hp * slots + slot;
         const bool active = h < H;
-        uint16_t* const dst_q = p.joint + ((((u.b * 3) * H + h) * s_tot + u.s) * HD) + l * kChunk;
-        const int64_t part_out = (int64_t)H * s_tot * HD;  // between the Q, K and V planes
+        uint16_t* const dst_q = p.joint + (((((u.b * 3) * (I)H + (I)h) * s_tot + u.s) * (I)HD) + (I)(l * kChunk));
+        const I part_out = (I)H * s_tot * (I)HD;  // between the Q, K and V planes
         if (active) st_v4(dst_q + 2 * part_out, xv);  // V: bit copy
 
         const uint4 wq = ld_shared_row((u.txt ? p.wq_txt : p.wq_img) + l * kChunk);
@@ -185,9 +192,23 @@ __global__ void __launch_bounds__(512) qkv_epilogue_kernel(QkvParams p) {
     }
 }
 
-template <int TPH, bool HIGH>
+// Whether every element offset the kernel forms fits in 32 bits: the joint
+// buffer, and each branch's rows (last row start plus the Q, K, V columns).
+static bool qkv_fits_32(const QkvParams& p) {
+    const int64_t lim = (int64_t)1 << 32;
+    const int64_t s_tot = p.s_txt + p.s_img, cols = 3 * (int64_t)p.heads * p.head_dim;
+    if (p.batch * 3 * p.heads * s_tot * p.head_dim >= lim) return false;
+    for (int t = 0; t < 2; ++t) {
+        const int64_t rows = p.batch * (t == 0 ? p.s_txt : p.s_img), stride = t == 0 ? p.txt_stride : p.img_stride;
+        if (rows > 0 && (rows - 1) * stride + cols >= lim) return false;
+        if (rows * stride >= lim) return false;  // the row-start product itself
+    }
+    return true;
+}
+
+template <int TPH, bool HIGH, bool I32>
 static cudaError_t launch_one(const QkvParams& p0, cudaStream_t s) {
-    auto k = qkv_epilogue_kernel<TPH, HIGH>;
+    auto k = qkv_epilogue_kernel<TPH, HIGH, I32>;
     int slots = p0.heads < 512 / TPH ? (int)p0.heads : 512 / TPH;
     int block = slots * TPH;
     if (block % 32) block += 32 - block % 32;  // whole warps (extra units idle)
@@ -203,11 +224,17 @@ static cudaError_t launch_one(const QkvParams& p0, cudaStream_t s) {
     return launch_pdl(k, grid, block, 0, s, p);
 }
 
+template <int TPH>
+static cudaError_t launch_hd(const QkvParams& p, bool high, cudaStream_t s) {
+    if (qkv_fits_32(p)) return high ? launch_one<TPH, true, true>(p, s) : launch_one<TPH, false, true>(p, s);
+    return high ? launch_one<TPH, true, false>(p, s) : launch_one<TPH, false, false>(p, s);
+}
+
 cudaError_t launch_qkv_epilogue(const QkvParams& p, bool high, cudaStream_t s) {
     switch (p.head_dim) {
-        case 64: return high ? launch_one<8, true>(p, s) : launch_one<8, false>(p, s);
-        case 128: return high ? launch_one<16, true>(p, s) : launch_one<16, false>(p, s);
-        case 256: return high ? launch_one<32, true>(p, s) : launch_one<32, false>(p, s);
+        case 64: return launch_hd<8>(p, high, s);
+        case 128: return launch_hd<16>(p, high, s);
+        case 256: return launch_hd<32>(p, high, s);
         default: return cudaErrorInvalidValue;
     }
 }
