@@ -84,6 +84,25 @@ def test_qkv_epilogue_full_size(mbx):
     assert_bits_equal(u16(_qkv_gpu(mbx, q)), _qkv_oracle(q), "joint")
 
 
+def test_qkv_epilogue_offsets_past_32_bits(mbx):
+    """Text rows 2^31 elements apart: the source offsets pass 2^32, so the
+    call takes the 64-bit index form (8.6 GB of address space, three rows
+    written); bit-exact like the 32-bit form."""
+    q = synth.qkv_epilogue_case(batch=1, s_txt=3, grid_h=4, grid_w=4, heads=2, head_dim=64)
+    width = q["txt"].shape[1]
+    stride = 2 ** 31
+    big = torch.empty(2 * stride + width, dtype=torch.bfloat16, device=DEV)
+    txt = torch.as_strided(big, (3, width), (stride, 1))
+    txt.copy_(q["txt"].to(DEV))
+    qd = {k: (v.to(DEV) if torch.is_tensor(v) else v) for k, v in q.items()}
+    out = mbx.qk_norm_rope_qkv_epilogue(
+        txt, qd["img"], q["batch"], q["heads"], q["head_dim"], qd["wq_txt"], qd["wk_txt"], qd["wq_img"],
+        qd["wk_img"], qd["cos_txt"], qd["sin_txt"], qd["cos_img"], qd["sin_img"], q["eps"])
+    assert_bits_equal(u16(out), _qkv_oracle(q), "joint (64-bit offsets)")
+    del big, txt, out
+    torch.cuda.empty_cache()
+
+
 def _qkv_high_check(mbx, q):
     got = u16(_qkv_gpu(mbx, q, variant="high"))
     want = _qkv_oracle(q)
