@@ -517,9 +517,12 @@ static cudaError_t launch_rms_pipe_v(const typename RmsPipeArgs<OP>::P& p, bool 
 // two elsewhere; one warp per row
 // up to 2048 elements (two for the tanh op at 2048), two at 3072 and 4096,
 // four above; four warps at 3072 for rmsnorm_scale from 32768 rows and at
-// 4096 from 16384 rows (faster there, slower on fewer rows).
+// 4096 from 16384 rows (faster there, slower on fewer rows); two warps for
+// lossless rmsnorm_scale with per-sample modulation at 5120, 6144 and 8192
+// (+2..4%; the high variant is slower with two).
 template <int OP>
 static cudaError_t launch_rms_pipe_d(const typename RmsPipeArgs<OP>::P& p, bool high, cudaStream_t s) {
+    const bool staged_lossless = !high && pipe_rows_per_cta(p.rows) <= p.seq;
     switch (chunks_per_lane(p.D)) {
         case 1: return launch_rms_pipe_v<OP, 32, 1, 2>(p, high, s);
         case 2:
@@ -533,12 +536,24 @@ static cudaError_t launch_rms_pipe_d(const typename RmsPipeArgs<OP>::P& p, bool 
         case 4:
             if (p.rows >= 16384) return launch_rms_pipe_v<OP, 128, 4, 2>(p, high, s);
             return launch_rms_pipe_v<OP, 64, 4, 2>(p, high, s);
-        case 5: return launch_rms_pipe_v<OP, 128, 5, 2>(p, high, s);
-        case 6: return launch_rms_pipe_v<OP, 128, 6, 2>(p, high, s);
+        case 5:
+            if constexpr (OP == kRmsScale) {
+                if (staged_lossless) return launch_rms_pipe<64, 5, 2, false, OP, kRmsModStaged>(p, s);
+            }
+            return launch_rms_pipe_v<OP, 128, 5, 2>(p, high, s);
+        case 6:
+            if constexpr (OP == kRmsScale) {
+                if (staged_lossless) return launch_rms_pipe<64, 6, 2, false, OP, kRmsModStaged>(p, s);
+            }
+            return launch_rms_pipe_v<OP, 128, 6, 2>(p, high, s);
         case 7: return launch_rms_pipe_v<OP, 128, 7, 2>(p, high, s);
         case 8:
-            if constexpr (OP == kRmsTanh) return launch_rms_pipe_v<OP, 128, 8, 3>(p, high, s);
-            else return launch_rms_pipe_v<OP, 128, 8, 2>(p, high, s);
+            if constexpr (OP == kRmsTanh) {
+                return launch_rms_pipe_v<OP, 128, 8, 3>(p, high, s);
+            } else {
+                if (staged_lossless) return launch_rms_pipe<64, 8, 2, false, OP, kRmsModStaged>(p, s);
+                return launch_rms_pipe_v<OP, 128, 8, 2>(p, high, s);
+            }
         default: return cudaErrorInvalidValue;
     }
 }
