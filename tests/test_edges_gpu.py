@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import synth
-from tests.gpu_util import assert_bits_equal, guarded, u16
+from tests.gpu_util import assert_bits_equal, assert_high_close, guarded, u16
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -236,6 +236,28 @@ def test_device_rejections(mbx):
                                  ctypes.byref(mbx._view(sc)), ctypes.byref(mbx._view(sc)),
                                  ctypes.c_float(1e-6), 0)
     assert st == 0
+
+
+@pytest.mark.parametrize("D,rows", [(2048, 1200), (4096, 1200), (6144, 600), (8192, 600), (4096, 16384),
+                                    (3072, 32768)])
+def test_per_token_modulation_every_width(mbx, D, rows):
+    """Per-token modulation (each row reads its own modulation row) at the
+    widths and row counts where the ring kernels change threads per row or
+    stages: the plain, FP8 and RMSNorm kernels on their per-row path, both
+    variants."""
+    t = _inputs(rows, D, rows, seed=D + rows)
+    _all_ops(mbx, t)
+    v = {k: a.to(DEV) for k, a in t.items()}
+    U = {k: u16(a) for k, a in t.items()}
+    want = oracle.ln_modulate(U["x"], U["sc"], U["sh"], 1e-6)
+    s8 = torch.tensor([0.02], dtype=torch.float32, device=DEV)
+    out, q = mbx.ln_modulate_fp8(v["x"], v["sc"], v["sh"], s8)
+    assert_bits_equal(u16(out), want, "fp8 ln bf16")
+    assert_bits_equal(q.view(torch.uint8).cpu().numpy(), oracle.quant_e4m3(want, 0.02), "fp8 ln e4m3")
+    ex, mag = oracle.ln_modulate_f64(U["x"], U["sc"], U["sh"], 1e-6)
+    assert_high_close(u16(mbx.ln_modulate(v["x"], v["sc"], v["sh"], variant="high")), ex, mag, what="ln high")
+    out_h, _ = mbx.ln_modulate_fp8(v["x"], v["sc"], v["sh"], s8, variant="high")
+    assert_high_close(u16(out_h), ex, mag, what="fp8 ln high")
 
 
 @pytest.mark.parametrize("rows,mrows,D", [(4096, 512, 1024), (6000, 3000, 3072), (2048, 1024, 5120)])
