@@ -117,7 +117,7 @@ def test_shapes(mbx, batch, seq, D):
     _check(mbx, _case(batch, seq, D), f"B={batch} S={seq} D={D}")
 
 
-@pytest.mark.parametrize("D", [1024, 5120])
+@pytest.mark.parametrize("D", [1024, 2048, 3072, 4096, 5120, 6144, 8192])
 def test_per_token(mbx, D):
     _check(mbx, _case(1, 300, D, per_token=True), f"per-token D={D}")
 
