@@ -79,7 +79,9 @@ def test_ln_modulate_nvfp4_image_dit(mbx):
 
 
 @pytest.mark.parametrize("D,rows,mrows,shift", [(1024, 300, 3, 0), (5120, 97, 97, 0), (8192, 40, 40, 0),
-                                                (2048, 64, 2, 1), (64, 129, 1, 0), (48, 7, 7, 0)])
+                                                (2048, 64, 2, 1), (64, 129, 1, 0), (48, 7, 7, 0),
+                                                (2048, 256, 256, 0), (3072, 300, 300, 0), (4096, 200, 200, 0),
+                                                (6144, 100, 100, 0)])
 def test_ln_modulate_nvfp4_shapes(mbx, D, rows, mrows, shift):
     """Staged and per-token modulation, rows that do not fill a 128-row tile,
     D = 48 (blocks padded to 4), a misaligned view (the separate quantiser)."""
@@ -113,6 +115,25 @@ def test_gated_nvfp4(mbx, bias, D):
                                                            bias=None if b is None else b.to(DEV))
     want_r, want_o = oracle.gated_residual_ln_modulate(u16(r), u16(gt), u16(u), None if b is None else u16(b),
                                                        u16(sc), u16(sh), 1e-6)
+    assert_bits_equal(u16(res), want_r, "residual")
+    assert_bits_equal(u16(out), want_o, "bf16")
+    _check_lossless(q, sf, want_o, gs)
+
+
+@pytest.mark.parametrize("D", [1024, 3072, 5120])
+def test_gated_nvfp4_per_token(mbx, D):
+    """Per-token gate, scale and shift: the fused kernel's per-row path (its
+    threads per row differ by width)."""
+    g = torch.Generator().manual_seed(11 + D)
+    rows = 300
+    r = torch.randn(rows, D, generator=g).to(BF16)
+    u = torch.randn(rows, D, generator=g).to(BF16)
+    gt, sc, sh = ((0.1 * torch.randn(rows, D, generator=g)).to(BF16) for _ in range(3))
+    b = (0.5 * torch.randn(1, D, generator=g)).to(BF16)
+    gs = 300.0
+    res, out, q, sf = mbx.gated_residual_ln_modulate_nvfp4(r.to(DEV), gt.to(DEV), u.to(DEV), sc.to(DEV),
+                                                           sh.to(DEV), _gs(gs), bias=b.to(DEV))
+    want_r, want_o = oracle.gated_residual_ln_modulate(u16(r), u16(gt), u16(u), u16(b), u16(sc), u16(sh), 1e-6)
     assert_bits_equal(u16(res), want_r, "residual")
     assert_bits_equal(u16(out), want_o, "bf16")
     _check_lossless(q, sf, want_o, gs)
