@@ -109,6 +109,28 @@ def test_gated_fp8(mbx, bias, D):
     _self_consistent(out_h, q_h, 0.02)
 
 
+@pytest.mark.parametrize("D", [1024, 3072, 5120])
+def test_gated_fp8_per_token(mbx, D):
+    """Per-token gate, scale and shift (the fused kernel's per-row path, whose
+    threads per row differ by width and, at 5120, by variant)."""
+    g = torch.Generator().manual_seed(23 + D)
+    rows = 300
+    r = torch.randn(rows, D, generator=g).to(BF16)
+    u = torch.randn(rows, D, generator=g).to(BF16)
+    gt, sc, sh = ((0.1 * torch.randn(rows, D, generator=g)).to(BF16) for _ in range(3))
+    args = (r.to(DEV), gt.to(DEV), u.to(DEV), sc.to(DEV), sh.to(DEV), _scale(0.02))
+    res, out, q = mbx.gated_residual_ln_modulate_fp8(*args)
+    want_r, want_o = oracle.gated_residual_ln_modulate(u16(r), u16(gt), u16(u), None, u16(sc), u16(sh), 1e-6)
+    assert_bits_equal(u16(res), want_r, "residual")
+    assert_bits_equal(u16(out), want_o, "bf16")
+    assert_bits_equal(_b8(q), oracle.quant_e4m3(want_o, 0.02), "e4m3")
+    res_h, out_h, q_h = mbx.gated_residual_ln_modulate_fp8(*args, variant="high")
+    assert_bits_equal(u16(res_h), want_r, "residual (high)")
+    ex, mag = oracle.ln_modulate_f64(want_r, u16(sc), u16(sh), 1e-6)
+    assert_high_close(u16(out_h), ex, mag, what="bf16 (high)")
+    _self_consistent(out_h, q_h, 0.02)
+
+
 def test_scale_is_read_on_the_stream(mbx):
     """The scale is a device value read when the kernel runs: updating it in
     place between two calls changes the second result, with no sync."""
