@@ -233,7 +233,7 @@ cudaError_t launch_gated_add_part(const LnModParams& p, bool vec, cudaStream_t s
 }
 
 cudaError_t launch_gated_residual_ln_modulate(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
-    if (vec && fused_fits(p, high)) return launch_pipe_d<true, false>(p, high, s);
+    if (vec && fused_fits(p, high, false)) return launch_pipe_d<true, false>(p, high, s);
     // unaligned or ragged rows, or rows too wide for the fused ring: the same
     // definition as two steps, the gated residual into res_out, then
     // LayerNorm + modulate of res_out
@@ -270,7 +270,7 @@ cudaError_t launch_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cu
 }
 
 cudaError_t launch_gated_residual_ln_modulate_fp8(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
-    if (vec && fused_fits(p, high)) return launch_pipe_d<true, false>(p, high, s);
+    if (vec && fused_fits(p, high, false)) return launch_pipe_d<true, false>(p, high, s);
     if (vec) return launch_gated_residual_ln_modulate(p, true, high, s);  // composed; the LN pass writes the FP8 copy
     return launch_all_or_none([&]() {
         LnModParams q = p;

@@ -39,7 +39,7 @@ cudaError_t launch_ln_modulate_nvfp4(const LnModParams& p, bool vec, bool high, 
 }
 
 cudaError_t launch_gated_residual_ln_modulate_nvfp4(const LnModParams& p, bool vec, bool high, cudaStream_t s) {
-    if (vec && fused_fits(p, high)) return launch_pipe_d<true, true>(p, high, s);
+    if (vec && fused_fits(p, high, true)) return launch_pipe_d<true, true>(p, high, s);
     if (vec) {  // rows too wide for the fused ring: gated add, then the NVFP4 LN pass
         return launch_all_or_none([&]() {
             LnModParams q;

@@ -669,13 +669,13 @@ static int ln_tpr(int J, bool fused, bool fp4, bool fp8, bool high, int64_t rows
 // gate, and scale and shift where they are not loaded directly); staged
 // per-sample modulation, gate and bias take a fixed share.  Same arithmetic
 // as launch_pipe.
-static int fused_groups(const LnModParams& p, bool high, int mode) {
+static int fused_groups(const LnModParams& p, bool high, int mode, bool fp4) {
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     const int J = chunks_per_lane(p.D), nch = p.D / kChunk;
     const int nops = ln_ring_ops(true, mode, J, high);
-    const int tpr = ln_tpr(J, true, false, false, high, p.rows, mode == kModRing);  // as launch_pipe_d chooses
+    const int tpr = ln_tpr(J, true, fp4, false, high, p.rows, mode == kModRing);  // as launch_pipe_d chooses
     const int tree = tpr == 32 ? (int)sizeof(TreeAll<32>) : tpr == 64 ? (int)sizeof(TreeAll<64>) : (int)sizeof(TreeAll<128>);
     const int per_group = tree + (2 * nops + (ln_update_one_stage(J) ? 1 : 0)) * kLanes * J * 16;  // + the update's one stage
     const int fixed = (mode == kModStaged ? 2 * LnOps<true, kModStaged, 1, false>::SLOT * nch * 16 : 0) +
@@ -687,19 +687,20 @@ static int fused_groups(const LnModParams& p, bool high, int mode) {
 // row groups per SM (then two launches, gated add and LN, run faster).
 // Per-sample rows stage their vectors unless reading them from L1 fits at
 // least twice the row groups (rows of more than 4096 elements).
-static int fused_mode(const LnModParams& p, bool high) {
+static int fused_mode(const LnModParams& p, bool high, bool fp4) {
     const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
-    if (!staged) return fused_groups(p, high, kModRing) >= 2 ? kModRing : -1;
-    const int cap = 512 / ln_tpr(chunks_per_lane(p.D), true, false, false, high, p.rows, false);  // 512 threads per CTA
-    const int gs = std::min(fused_groups(p, high, kModStaged), cap);
-    const int gl = chunks_per_lane(p.D) >= 5 ? std::min(fused_groups(p, high, kModL1), cap) : 0;
+    if (!staged) return fused_groups(p, high, kModRing, fp4) >= 2 ? kModRing : -1;
+    const int cap = 512 / ln_tpr(chunks_per_lane(p.D), true, fp4, false, high, p.rows, false);  // 512 threads per CTA
+    const int gs = std::min(fused_groups(p, high, kModStaged, fp4), cap);
+    const int gl = chunks_per_lane(p.D) >= 5 ? std::min(fused_groups(p, high, kModL1, fp4), cap) : 0;
     // the L1 mode's global reads cost more than the staged form's shared ones:
     // taken where it fits at least twice the row groups (measured)
     if (gs >= 2 && gl < 2 * gs) return kModStaged;
     return gl >= 2 ? kModL1 : -1;
 }
 
-static bool fused_fits(const LnModParams& p, bool high) { return fused_mode(p, high) >= 0; }
+// fp4: the kernel with the NVFP4 store (its threads per row may differ)
+static bool fused_fits(const LnModParams& p, bool high, bool fp4) { return fused_mode(p, high, fp4) >= 0; }
 
 template <int TPR, int J, int NS, bool FUSED, bool FP4>
 static cudaError_t launch_pipe_v(const LnModParams& p, bool high, cudaStream_t s) {
@@ -707,7 +708,7 @@ static cudaError_t launch_pipe_v(const LnModParams& p, bool high, cudaStream_t s
     // samples (rows per CTA <= seq); otherwise read it per row
     const bool staged = pipe_rows_per_cta(p.rows) <= p.seq;
     if constexpr (FUSED && J >= 5) {
-        if (staged && fused_mode(p, high) == kModL1)
+        if (staged && fused_mode(p, high, FP4) == kModL1)
             return high ? launch_pipe<TPR, J, NS, true, kModL1, FUSED, FP4>(p, s)
                         : launch_pipe<TPR, J, NS, false, kModL1, FUSED, FP4>(p, s);
     }
